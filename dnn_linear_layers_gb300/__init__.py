@@ -1,15 +1,8 @@
 """GB300 (sm_103a) tiled GEMM / Linear-layer library.
 
-The compute path is the C-ABI shared library built from ``csrc/`` (see
-``include/gemm.h``); ``gemm`` is its thin ctypes binding.  Importing the
-package does not load the library; the first call into ``gemm`` does, and
+The compute path is the C-ABI shared library built from ``csrc/`` (declared
+in ``include/gemm.h``); ``dnn_linear_layers_gb300.gemm`` is its thin ctypes
+binding.  The library is loaded on the first call into the binding, which
 raises if it has not been built.
 """
-__all__ = ["gemm", "inputs", "roofline"]
-
-
-def __getattr__(name):
-    if name == "gemm":
-        from . import gemm as _g
-        return _g
-    raise AttributeError(name)
+__all__ = ["gemm", "inputs", "roofline", "build"]

@@ -1,0 +1,353 @@
+// C-ABI layer: plans, argument validation, TMA tensor maps, operand packing
+// and kernel dispatch.  The interface mirrors the BLAS GEMM call of
+// youngju.dev "GEMM to FlashAttention" ("GEMM interface": m, n, k, lda, ldb,
+// ldc, transb) and the handle create/use/destroy pattern of its cuBLAS
+// example, for row-major operands and alpha = 1, beta = 0.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+
+using namespace gb300;
+
+struct gemm_plan {
+    int device = 0;
+    unsigned flags = 0;
+    int sm_count = 0;
+    int max_pairs = 0;        // co-resident 2-CTA clusters
+    int max_singles = 0;      // co-resident single CTAs
+    int* status_dev = nullptr;
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
+    int forced_kernel = GEMM_KERNEL_AUTO;
+    int last_kernel = -1;
+    int64_t launches = 0;
+    int last_cuda_error = 0;
+    uint64_t timeout_ns = 1000000000ull;
+    int packing = 1;
+    unsigned debug = 0;
+    int group_m = 16;
+    cudaStream_t last_stream = nullptr;
+    bool have_stream = false;
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+
+int record(gemm_plan* p, cudaError_t e) {
+    if (p) p->last_cuda_error = (int)e;
+    return GEMM_ERR_CUDA;
+}
+
+bool get_encode() {
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return true;
+}
+
+// 2-D tensor map: `inner` contiguous elements per row, `outer` rows, row pitch
+// in bytes; box of box_inner x box_outer elements, 128-byte swizzle, zero fill
+// out of bounds.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t gdim[2] = {inner, outer};
+    cuuint64_t gstride[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+bool in_is_bf16(int dtype) { return dtype == DT_BF16_F32 || dtype == DT_BF16_BF16; }
+int out_bytes(int dtype) { return (dtype == DT_BF16_F32 || dtype == DT_F16_F32) ? 4 : 2; }
+
+uint32_t make_idesc(int dtype, bool b_mn_major, int mma_m, int mma_n) {
+    const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;   // 1 = bf16, 0 = fp16
+    return (1u << 4)                       // accumulator fp32
+         | (ab << 7) | (ab << 10)          // A and B formats
+         | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness (A is always K-major)
+         | ((uint32_t)(mma_n >> 3) << 17)
+         | ((uint32_t)(mma_m >> 4) << 24);
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) changed = (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+int ensure_workspace(gemm_plan* p, size_t bytes) {
+    if (bytes <= p->workspace_bytes) return GEMM_OK;
+    if (p->workspace) {
+        if (p->have_stream) cudaStreamSynchronize(p->last_stream);
+        cudaFree(p->workspace);
+        p->workspace = nullptr;
+        p->workspace_bytes = 0;
+    }
+    const size_t want = (size_t)round_up((int64_t)bytes, 1 << 20);
+    cudaError_t e = cudaMalloc(&p->workspace, want);
+    if (e != cudaSuccess) {
+        p->workspace = nullptr;
+        p->last_cuda_error = (int)e;
+        cudaGetLastError();
+        return GEMM_ERR_NO_MEMORY;
+    }
+    p->workspace_bytes = want;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                  int64_t ldb, const void* bias, const void* C, int64_t ldc, int epilogue, int dtype) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
+    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_F16_F16OUT) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~GEMM_B_NK) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if ((epilogue & GEMM_EPI_BIAS) && bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+        if (lda < K) return GEMM_ERR_INVALID_ARG;
+        if (ldb < ((flags & GEMM_B_NK) ? K : N)) return GEMM_ERR_INVALID_ARG;
+    }
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;
+}
+
+int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
+    if (plan == nullptr || device < 0 || (flags & ~GEMM_B_NK)) return GEMM_ERR_INVALID_ARG;
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+    if (device >= ndev) return GEMM_ERR_INVALID_ARG;
+    if (!get_encode()) return GEMM_ERR_CUDA;
+    gemm_plan* p = new (std::nothrow) gemm_plan();
+    if (!p) return GEMM_ERR_NO_MEMORY;
+    p->device = device;
+    p->flags = flags;
+    DeviceGuard g(device);
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) { delete p; return GEMM_ERR_CUDA; }
+    if (prop.major * 10 + prop.minor < 100) { delete p; return GEMM_ERR_UNSUPPORTED; }
+    p->sm_count = prop.multiProcessorCount;
+    for (int dt = 0; dt < 4; ++dt) {
+        int n2 = 0, n1 = 0;
+        e = tc_prepare(2, dt, &n2);
+        if (e == cudaSuccess) e = tc_prepare(1, dt, &n1);
+        if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+        p->max_pairs = n2;
+        p->max_singles = n1;
+    }
+    if (p->max_pairs < 1 || p->max_singles < 1) { delete p; return GEMM_ERR_UNSUPPORTED; }
+    e = cudaMalloc(&p->status_dev, sizeof(int));
+    if (e != cudaSuccess) { delete p; return GEMM_ERR_NO_MEMORY; }
+    e = cudaMemset(p->status_dev, 0, sizeof(int));
+    if (e != cudaSuccess) { cudaFree(p->status_dev); delete p; return GEMM_ERR_CUDA; }
+    if (const char* s = std::getenv("GB300_GEMM_GROUP_M")) {
+        int v = std::atoi(s);
+        if (v >= 1 && v <= 1024) p->group_m = v;
+    }
+    *plan = p;
+    return GEMM_OK;
+}
+
+int gemm_plan_destroy(gemm_plan_t p) {
+    if (!p) return GEMM_OK;
+    DeviceGuard g(p->device);
+    if (p->have_stream) cudaStreamSynchronize(p->last_stream);
+    if (p->workspace) cudaFree(p->workspace);
+    if (p->status_dev) cudaFree(p->status_dev);
+    delete p;
+    return GEMM_OK;
+}
+
+int gemm_plan_set_kernel(gemm_plan_t p, int kernel) {
+    if (!p || kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_SKINNY) return GEMM_ERR_INVALID_ARG;
+    p->forced_kernel = kernel;
+    return GEMM_OK;
+}
+
+int gemm_plan_last_kernel(gemm_plan_t p) { return p ? p->last_kernel : -1; }
+int64_t gemm_plan_launch_count(gemm_plan_t p) { return p ? p->launches : -1; }
+int gemm_plan_last_cuda_error(gemm_plan_t p) { return p ? p->last_cuda_error : 0; }
+int64_t gemm_plan_workspace_bytes(gemm_plan_t p) { return p ? (int64_t)p->workspace_bytes : -1; }
+
+int gemm_plan_set_timeout_ns(gemm_plan_t p, uint64_t ns) {
+    if (!p || ns == 0) return GEMM_ERR_INVALID_ARG;
+    p->timeout_ns = ns;
+    return GEMM_OK;
+}
+
+int gemm_plan_set_packing(gemm_plan_t p, int enabled) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    p->packing = enabled ? 1 : 0;
+    return GEMM_OK;
+}
+
+int gemm_plan_set_debug(gemm_plan_t p, unsigned flags) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    p->debug = flags;
+    return GEMM_OK;
+}
+
+int gemm_plan_status(gemm_plan_t p) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard g(p->device);
+    cudaError_t e = p->have_stream ? cudaStreamSynchronize(p->last_stream) : cudaDeviceSynchronize();
+    if (e != cudaSuccess) return record(p, e);
+    int st = 0;
+    e = cudaMemcpy(&st, p->status_dev, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return record(p, e);
+    if (st != 0) {
+        cudaMemset(p->status_dev, 0, sizeof(int));
+        cudaDeviceSynchronize();
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+const char* gemm_strerror(int code) {
+    switch (code) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_ALIGNMENT: return "operand not 16-byte aligned and packing disabled";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GEMM_ERR_CUDA: return "CUDA call failed";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case GEMM_ERR_NO_MEMORY: return "out of memory";
+        default: return "unknown error";
+    }
+}
+
+int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+             int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, void* stream_v) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    int rc = gemm_validate(p->flags, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+    DeviceGuard g(p->device);
+    const bool b_nk = (p->flags & GEMM_B_NK) != 0;
+    const uint32_t epi = (uint32_t)epilogue;   // GEMM_EPI_* == EpiFlags bits
+    cudaError_t e;
+
+    if (K == 0) {
+        e = launch_fill_epilogue(dtype, M, N, bias, epi, C, ldc, stream);
+        if (e != cudaSuccess) return record(p, e);
+        p->launches += 1;
+        p->last_kernel = GEMM_KERNEL_FILL;
+        p->last_stream = stream; p->have_stream = true;
+        return GEMM_OK;
+    }
+
+    int kernel = p->forced_kernel;
+    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128) ? GEMM_KERNEL_TC_SINGLE : GEMM_KERNEL_TC_PAIR;
+    if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE) return GEMM_ERR_UNSUPPORTED;
+    const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
+
+    // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
+    const int ob = out_bytes(dtype);
+    const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
+    const bool a_ok = aligned16(A) && (lda * 2) % 16 == 0;
+    const bool b_ok = aligned16(B) && (ldb * 2) % 16 == 0;
+    const bool c_ok = aligned16(C) && (ldc * ob) % 16 == 0;
+    const void* A_use = A; int64_t lda_use = lda;
+    const void* B_use = B; int64_t ldb_use = ldb;
+    void* C_use = C; int64_t ldc_use = ldc;
+    if (!a_ok || !b_ok || !c_ok) {
+        if (!p->packing) return GEMM_ERR_ALIGNMENT;
+        const int64_t lda_p = round_up(K, 8), ldb_p = round_up(b_cols, 8), ldc_p = round_up(N, 16 / ob);
+        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(M * lda_p * 2, 256);
+        const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * 2, 256);
+        const size_t c_bytes = c_ok ? 0 : (size_t)round_up(M * ldc_p * ob, 256);
+        rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes);
+        if (rc != GEMM_OK) return rc;
+        char* ws = static_cast<char*>(p->workspace);
+        if (!a_ok) {
+            e = launch_copy2d(A, lda, ws, lda_p, M, K, 2, stream);
+            if (e != cudaSuccess) return record(p, e);
+            p->launches += 1;
+            A_use = ws; lda_use = lda_p;
+        }
+        if (!b_ok) {
+            e = launch_copy2d(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, 2, stream);
+            if (e != cudaSuccess) return record(p, e);
+            p->launches += 1;
+            B_use = ws + a_bytes; ldb_use = ldb_p;
+        }
+        if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
+    }
+
+    const CUtensorMapDataType in_dt = in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType out_dt = (ob == 4) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                 : (in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUtensorMap tmA, tmB, tmC;
+    if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * 2, TC_BK, TC_BM))
+        return GEMM_ERR_CUDA;
+    bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * 2, TC_BK, TC_BN / cg)
+                    : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * 2, 64, TC_BK);
+    if (!okb) return GEMM_ERR_CUDA;
+    if (!make_map(&tmC, out_dt, C_use, (uint64_t)N, (uint64_t)M, (uint64_t)ldc_use * ob, 128 / ob, 32))
+        return GEMM_ERR_CUDA;
+
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.M = (int32_t)M; prm.N = (int32_t)N; prm.K = (int32_t)K;
+    prm.num_m_tiles = (int32_t)((M + TC_BM * cg - 1) / (TC_BM * cg));
+    prm.num_n_tiles = (int32_t)((N + TC_BN - 1) / TC_BN);
+    prm.num_k_blocks = (int32_t)((K + TC_BK - 1) / TC_BK);
+    prm.group_m = p->group_m;
+    prm.epi = epi;
+    prm.idesc = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN);
+    prm.b_mn_major = b_nk ? 0u : 1u;
+    prm.bias = bias;
+    prm.bias_vec16 = (bias != nullptr && aligned16(bias)) ? 1u : 0u;
+    prm.status = p->status_dev;
+    prm.timeout_ns = p->timeout_ns;
+    prm.debug = p->debug;
+    const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
+    if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    const int64_t units = tiles < (cg == 2 ? p->max_pairs : p->max_singles) ? tiles : (cg == 2 ? p->max_pairs : p->max_singles);
+    e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+
+    if (C_use != C) {
+        e = launch_copy2d(C_use, ldc_use, C, ldc, M, N, ob, stream);
+        if (e != cudaSuccess) return record(p, e);
+        p->launches += 1;
+    }
+    p->last_kernel = kernel;
+    p->last_stream = stream; p->have_stream = true;
+    return GEMM_OK;
+}
+
+}  // extern "C"

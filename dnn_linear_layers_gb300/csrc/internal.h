@@ -1,0 +1,70 @@
+// Host-side declarations shared by the C-ABI layer and the kernel translation
+// units.  Not part of the public interface (that is include/gemm.h).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+// Output/input type combinations, same numbering as gemm_dtype_t.
+enum Dtype : int { DT_BF16_F32 = 0, DT_BF16_BF16 = 1, DT_F16_F32 = 2, DT_F16_F16 = 3 };
+
+enum EpiFlags : uint32_t { EPI_BIAS = 1u, EPI_RELU = 2u };
+
+// Bits written into the device status word by a wait that ran out of time.
+enum StatusBits : int {
+    ST_TIMEOUT_PRODUCER = 1,
+    ST_TIMEOUT_MMA = 2,
+    ST_TIMEOUT_EPILOGUE = 4,
+};
+
+// Fault-injection flags (tests only): make one wait run out on purpose.
+enum DebugFlags : uint32_t {
+    DBG_SKIP_FIRST_ACC_COMMIT = 1u,   // MMA warp never signals the first accumulator
+};
+
+// Tile shape of the tensor-core kernels: each CTA owns 128 rows of C, the
+// tile is 256 columns wide, k-blocks are 64 elements (one 128-byte swizzle row).
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 256;
+constexpr int TC_BK = 64;
+
+struct TcParams {
+    int32_t M, N, K;
+    int32_t num_m_tiles;   // tiles of TC_BM * cta_group rows
+    int32_t num_n_tiles;   // tiles of TC_BN columns
+    int32_t num_k_blocks;  // ceil(K / TC_BK)
+    int32_t group_m;       // rasterisation: m-tiles per group
+    uint32_t epi;          // EpiFlags
+    uint32_t idesc;        // tcgen05 instruction descriptor
+    uint32_t b_mn_major;   // 1: B is K x N (N contiguous); 0: B is N x K
+    const void* bias;      // N elements of the input type, or null
+    uint32_t bias_vec16;   // 1: bias is 16-byte aligned (vector loads allowed)
+    int* status;           // device status word (StatusBits)
+    uint64_t timeout_ns;   // bound on any single wait
+    uint32_t debug;        // DebugFlags
+};
+
+// Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the
+// number of CTAs (a multiple of cta_group).  Returns the launch's cudaError_t.
+cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream);
+
+// Dynamic shared memory the tensor-core kernel needs for a cta_group.
+int tc_smem_bytes(int cta_group);
+
+// Configure kernel attributes (dynamic smem) and report the largest number of
+// co-resident clusters (cta_group 2) or CTAs (cta_group 1) on this device.
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units);
+
+// Auxiliary kernels ------------------------------------------------------
+// C[i][j] = epilogue(0) for K == 0 (bias and/or ReLU of an empty sum).
+cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,
+                                 void* C, int64_t ldc, cudaStream_t stream);
+
+// Copy a rows x cols matrix of elem_bytes-sized elements between strides.
+cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+}  // namespace gb300

@@ -1,0 +1,101 @@
+// Small memory-bound helper kernels of the GEMM path:
+//
+//  * fill_epilogue: the K == 0 case, where every output is the epilogue of an
+//    empty sum (bias and/or ReLU of zero, then the cast);
+//  * copy2d: strided 2-D copy used to pack operands whose base address or row
+//    stride breaks the 16-byte rule of TMA into an aligned workspace, and to
+//    copy a padded result back out.  Padding rows to an aligned length is the
+//    "pad to a multiple of 16" advice of youngju.dev "GEMM to FlashAttention"
+//    (PyTorch tips) and the tile/burst alignment remark of the devpress.csdn.net
+//    notes, section 3.6.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace gb300 {
+
+namespace {
+
+template <typename InT, typename OutT>
+__global__ void fill_epilogue_kernel(int64_t M, int64_t N, const InT* bias, uint32_t epi, OutT* C, int64_t ldc) {
+    const int64_t total = M * N;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = t / N, j = t - i * N;
+        float v = 0.0f;
+        if (epi & EPI_BIAS) v += static_cast<float>(bias[j]);
+        if (epi & EPI_RELU) v = fmaxf(v, 0.0f);
+        C[i * ldc + j] = static_cast<OutT>(v);
+    }
+}
+
+template <typename T>
+__global__ void copy2d_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
+                              int64_t rows, int64_t cols) {
+    // one CTA per row chunk: threads stride along the row (coalesced on both sides)
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const T* s = src + r * ld_src;
+        T* d = dst + r * ld_dst;
+        for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x)
+            d[c] = s[c];
+    }
+}
+
+int blocks_for(int64_t work, int threads) {
+    int64_t b = (work + threads - 1) / threads;
+    if (b > 152 * 32) b = 152 * 32;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,
+                                 void* C, int64_t ldc, cudaStream_t stream) {
+    const int threads = 256;
+    const int blocks = blocks_for(M * N, threads);
+    switch (dtype) {
+        case DT_BF16_F32:
+            fill_epilogue_kernel<__nv_bfloat16, float><<<blocks, threads, 0, stream>>>(
+                M, N, (const __nv_bfloat16*)bias, epi, (float*)C, ldc);
+            break;
+        case DT_BF16_BF16:
+            fill_epilogue_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, threads, 0, stream>>>(
+                M, N, (const __nv_bfloat16*)bias, epi, (__nv_bfloat16*)C, ldc);
+            break;
+        case DT_F16_F32:
+            fill_epilogue_kernel<__half, float><<<blocks, threads, 0, stream>>>(
+                M, N, (const __half*)bias, epi, (float*)C, ldc);
+            break;
+        case DT_F16_F16:
+            fill_epilogue_kernel<__half, __half><<<blocks, threads, 0, stream>>>(
+                M, N, (const __half*)bias, epi, (__half*)C, ldc);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t bx = (cols + threads - 1) / threads;
+    if (bx > 64) bx = 64;
+    int64_t by = rows < 65535 ? rows : 65535;
+    dim3 grid((unsigned)bx, (unsigned)by, 1);
+    if (elem_bytes == 2)
+        copy2d_kernel<uint16_t><<<grid, threads, 0, stream>>>((const uint16_t*)src, ld_src, (uint16_t*)dst,
+                                                              ld_dst, rows, cols);
+    else if (elem_bytes == 4)
+        copy2d_kernel<uint32_t><<<grid, threads, 0, stream>>>((const uint32_t*)src, ld_src, (uint32_t*)dst,
+                                                              ld_dst, rows, cols);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace gb300

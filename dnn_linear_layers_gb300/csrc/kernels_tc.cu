@@ -1,0 +1,490 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   C[m][n] = epilogue( sum_k A[m][k] * B[k][n] )   epilogue = (+bias[n]) (ReLU) cast
+//
+// The algorithm is the tiled product of youngju.dev "GEMM to FlashAttention"
+// (tiling diagram: each output tile is the sum over k-tiles of A-tile x
+// B-tile) mapped onto the Blackwell primitives of the CMU 15-418 notes,
+// section 2.9 (TMA copies into shared memory completing on mbarriers, one
+// thread issuing tensor-core MMAs into a TMEM accumulator).  Tile sizes are
+// chosen for sm_103a, not the pages' CPU blocking:
+//
+//   * one CTA owns 128 rows x 256 columns of the output; with cta_group::2 a
+//     pair of CTAs (a 2-CTA cluster) issues 256 x 256 x 16 MMAs, each CTA
+//     holding half of A's rows and half of B's columns in its own smem;
+//   * k-blocks of 64 elements = one 128-byte swizzle row; a ring of stages
+//     (6 for a pair, 4 for a single CTA) keeps TMA loads ahead of the MMAs;
+//   * warp 0 issues TMA loads, warp 1 issues MMAs (leader CTA only) and owns
+//     the TMEM allocation, warps 2-5 run the epilogue: TMEM -> registers ->
+//     (+bias, ReLU, cast) -> swizzled smem -> TMA store;
+//   * the accumulator is double buffered in TMEM (2 x 256 fp32 columns), so
+//     the epilogue of one tile overlaps the main loop of the next;
+//   * the grid is persistent (one CTA per SM) and walks the output tiles in
+//     groups of `group_m` tile-rows so that the B panel stays in L2 while the
+//     group is swept (wave-quantisation and even-load concerns of the
+//     devpress.csdn.net notes, sections 3.6-3.7).
+//
+// Tails: A, B and C are described by TMA tensor maps with their true extents,
+// so loads past M, N or K read zeros and stores past M or N are clipped.
+//
+// Every mbarrier wait is bounded by a %globaltimer budget; a wait that runs
+// out records a status bit, raises a CTA-local abort flag and the roles fall
+// through to a common exit that releases TMEM.  No trap, no endless spin.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int kThreads = 192;          // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kTmemCols = 512;         // 2 accumulators x 256 fp32 columns
+constexpr int kUmmaK = 16;             // K per tcgen05.mma for 16-bit inputs
+
+template <int CG>
+struct TcCfg {
+    static constexpr int kStages = (CG == 2) ? 6 : 4;
+    static constexpr int kBnCta = TC_BN / CG;                    // B columns held per CTA
+    static constexpr int kAStage = TC_BM * TC_BK * 2;           // 16 KB
+    static constexpr int kBStage = kBnCta * TC_BK * 2;          // 16 or 32 KB
+    static constexpr int kCStage = 32 * 128;                     // one warp's 32 rows x 128 B
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kAStage;
+    static constexpr int kOffC = kOffB + kStages * kBStage;
+    static constexpr int kOffMisc = kOffC + kEpiWarps * 2 * kCStage;
+    static constexpr int kMiscBytes = 1024;
+    static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+    // misc region layout (bytes from kOffMisc)
+    static constexpr int kBarFull = 0;
+    static constexpr int kBarEmpty = kBarFull + 8 * kStages;
+    static constexpr int kBarTFull = kBarEmpty + 8 * kStages;
+    static constexpr int kBarTEmpty = kBarTFull + 16;
+    static constexpr int kBarDone = kBarTEmpty + 16;
+    static constexpr int kTmemPtr = kBarDone + 8;
+    static constexpr int kAbort = kTmemPtr + 4;
+    static_assert(kAbort + 4 <= kMiscBytes, "misc layout");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct Waiter {
+    uint64_t budget_ns;
+    volatile int* abort;
+    int* status;
+    int bit;
+    // true once the barrier phase completed; false on timeout or abort.
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t n = 0;
+        while (true) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((++n & 31u) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > budget_ns) {
+                    atomicOr(status, bit);
+                    *abort = 1;
+                    return false;
+                }
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n_tiles, int group_m,
+                                            int& tm, int& tn) {
+    const int per_group = group_m * num_n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int rows = min(num_m_tiles - first_m, group_m);
+    const int r = tile - g * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+template <typename OutT> struct OutTraits;
+template <> struct OutTraits<float> {
+    static constexpr int kCols = 32;   // 128-byte row chunk
+};
+template <> struct OutTraits<__nv_bfloat16> { static constexpr int kCols = 64; };
+template <> struct OutTraits<__half> { static constexpr int kCols = 64; };
+
+template <typename InT> __device__ __forceinline__ float to_f32(InT v);
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int CG, typename InT, typename OutT>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+    using Cfg = TcCfg<CG>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern.
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw_addr);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int unit = (CG == 2) ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int num_units = (CG == 2) ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+
+    const uint32_t misc = base + Cfg::kOffMisc;
+    auto bar_full = [&](int s) { return misc + Cfg::kBarFull + 8u * s; };
+    auto bar_empty = [&](int s) { return misc + Cfg::kBarEmpty + 8u * s; };
+    auto bar_tfull = [&](int a) { return misc + Cfg::kBarTFull + 8u * a; };
+    auto bar_tempty = [&](int a) { return misc + Cfg::kBarTEmpty + 8u * a; };
+    const uint32_t bar_done = misc + Cfg::kBarDone;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Cfg::kOffMisc + Cfg::kAbort);
+    uint32_t* tmem_ptr_smem = reinterpret_cast<uint32_t*>(base_ptr + Cfg::kOffMisc + Cfg::kTmemPtr);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull(a), 1);
+            mbar_init(bar_tempty(a), kEpiWarps * CG);
+        }
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_ptr_smem), kTmemCols);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_ptr_smem;
+
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+    const int nkb = p.num_k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_PRODUCER};
+            const uint64_t pol_a = l2_policy_evict_normal();
+            const uint64_t pol_b = l2_policy_evict_last();
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+                int tm, tn;
+                tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
+                const int m0 = tm * TC_BM * CG + (int)rank * TC_BM;
+                const int nb = tn * TC_BN + (int)rank * Cfg::kBnCta;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = (int)(it % Cfg::kStages);
+                    const uint32_t ph = (it / Cfg::kStages) & 1u;
+                    if (!w.wait(bar_empty(s), ph ^ 1u)) { ok = false; break; }
+                    const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
+                    const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
+                    const int k0 = kb * TC_BK;
+                    if constexpr (CG == 2) {
+                        const uint32_t fb = mapa_shared(bar_full(s), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + Cfg::kBStage));
+                        tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                        if (p.b_mn_major) {
+#pragma unroll
+                            for (int c = 0; c < Cfg::kBnCta / 64; ++c)
+                                tma_load_2d_pair(sb + c * 8192, &tmB, fb, nb + 64 * c, k0, pol_b);
+                        } else {
+                            tma_load_2d_pair(sb, &tmB, fb, k0, nb, pol_b);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(bar_full(s), Cfg::kAStage + Cfg::kBStage);
+                        tma_load_2d(sa, &tmA, bar_full(s), k0, m0, pol_a);
+                        if (p.b_mn_major) {
+#pragma unroll
+                            for (int c = 0; c < Cfg::kBnCta / 64; ++c)
+                                tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);
+                        } else {
+                            tma_load_2d(sb, &tmB, bar_full(s), k0, nb, pol_b);
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Let copies already issued land before shared memory is released.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 100000ull) { }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ----
+        if (rank == 0 && lane == 0) {
+            const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
+            uint32_t it = 0, tcount = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++tcount) {
+                const uint32_t a = tcount & 1u;
+                const uint32_t aph = (tcount >> 1) & 1u;
+                if (!w.wait(bar_tempty(a), aph ^ 1u)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + a * TC_BN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = (int)(it % Cfg::kStages);
+                    const uint32_t ph = (it / Cfg::kStages) & 1u;
+                    if (!w.wait(bar_full(s), ph)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
+                    const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / kUmmaK; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * (kUmmaK * 2), 16, 1024);
+                        const uint64_t bdesc = p.b_mn_major
+                            ? smem_desc_sw128(sb + kk * (kUmmaK * 128), 8192, 1024)
+                            : smem_desc_sw128(sb + kk * (kUmmaK * 2), 16, 1024);
+                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    if constexpr (CG == 2) tc_commit_2(bar_empty(s), 0x3); else tc_commit_1(bar_empty(s));
+                }
+                if (!ok) break;
+                if (!((p.debug & DBG_SKIP_FIRST_ACC_COMMIT) && tcount == 0)) {
+                    if constexpr (CG == 2) tc_commit_2(bar_tfull(a), 0x3); else tc_commit_1(bar_tfull(a));
+                }
+            }
+            // Every MMA this thread issued has finished before TMEM can be released.
+            if constexpr (CG == 2) tc_commit_2(bar_done, 0x1); else tc_commit_1(bar_done);
+            const Waiter wd{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
+            if (!mbar_try_wait(bar_done, 0)) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar_done, 0) && globaltimer_ns() - t0 < wd.budget_ns) { }
+            }
+        }
+    } else {
+        // --------------------------------------------------- epilogue ----
+        const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
+        const uint32_t q = warp & 3u;                 // TMEM lane quarter of this warp
+        constexpr int kCols = OutTraits<OutT>::kCols;
+        constexpr int kChunks = TC_BN / kCols;
+        const uint32_t cbuf0 = base + Cfg::kOffC + (warp - 2) * 2 * Cfg::kCStage;
+        const bool has_bias = (p.epi & EPI_BIAS) != 0;
+        const bool relu = (p.epi & EPI_RELU) != 0;
+        const InT* bias = reinterpret_cast<const InT*>(p.bias);
+        const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), 0) : bar_tempty(0);
+        const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), 0) : bar_tempty(1);
+        uint32_t tcount = 0, cstore = 0;
+        for (int tile = unit; tile < num_tiles; tile += num_units, ++tcount) {
+            int tm, tn;
+            tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
+            const int m0 = tm * TC_BM * CG + (int)rank * TC_BM;
+            const int n0 = tn * TC_BN;
+            const int row0 = m0 + 32 * (int)q;
+            const uint32_t a = tcount & 1u;
+            const uint32_t aph = (tcount >> 1) & 1u;
+            // all lanes poll; the warp leaves together if any lane gave up
+            const bool ready = w.wait(bar_tfull(a), aph);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + ((32u * q) << 16) + a * TC_BN;
+            for (int c = 0; c < kChunks; ++c) {
+                float v[kCols];
+#pragma unroll
+                for (int h = 0; h < kCols / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * kCols + h * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[h * 32 + j] = __uint_as_float(r[j]);
+                }
+                if (c == kChunks - 1) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+                }
+                if (has_bias) {
+                    // every lane reads the same addresses: one broadcast load per vector
+                    const int cb = n0 + c * kCols;
+                    if (p.bias_vec16 && cb + kCols <= p.N) {
+                        const uint4* bv = reinterpret_cast<const uint4*>(bias + cb);
+#pragma unroll
+                        for (int j = 0; j < kCols / 8; ++j) {
+                            const uint4 u = __ldg(bv + j);
+                            const InT* e = reinterpret_cast<const InT*>(&u);
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) v[8 * j + t] += to_f32<InT>(e[t]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j)
+                            if (cb + j < p.N) v[j] += to_f32<InT>(bias[cb + j]);
+                    }
+                }
+                if (relu) {
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) v[j] = fmaxf(v[j], 0.0f);
+                }
+                const uint32_t buf = cbuf0 + (cstore & 1u) * Cfg::kCStage;
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {            // eight 16-byte pieces of the 128-byte row
+                    uint32_t w0, w1, w2, w3;
+                    if constexpr (sizeof(OutT) == 4) {
+                        w0 = __float_as_uint(v[4 * j + 0]); w1 = __float_as_uint(v[4 * j + 1]);
+                        w2 = __float_as_uint(v[4 * j + 2]); w3 = __float_as_uint(v[4 * j + 3]);
+                    } else {
+                        w0 = pack2(v[8 * j + 0], v[8 * j + 1], (OutT*)nullptr);
+                        w1 = pack2(v[8 * j + 2], v[8 * j + 3], (OutT*)nullptr);
+                        w2 = pack2(v[8 * j + 4], v[8 * j + 5], (OutT*)nullptr);
+                        w3 = pack2(v[8 * j + 6], v[8 * j + 7], (OutT*)nullptr);
+                    }
+                    st_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int col = n0 + c * kCols;
+                    if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
+                    bulk_commit_group();
+                }
+                ++cstore;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ teardown ----
+    __syncwarp();
+    tc_fence_before();
+    if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, kTmemCols);
+    }
+    if constexpr (CG == 2) cluster_sync_all();
+}
+
+template <int CG, typename InT, typename OutT>
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const TcParams& p, int grid, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TcCfg<CG>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, InT, OutT>, tmA, tmB, tmC, p);
+}
+
+template <int CG, typename InT, typename OutT>
+cudaError_t prepare_impl(int* max_units) {
+    auto fn = gemm_tc_kernel<CG, InT, OutT>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<CG>::kSmem);
+    if (e != cudaSuccess) return e;
+    if (CG == 2) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        (void)e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CG, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TcCfg<CG>::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (e != cudaSuccess) return e;
+    *max_units = n;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int tc_smem_bytes(int cta_group) {
+    return cta_group == 2 ? TcCfg<2>::kSmem : TcCfg<1>::kSmem;
+}
+
+#define GB300_DISPATCH_DT(CG, CALL)                                                     \
+    switch (dtype) {                                                                    \
+        case DT_BF16_F32: return CALL<CG, __nv_bfloat16, float>;                        \
+        case DT_BF16_BF16: return CALL<CG, __nv_bfloat16, __nv_bfloat16>;               \
+        case DT_F16_F32: return CALL<CG, __half, float>;                                \
+        case DT_F16_F16: return CALL<CG, __half, __half>;                               \
+        default: return cudaErrorInvalidValue;                                          \
+    }
+
+cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream) {
+#define GB300_LAUNCH(CG_, IN_, OUT_) launch_impl<CG_, IN_, OUT_>(tmA, tmB, tmC, p, grid, stream)
+    if (cta_group == 2) {
+        switch (dtype) {
+            case DT_BF16_F32: return GB300_LAUNCH(2, __nv_bfloat16, float);
+            case DT_BF16_BF16: return GB300_LAUNCH(2, __nv_bfloat16, __nv_bfloat16);
+            case DT_F16_F32: return GB300_LAUNCH(2, __half, float);
+            case DT_F16_F16: return GB300_LAUNCH(2, __half, __half);
+        }
+    } else if (cta_group == 1) {
+        switch (dtype) {
+            case DT_BF16_F32: return GB300_LAUNCH(1, __nv_bfloat16, float);
+            case DT_BF16_BF16: return GB300_LAUNCH(1, __nv_bfloat16, __nv_bfloat16);
+            case DT_F16_F32: return GB300_LAUNCH(1, __half, float);
+            case DT_F16_F16: return GB300_LAUNCH(1, __half, __half);
+        }
+    }
+#undef GB300_LAUNCH
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units) {
+#define GB300_PREP(CG_, IN_, OUT_) prepare_impl<CG_, IN_, OUT_>(max_units)
+    if (cta_group == 2) {
+        switch (dtype) {
+            case DT_BF16_F32: return GB300_PREP(2, __nv_bfloat16, float);
+            case DT_BF16_BF16: return GB300_PREP(2, __nv_bfloat16, __nv_bfloat16);
+            case DT_F16_F32: return GB300_PREP(2, __half, float);
+            case DT_F16_F16: return GB300_PREP(2, __half, __half);
+        }
+    } else if (cta_group == 1) {
+        switch (dtype) {
+            case DT_BF16_F32: return GB300_PREP(1, __nv_bfloat16, float);
+            case DT_BF16_BF16: return GB300_PREP(1, __nv_bfloat16, __nv_bfloat16);
+            case DT_F16_F32: return GB300_PREP(1, __half, float);
+            case DT_F16_F16: return GB300_PREP(1, __half, __half);
+        }
+    }
+#undef GB300_PREP
+    return cudaErrorInvalidValue;
+}
+
+#undef GB300_DISPATCH_DT
+
+}  // namespace gb300

@@ -1,0 +1,217 @@
+"""ctypes binding of the C-ABI library (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into (pointer, shape, leading dimension) triples and the
+current torch stream into a ``cudaStream_t``.  It never computes a result on
+its own: if the library is missing or a call fails, it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libgb300gemm.so"
+
+EPI_NONE, EPI_BIAS, EPI_RELU, EPI_BIAS_RELU = 0, 1, 2, 3
+BF16_F32OUT, BF16_BF16OUT, F16_F32OUT, F16_F16OUT = 0, 1, 2, 3
+B_KN, B_NK = 0, 1
+KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
+    0, -1, -2, -3, -4, -5, -6)
+
+# Every symbol include/gemm.h declares, with its ctypes signature.
+_vp, _i64, _int, _uint, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_uint64
+SIGNATURES = {
+    "gemm_plan_create": (_int, [ctypes.POINTER(_vp), _int, _uint]),
+    "gemm_run": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _vp]),
+    "gemm_plan_status": (_int, [_vp]),
+    "gemm_plan_destroy": (_int, [_vp]),
+    "gemm_strerror": (ctypes.c_char_p, [_int]),
+    "gemm_plan_set_kernel": (_int, [_vp, _int]),
+    "gemm_plan_last_kernel": (_int, [_vp]),
+    "gemm_plan_launch_count": (_i64, [_vp]),
+    "gemm_plan_last_cuda_error": (_int, [_vp]),
+    "gemm_plan_set_timeout_ns": (_int, [_vp, _u64]),
+    "gemm_plan_set_packing": (_int, [_vp, _int]),
+    "gemm_plan_set_debug": (_int, [_vp, _uint]),
+    "gemm_plan_workspace_bytes": (_i64, [_vp]),
+    "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
+}
+
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run dnn_linear_layers_gb300/build.py or __graft_entry__.build())")
+        l = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().gemm_strerror(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise GemmError(code, what)
+
+
+def dtype_code(in_dtype: torch.dtype, out_dtype: torch.dtype) -> int:
+    table = {(torch.bfloat16, torch.float32): BF16_F32OUT, (torch.bfloat16, torch.bfloat16): BF16_BF16OUT,
+             (torch.float16, torch.float32): F16_F32OUT, (torch.float16, torch.float16): F16_F16OUT}
+    try:
+        return table[(in_dtype, out_dtype)]
+    except KeyError:
+        raise ValueError(f"unsupported dtype pair {in_dtype} -> {out_dtype}") from None
+
+
+def _ld(t: torch.Tensor) -> int:
+    """Leading dimension (elements) of a row-major 2-D view with unit column stride."""
+    if t.dim() != 2 or (t.stride(1) != 1 and t.shape[1] > 1):
+        raise ValueError("operands must be 2-D row-major views with unit column stride")
+    return max(t.stride(0), t.shape[1], 1)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Plan:
+    """Owner of a ``gemm_plan_t``.  ``b_layout`` is "kn" (B is K x N) or "nk"
+    (B is a Linear weight W, N x K)."""
+
+    def __init__(self, device: int | torch.device = 0, b_layout: str = "kn"):
+        if isinstance(device, torch.device):
+            device = device.index if device.index is not None else torch.cuda.current_device()
+        self.device = int(device)
+        self.b_nk = b_layout == "nk"
+        h = _vp()
+        _check(lib().gemm_plan_create(ctypes.byref(h), self.device, B_NK if self.b_nk else B_KN),
+               "gemm_plan_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().gemm_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- controls ---------------------------------------------------------
+    def set_kernel(self, kernel: int):
+        _check(lib().gemm_plan_set_kernel(self._h, kernel), "gemm_plan_set_kernel")
+
+    def set_timeout_ns(self, ns: int):
+        _check(lib().gemm_plan_set_timeout_ns(self._h, int(ns)), "gemm_plan_set_timeout_ns")
+
+    def set_packing(self, enabled: bool):
+        _check(lib().gemm_plan_set_packing(self._h, int(bool(enabled))), "gemm_plan_set_packing")
+
+    def set_debug(self, flags: int):
+        _check(lib().gemm_plan_set_debug(self._h, int(flags)), "gemm_plan_set_debug")
+
+    @property
+    def last_kernel(self) -> int:
+        return lib().gemm_plan_last_kernel(self._h)
+
+    @property
+    def launch_count(self) -> int:
+        return lib().gemm_plan_launch_count(self._h)
+
+    @property
+    def workspace_bytes(self) -> int:
+        return lib().gemm_plan_workspace_bytes(self._h)
+
+    def status(self) -> int:
+        """Synchronise and return the device status (0 or a GEMM_ERR_* code)."""
+        return lib().gemm_plan_status(self._h)
+
+    # -- the call -----------------------------------------------------------
+    def run_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, bias_ptr, C_ptr, ldc, epilogue, dtype, stream=None) -> int:
+        return lib().gemm_run(self._h, M, N, K, A_ptr, lda, B_ptr, ldb, bias_ptr, C_ptr, ldc,
+                              epilogue, dtype, _stream_handle(stream))
+
+    def run(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, bias: torch.Tensor | None = None,
+            relu: bool = False, stream=None):
+        """C = (A . B (+bias)) (ReLU), written into the caller's C."""
+        M, K = A.shape
+        N = B.shape[0] if self.b_nk else B.shape[1]
+        if (B.shape[1] if self.b_nk else B.shape[0]) != K or tuple(C.shape) != (M, N):
+            raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} C {tuple(C.shape)}")
+        if A.dtype != B.dtype or (bias is not None and bias.dtype != A.dtype):
+            raise ValueError("A, B and bias must share one input dtype")
+        for t in (A, B, C) + ((bias,) if bias is not None else ()):
+            if t.device.type != "cuda":
+                raise ValueError("operands must be CUDA tensors")
+        if bias is not None and (bias.dim() != 1 or bias.shape[0] != N or bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous vector of length N")
+        epi = (EPI_BIAS if bias is not None else 0) | (EPI_RELU if relu else 0)
+        rc = self.run_raw(M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B),
+                          bias.data_ptr() if bias is not None else None, C.data_ptr(), _ld(C), epi,
+                          dtype_code(A.dtype, C.dtype), stream)
+        _check(rc, "gemm_run")
+        return C
+
+
+_plans: dict = {}
+
+
+def _plan_for(device: torch.device, b_layout: str) -> Plan:
+    key = (device.index if device.index is not None else torch.cuda.current_device(), b_layout)
+    p = _plans.get(key)
+    if p is None:
+        p = _plans[key] = Plan(key[0], b_layout)
+    return p
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, out_dtype: torch.dtype | None = None,
+           bias: torch.Tensor | None = None, relu: bool = False, out: torch.Tensor | None = None):
+    """C = A . B (+bias) (ReLU) with B stored K x N."""
+    out_dtype = out_dtype or A.dtype
+    if out is None:
+        out = torch.empty(A.shape[0], B.shape[1], device=A.device, dtype=out_dtype)
+    return _plan_for(A.device, "kn").run(A, B, out, bias, relu)
+
+
+def linear(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None = None, relu: bool = False,
+           out_dtype: torch.dtype | None = None, out: torch.Tensor | None = None):
+    """Linear layer y = x W^T + b (W stored out x in, as ``torch.nn.Linear`` keeps it)."""
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty(x.shape[0], weight.shape[0], device=x.device, dtype=out_dtype)
+    return _plan_for(x.device, "nk").run(x, weight, out, bias, relu)

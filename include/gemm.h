@@ -1,0 +1,153 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) GEMM / Linear-layer library.
+ *
+ * Operation (youngju.dev "GEMM to FlashAttention": the `naive_matmul` listing
+ * C[i][j] = sum_k A[i][k] * B[k][j]; the Linear-layer header
+ * output = W x input + b; CMU 15-418 "DNNs and ML accelerators" notes,
+ * section 2.1: activation f(x) = max(0, x) applied after the bias):
+ *
+ *     C[i][j] = cast( relu?( sum_{k<K} A[i][k] * B(k, j)  (+ bias[j]) ) )
+ *
+ * Layout.  Every matrix is row-major with an explicit leading dimension given
+ * in ELEMENTS (the lda/ldb/ldc of the BLAS GEMM interface, same page, "GEMM
+ * interface").  A is M x K (A[i][k] at A + i*lda + k, lda >= K).  B is K x N
+ * (B[k][j] at B + k*ldb + j, ldb >= N) by default; with the plan flag
+ * GEMM_B_NK, B is a Linear weight W stored N x K, out x in (B(k, j) = W[j][k]
+ * at B + j*ldb + k, ldb >= K) -- the "transb" of the BLAS interface.  C is
+ * M x N (ldc >= N).  bias has N elements of the input type.
+ *
+ * Numerics.  A, B, bias: bf16 or fp16; products and sums in fp32 (the mixed-
+ * precision rule of the same notes, section 2.7: low-precision storage, fp32
+ * accumulation); the bias is added in fp32 before the ReLU and the single
+ * final cast (round to nearest even) to the output type.  alpha = 1 and
+ * beta = 0: C is overwritten, never read.
+ *
+ * Memory.  A, B, bias and C are DEVICE pointers on the plan's device, owned by
+ * the caller and never freed by the library.  The plan owns a small device
+ * status word and, only when an operand breaks the 16-byte rule of the TMA
+ * copies (base address or leading dimension x element size not a multiple of
+ * 16 bytes), a workspace into which that operand is packed; the workspace is
+ * allocated on first need, grows, and is freed by gemm_plan_destroy.
+ *
+ * Asynchrony.  gemm_run enqueues its kernels on `stream` (a cudaStream_t,
+ * NULL = legacy default stream) and returns without waiting.  Only
+ * gemm_plan_status synchronises.  A plan may be used by one stream at a time.
+ *
+ * Errors.  Every function returns 0 (GEMM_OK) or a negative GEMM_ERR_* code;
+ * nothing is launched when argument validation fails.  No function exits the
+ * process or throws.  Device-side waits are bounded: a wait that runs out of
+ * time records GEMM_ERR_DEVICE_TIMEOUT in the plan's status word, which
+ * gemm_plan_status reports (and clears).
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_plan* gemm_plan_t;
+
+/* Epilogue applied to the fp32 accumulator before the output cast. */
+typedef enum {
+    GEMM_EPI_NONE = 0,       /* C = A.B                 */
+    GEMM_EPI_BIAS = 1,       /* C = A.B + bias          */
+    GEMM_EPI_RELU = 2,       /* C = max(0, A.B)         */
+    GEMM_EPI_BIAS_RELU = 3   /* C = max(0, A.B + bias)  */
+} gemm_epilogue_t;
+
+/* Input type of A, B, bias and output type of C. */
+typedef enum {
+    GEMM_BF16_F32OUT = 0,
+    GEMM_BF16_BF16OUT = 1,
+    GEMM_F16_F32OUT = 2,
+    GEMM_F16_F16OUT = 3
+} gemm_dtype_t;
+
+/* Plan flags. */
+#define GEMM_B_KN 0u   /* B is K x N (default) */
+#define GEMM_B_NK 1u   /* B is a Linear weight W, N x K */
+
+/* Kernel selection (gemm_plan_set_kernel / gemm_plan_last_kernel). */
+#define GEMM_KERNEL_AUTO 0
+#define GEMM_KERNEL_TC_PAIR 1   /* tcgen05, 2-CTA clusters (cta_group::2), 256 x 256 tiles */
+#define GEMM_KERNEL_TC_SINGLE 2 /* tcgen05, one CTA per tile (cta_group::1), 128 x 256 tiles */
+#define GEMM_KERNEL_FILL 3      /* K == 0: epilogue of an empty sum */
+#define GEMM_KERNEL_SKINNY 4    /* small-M Linear layer (weight streaming) */
+
+/* Return codes. */
+#define GEMM_OK 0
+#define GEMM_ERR_INVALID_ARG (-1)     /* null/negative/inconsistent argument   */
+#define GEMM_ERR_ALIGNMENT (-2)       /* misaligned operand and packing disabled */
+#define GEMM_ERR_UNSUPPORTED (-3)     /* dtype/epilogue/kernel not available   */
+#define GEMM_ERR_CUDA (-4)            /* a CUDA call failed; see gemm_plan_last_cuda_error */
+#define GEMM_ERR_DEVICE_TIMEOUT (-5)  /* a device-side wait ran out of time    */
+#define GEMM_ERR_NO_MEMORY (-6)       /* workspace allocation failed           */
+
+/* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK.
+ * Allocates the plan and its device status word; restores the caller's
+ * current device before returning.  *plan is set only on success. */
+int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
+
+/* C = epilogue(A.B) (see above).  M, N, K >= 0; M == 0 or N == 0 is a no-op;
+ * K == 0 writes epilogue(0).  `bias` may be NULL unless the epilogue adds it.
+ * `epilogue` is a gemm_epilogue_t, `dtype` a gemm_dtype_t, `stream` a
+ * cudaStream_t.  Returns after enqueueing the work. */
+int gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+             const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+             void* C, int64_t ldc, int epilogue, int dtype, void* stream);
+
+/* Synchronise the stream of the last gemm_run and report device-side errors:
+ * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last call (the
+ * status word is then cleared), GEMM_ERR_CUDA if the stream reports an error. */
+int gemm_plan_status(gemm_plan_t plan);
+
+/* Release the plan, its status word and its workspace.  NULL is accepted. */
+int gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static description of a return code. */
+const char* gemm_strerror(int code);
+
+/* --- controls and introspection (benchmarks and tests) ------------------ */
+
+/* Force a kernel (GEMM_KERNEL_*); GEMM_KERNEL_AUTO restores the dispatcher. */
+int gemm_plan_set_kernel(gemm_plan_t plan, int kernel);
+
+/* Kernel chosen by the last successful gemm_run (GEMM_KERNEL_*), or -1. */
+int gemm_plan_last_kernel(gemm_plan_t plan);
+
+/* Number of kernels this plan has launched since creation. */
+int64_t gemm_plan_launch_count(gemm_plan_t plan);
+
+/* cudaError_t of the last failing CUDA call made for this plan (0 if none). */
+int gemm_plan_last_cuda_error(gemm_plan_t plan);
+
+/* Bound, in nanoseconds, on any single device-side wait (default 1e9). */
+int gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns);
+
+/* Allow (1, default) or forbid (0) packing of misaligned operands; when
+ * forbidden, gemm_run returns GEMM_ERR_ALIGNMENT for them instead. */
+int gemm_plan_set_packing(gemm_plan_t plan, int enabled);
+
+/* Test hook: fault-injection flags.  Bit 0 makes the MMA warp skip the first
+ * "accumulator ready" signal so the epilogue's bounded wait runs out and the
+ * run reports GEMM_ERR_DEVICE_TIMEOUT; the GPU context stays usable. */
+int gemm_plan_set_debug(gemm_plan_t plan, unsigned flags);
+
+/* Bytes of workspace the plan currently holds. */
+int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
+
+/* Host-only argument check: the code gemm_run would return for these
+ * arguments before touching the GPU (GEMM_OK if they are acceptable).
+ * `flags` are the plan flags.  Needs no device and launches nothing. */
+int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                  const void* C, int64_t ldc, int epilogue, int dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,106 @@
+"""Host-only checks of the C-ABI library: it builds, loads without a GPU,
+exports every symbol include/gemm.h declares, and validates arguments exactly
+as documented (no device needed, nothing launched)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+import torch
+
+from dnn_linear_layers_gb300 import build as B
+from dnn_linear_layers_gb300 import gemm as G
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return G.lib()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "gemm.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s+\**\s*(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for core in ("gemm_plan_create", "gemm_run", "gemm_plan_status", "gemm_plan_destroy", "gemm_strerror"):
+        assert core in names
+    assert set(names) == set(G.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert G.strerror(code) and G.strerror(code) != "unknown error"
+    assert G.strerror(17) == "unknown error"
+
+
+P = ctypes.c_void_p(0x1000)   # any non-null, 16-byte aligned host value: validate never dereferences
+
+
+def val(flags=0, M=64, N=64, K=64, A=P, lda=64, Bp=P, ldb=64, bias=None, C=P, ldc=64, epi=0, dtype=1):
+    return G.lib().gemm_validate(flags, M, N, K, A, lda, Bp, ldb, bias, C, ldc, epi, dtype)
+
+
+def test_validate_accepts_good_arguments(lib):
+    assert val() == G.OK
+    assert val(flags=G.B_NK, N=32, ldb=64, ldc=32) == G.OK
+    assert val(epi=G.EPI_BIAS_RELU, bias=P) == G.OK
+
+
+def test_validate_rejects_bad_arguments(lib):
+    assert val(M=-1) == G.ERR_INVALID_ARG
+    assert val(K=-5) == G.ERR_INVALID_ARG
+    assert val(epi=4) == G.ERR_INVALID_ARG
+    assert val(dtype=9) == G.ERR_INVALID_ARG
+    assert val(flags=2) == G.ERR_INVALID_ARG
+    assert val(lda=63) == G.ERR_INVALID_ARG               # lda < K
+    assert val(ldb=63) == G.ERR_INVALID_ARG               # ldb < N (K x N layout)
+    assert val(flags=G.B_NK, K=128, lda=128, ldb=64) == G.ERR_INVALID_ARG   # ldb < K (N x K layout)
+    assert val(ldc=10) == G.ERR_INVALID_ARG
+    assert val(A=None) == G.ERR_INVALID_ARG
+    assert val(Bp=None) == G.ERR_INVALID_ARG
+    assert val(C=None) == G.ERR_INVALID_ARG
+    assert val(epi=G.EPI_BIAS, bias=None) == G.ERR_INVALID_ARG
+    assert val(M=2 ** 31, lda=64) == G.ERR_UNSUPPORTED
+
+
+def test_validate_size_zero_is_a_noop(lib):
+    assert val(M=0, A=None, Bp=None, C=None) == G.OK
+    assert val(N=0, A=None, Bp=None, C=None) == G.OK
+    # K == 0: A and B are not read, but C is written (epilogue of 0)
+    assert val(K=0, A=None, Bp=None, lda=0) == G.OK
+    assert val(K=0, A=None, Bp=None, C=None) == G.ERR_INVALID_ARG
+
+
+def test_null_plan_is_rejected(lib):
+    assert lib.gemm_run(None, 1, 1, 1, P, 1, P, 1, None, P, 1, 0, 1, None) == G.ERR_INVALID_ARG
+    assert lib.gemm_plan_status(None) == G.ERR_INVALID_ARG
+    assert lib.gemm_plan_destroy(None) == G.OK
+    assert lib.gemm_plan_set_kernel(None, 0) == G.ERR_INVALID_ARG
+    assert lib.gemm_plan_last_kernel(None) == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour on a host without a GPU")
+def test_plan_create_without_gpu_returns_error(lib):
+    h = ctypes.c_void_p()
+    rc = lib.gemm_plan_create(ctypes.byref(h), 0, 0)
+    assert rc in (G.ERR_CUDA, G.ERR_INVALID_ARG)
+    assert h.value is None
+    assert lib.gemm_plan_create(None, 0, 0) == G.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(G, "LIB_PATH", tmp_path / "missing.so")
+    monkeypatch.setattr(G, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        G.lib()

@@ -1,0 +1,202 @@
+"""GPU parity tests: the CUDA path through the C ABI against the float64 oracle.
+
+Sizes span several 256 x 256 tiles with ragged tails in M, N and K and stay
+small enough for the oracle to finish in seconds.  Integer cases must match
+exactly; float cases within 1e-3 * sum|a b| + 1e-6 (+ one output ulp for a
+16-bit output).  Every run checks a NaN guard band around C.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dnn_linear_layers_gb300 import gemm as G
+from dnn_linear_layers_gb300.inputs import GemmCase, SMALL_F32
+
+from parity import alloc_with_guard, compare, guard_intact, oracle_full, run_case
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"single": G.KERNEL_TC_SINGLE, "pair": G.KERNEL_TC_PAIR}
+
+
+@pytest.fixture(scope="module")
+def plans():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from dnn_linear_layers_gb300 import build
+    build.build()
+    kn = G.Plan(0, "kn")
+    nk = G.Plan(0, "nk")
+    yield {"kn": kn, "nk": nk}
+    kn.close(); nk.close()
+
+
+def plan_for(plans, case):
+    return plans["nk" if case.b_nk else "kn"]
+
+
+def check(plans, case, kernel=None):
+    p = plan_for(plans, case)
+    A, B, bias, C = run_case(p, case, kernel=KERNELS.get(kernel, kernel) if kernel else G.KERNEL_AUTO)
+    C_ref, S = oracle_full(case, A, B, bias)
+    return compare(case, C, C_ref, S)
+
+
+# ------------------------------------------------------------ first slice
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("b_nk", [False, True])
+def test_one_tile_integer_exact(plans, kernel, b_nk):
+    check(plans, GemmCase("one_tile", 256, 256, 64, b_nk=b_nk, out="f32", integer=True), kernel)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_config_512_f32_out(plans, kernel):
+    """M=N=K=512, N(0,1) bf16 inputs from seed 0, fp32 output, no epilogue."""
+    check(plans, SMALL_F32, kernel)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("b_nk", [False, True])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_integer_exact_ragged(plans, kernel, b_nk, out):
+    check(plans, GemmCase("int_ragged", 600, 700, 333, b_nk=b_nk, out=out, integer=True, seed=3), kernel)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("epi", [(False, False), (True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("b_nk", [False, True])
+def test_epilogues_integer_exact(plans, kernel, epi, b_nk):
+    bias, relu = epi
+    check(plans, GemmCase("int_epi", 520, 530, 200, b_nk=b_nk, bias=bias, relu=relu, out="bf16",
+                          integer=True, seed=5), kernel)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("b_nk", [False, True])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_float_within_tolerance(plans, kernel, b_nk, out):
+    check(plans, GemmCase("float_ragged", 700, 600, 1000, b_nk=b_nk, out=out, bias=True, relu=True,
+                          seed=7), kernel)
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("integer", [True, False])
+def test_fp16_inputs(plans, out, integer):
+    check(plans, GemmCase("fp16", 384, 520, 264, in_dtype="f16", out=out, integer=integer, bias=True, seed=9))
+
+
+TAILS = [1, 7, 127, 129, 255, 257]
+
+
+@pytest.mark.parametrize("M", TAILS)
+@pytest.mark.parametrize("N", [8, 129, 264])
+@pytest.mark.parametrize("K", [8, 72, 264])
+def test_tails_integer_exact(plans, M, N, K):
+    check(plans, GemmCase("tails", M, N, K, out="f32", integer=True, seed=M + N + K))
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (129, 77, 1000), (257, 1001, 99)])
+@pytest.mark.parametrize("b_nk", [False, True])
+def test_misaligned_strides_are_packed(plans, shape, b_nk):
+    """Row lengths whose byte size is not a multiple of 16 go through the pack path."""
+    M, N, K = shape
+    check(plans, GemmCase("misaligned", M, N, K, b_nk=b_nk, out="bf16", integer=True, bias=True, seed=11))
+
+
+def test_odd_1000_cube(plans):
+    check(plans, GemmCase("odd1000", 1000, 1000, 1000, out="bf16", seed=1))
+
+
+def test_k_zero_writes_epilogue(plans):
+    p = plans["kn"]
+    M, N = 37, 45
+    bias = torch.linspace(-2, 2, N, dtype=torch.bfloat16, device="cuda")
+    buf, C, iv, bits = alloc_with_guard(M, N, torch.float32)
+    A = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
+    p.run(A, B, C, bias, relu=True)
+    assert p.status() == 0 and p.last_kernel == G.KERNEL_FILL
+    assert guard_intact(buf, M, N, iv, bits)
+    expect = torch.clamp(bias.float(), min=0).expand(M, N).cpu()
+    assert torch.equal(C.cpu(), expect)
+
+
+def test_empty_is_noop(plans):
+    p = plans["kn"]
+    before = p.launch_count
+    C = torch.full((0, 5), 3.0, device="cuda")
+    p.run(torch.empty((0, 4), dtype=torch.bfloat16, device="cuda"),
+          torch.empty((4, 5), dtype=torch.bfloat16, device="cuda"), C)
+    assert p.launch_count == before
+
+
+def test_misaligned_bias_pointer(plans):
+    p = plans["kn"]
+    case = GemmCase("bias_off", 300, 264, 128, bias=True, out="f32", integer=True, seed=13)
+    A, B, bias = case.tensors()
+    big = torch.zeros(case.N + 1, dtype=torch.bfloat16)
+    big[1:] = bias
+    bias_dev = big.cuda()[1:]            # 2-byte offset: not 16-byte aligned
+    C = torch.empty(case.M, case.N, device="cuda")
+    p.run(A.cuda(), B.cuda(), C, bias_dev)
+    assert p.status() == 0
+    C_ref, S = oracle.gemm(A, B, bias=bias, with_mag=True)
+    compare(case, C.cpu(), C_ref, S)
+
+
+def test_non_default_stream(plans):
+    p = plans["kn"]
+    case = GemmCase("stream", 512, 512, 256, out="f32", integer=True, seed=17)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        A, B, bias, C = run_case(p, case, stream=s)
+    C_ref, S = oracle_full(case, A, B, bias)
+    compare(case, C, C_ref, S)
+
+
+def test_deterministic_bits(plans):
+    p = plans["kn"]
+    case = GemmCase("det", 640, 768, 1024, out="f32", seed=19)
+    A, B, _ = case.tensors()
+    A, B = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(5):
+        C = torch.empty(case.M, case.N, device="cuda")
+        p.run(A, B, C)
+        outs.append(C.cpu())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_packing_disabled_reports_alignment(plans):
+    p = G.Plan(0, "kn")
+    p.set_packing(False)
+    A = torch.ones(8, 7, dtype=torch.bfloat16, device="cuda")
+    B = torch.ones(7, 8, dtype=torch.bfloat16, device="cuda")
+    C = torch.empty(8, 8, device="cuda")
+    with pytest.raises(G.GemmError) as ei:
+        p.run(A, B, C)
+    assert ei.value.code == G.ERR_ALIGNMENT
+    p.close()
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_bounded_wait_reports_timeout_and_context_survives(plans, kernel):
+    """Fault injection on the host's request: the MMA warp withholds the first
+    'accumulator ready' signal, the epilogue's bounded wait runs out, the run
+    reports GEMM_ERR_DEVICE_TIMEOUT, and the next run on the same context is
+    correct."""
+    p = G.Plan(0, "kn")
+    p.set_kernel(KERNELS[kernel])
+    p.set_timeout_ns(20_000_000)          # 20 ms
+    p.set_debug(1)
+    A = torch.ones(256, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.ones(64, 256, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(256, 256, device="cuda")
+    p.run(A, B, C)
+    assert p.status() == G.ERR_DEVICE_TIMEOUT
+    p.set_debug(0)
+    p.run(A, B, C)
+    assert p.status() == 0
+    assert torch.all(C == 64.0)
+    p.close()
