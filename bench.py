@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Benchmark: bf16 GEMM throughput at M = N = K = 8192 on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one call of the library's public entry point, ``gemm_run`` (C ABI),
+on the workload: C[8192 x 8192] = A[8192 x 8192] . B[8192 x 8192], bf16
+inputs drawn N(0, 1) from fixed seeds, fp32 accumulation, bf16 output.  The
+inputs (384 MB with C) are larger than the 129 MB L2, so no flush is needed
+between steps.  ``value`` is TFLOP/s (2*M*N*K per step) with the inputs
+resident in HBM; ``e2e`` is the same metric when every step also copies A and
+B from pinned host memory and reads C back.
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica of the workload (the GEMM needs no exchange between GPUs) and the
+value is the work of all ranks over the slowest rank's time.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (whole rows of C) and prints the same
+metric; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "bf16 GEMM TFLOP/s at M=N=K=8192 and % of GB300 dense bf16 roofline"
+
+WORKLOADS = {
+    # name: (M, N, K, b_layout, epilogue(bias, relu), out, a_std, b_std)
+    "square8192_bf16": (8192, 8192, 8192, "kn", (False, False), "bf16", 1.0, 1.0),
+    "square4096_bf16": (4096, 4096, 4096, "kn", (False, False), "bf16", 1.0, 1.0),
+    "qkv_8192x4096x12288": (8192, 12288, 4096, "kn", (False, False), "bf16", 1.0, 4096 ** -0.5),
+    "ffn_up_8192x4096x14336": (8192, 14336, 4096, "kn", (True, True), "bf16", 1.0, 4096 ** -0.5),
+    "ffn_down_8192x14336x4096": (8192, 4096, 14336, "kn", (True, False), "bf16", 1.0, 14336 ** -0.5),
+    "conv_im2col_100352x2304x256": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
+    "odd_3000x5000x2048": (3000, 5000, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
+    "odd_4095": (4095, 4095, 4095, "kn", (False, False), "bf16", 1.0, 1.0),
+    "odd_1000": (1000, 1000, 1000, "kn", (False, False), "bf16", 1.0, 1.0),
+}
+DEFAULT_WORKLOAD = "square8192_bf16"
+KERNEL_NAME = "gemm_tc_kernel"
+SMI_QUERY = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "dnn_linear_layers_gb300" / "csrc").glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the top kernel from the committed ncu summary,
+    valid only if the kernel sources are unchanged since it was taken."""
+    f = ROOT / "profiles" / "traffic.json"
+    try:
+        d = json.loads(f.read_text())
+        e = d[workload]
+        if e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={SMI_QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, max_mhz_hint=None):
+        sms, maxes, reasons, powers = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm, mx = float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            sms.append(sm); maxes.append(mx)
+            try:
+                powers.append(float(f[4]))
+            except ValueError:
+                pass
+            for n, v in zip(names, f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz_hint, "reasons": [], "samples": 0}
+        # samples under load: the upper half by power (the tool starts before the load)
+        loaded = sms
+        if powers and len(powers) == len(sms) and len(sms) >= 4:
+            cut = statistics.median(powers)
+            loaded = [s for s, p in zip(sms, powers) if p >= cut] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms), "power_w_max": max(powers) if powers else None}
+
+
+def make_inputs(name, device, seed=0):
+    import torch
+    from dnn_linear_layers_gb300.inputs import normal_bf16
+    M, N, K, lay, (has_bias, relu), out, a_std, b_std = WORKLOADS[name]
+    A = normal_bf16((M, K), 3 * seed, a_std)
+    B = normal_bf16((N, K) if lay == "nk" else (K, N), 3 * seed + 1, b_std)
+    bias = normal_bf16((N,), 3 * seed + 2, 0.02) if has_bias else None
+    return A, B, bias
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from dnn_linear_layers_gb300 import gemm as G
+    from dnn_linear_layers_gb300 import roofline as R
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    name = args.workload
+    M, N, K, lay, (has_bias, relu), out, _, _ = WORKLOADS[name]
+    A_h, B_h, bias_h = make_inputs(name, dev, seed=0)
+    A, B = A_h.to(dev), B_h.to(dev)
+    bias = bias_h.to(dev) if bias_h is not None else None
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    plan = G.Plan(local_rank, lay)
+    stream = torch.cuda.current_stream(dev)
+    flops = 2.0 * M * N * K
+
+    def step(a=A, b=B, c=C):
+        plan.run(a, b, c, bias, relu, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert plan.status() == 0, "device status after warm-up"
+
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    # keep the GPU busy ~1 s (untimed) so the sampler is running and clocks settle
+    t_end = time.time() + (1.0 if sampler else 0.0)
+    while time.time() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+    launches0 = plan.launch_count
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = plan.launch_count - launches0
+    if sampler:
+        sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    st = plan.status()
+    assert st == 0, f"device status {st}"
+
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> gemm_run -> host result
+    A_p = A_h.pin_memory(); B_p = B_h.pin_memory()
+    C_p = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    A_e = torch.empty_like(A); B_e = torch.empty_like(B); C_e = torch.empty_like(C)
+
+    def e2e_step():
+        A_e.copy_(A_p, non_blocking=True)
+        B_e.copy_(B_p, non_blocking=True)
+        plan.run(A_e, B_e, C_e, bias, relu, stream=stream)
+        C_p.copy_(C_e, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(0 if args.no_e2e else 2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(0 if args.no_e2e else e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12 if not args.no_e2e else None
+    assert plan.status() == 0
+
+    peaks, src = R.load_peaks()
+    bias_bytes = 2 if has_bias else 0
+    nbytes = R.gemm_bytes(M, N, K, 2, 2, 2, bias_bytes)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    t_roof = R.roofline_time(flops, nbytes, peak * 1e12, peaks["hbm_gbs"] * 1e9)
+    result = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(name, A_h, B_h, bias_h, args.cpu_seconds)
+        clocks = sampler.summary() if sampler else {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM",
+            "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": lay,
+                       "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none",
+                       "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2 ({nbytes / 1e6:.1f} MB > 129 MB), no flush",
+                       "kernel": {1: "tc_pair", 2: "tc_single"}.get(plan.last_kernel, str(plan.last_kernel))},
+            "roofline": {"bound": "tensor" if flops / peak / 1e12 >= nbytes / peaks["hbm_gbs"] / 1e9 else "hbm",
+                         "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4),
+                         "frac_of_roofline_time": round(t_roof / (kernel_ms * 1e-3), 4),
+                         "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops, burst)" if src == "measured" else "fallback",
+                         "traffic": profiled_traffic(name),
+                         "algorithmic_bytes": nbytes, "flops_per_launch": flops,
+                         "kernel_ms": round(kernel_ms, 5)},
+            "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(A_p.numel() * 2 + B_p.numel() * 2),
+                    "d2h_bytes_per_step": int(C_p.numel() * 2), "steps": e2e_steps},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(result), flush=True)
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return result
+
+
+def _oracle_rows_timer(name, A, B, bias):
+    """Callable timing the oracle on n seeded whole rows of C: returns (seconds, n)."""
+    import numpy as np
+    import oracle
+    M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
+    threads = len(os.sched_getaffinity(0))
+    Af = A.double().numpy(); Bf = B.double().numpy()
+    bf = bias.double().numpy() if bias is not None else None
+    rng = np.random.default_rng(0)
+
+    def run(n):
+        rows = rng.choice(M, size=min(M, n), replace=False)
+        t = time.perf_counter()
+        oracle.gemm_rows(Af, Bf, rows, bias=bf, relu=relu, b_nk=(lay == "nk"), threads=threads)
+        return time.perf_counter() - t, len(rows)
+
+    return run, threads
+
+
+def cpu_baseline(name, A, B, bias, seconds: float):
+    """Oracle (float64 triple loop, OpenMP over rows) on whole rows of C, about `seconds` of work."""
+    M, N, K, *_ = WORKLOADS[name]
+    run, threads = _oracle_rows_timer(name, A, B, bias)
+    dt, n = run(threads)                        # calibration: one row per thread
+    n = int(max(threads, min(M, threads * max(1, round(seconds / max(dt, 1e-3))))))
+    dt, n = run(n)
+    return {"value": round(2.0 * n * N * K / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"{n} of {M} rows of C (each {N} x {K} MACs), {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    name = args.workload
+    M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
+    A, B, bias = make_inputs(name, None, seed=0)
+    run, threads = _oracle_rows_timer(name, A, B, bias)
+    dt, n = run(threads)
+    # size every step so the whole run stays within about two minutes
+    per_step = min(max(90.0 / (args.warmup + args.steps), 0.05), args.cpu_seconds)
+    n = int(max(threads, min(M, threads * max(1, round(per_step / max(dt, 1e-3))))))
+    vals, times = [], []
+    for i in range(args.warmup + args.steps):
+        dt, n_done = run(n)
+        if i >= args.warmup:
+            vals.append(2.0 * n_done * N * K / dt / 1e12); times.append(dt)
+    value = round(statistics.median(vals), 6)
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: same inputs as the GPU arm", "config": {"workload": name, "M": M, "N": N, "K": K},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                            "sample": f"{n} of {M} rows of C per step (each {N} x {K} MACs)"},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
