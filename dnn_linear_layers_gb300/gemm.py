@@ -39,6 +39,7 @@ SIGNATURES = {
     "gemm_plan_set_debug": (_int, [_vp, _uint]),
     "gemm_plan_workspace_bytes": (_i64, [_vp]),
     "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
+    "gemm_run_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _uint, _vp, _vp]),
 }
 
 _lib = None

@@ -146,6 +146,40 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K,
                   const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
                   const void* C, int64_t ldc, int epilogue, int dtype);
 
+/* --- entry point for callers that cannot allocate device memory --------- */
+
+/* Size in bytes of the fixed device scratch that gemm_run_noalloc uses on
+ * every GPU where the library is loaded (held until the process exits). */
+#define GEMM_NOALLOC_SCRATCH_BYTES 33554432u   /* 32 MiB */
+
+/* The pages have no counterpart to this function; it exists for callers that
+ * may not allocate device memory: processes whose HBM is reserved up front by
+ * a pool or framework allocator, and latency-sensitive callers that cannot
+ * accept cudaMalloc/cudaFree (which may synchronise the whole device).
+ *
+ * Same operation, layouts and codes as gemm_run, on the CURRENT device, with
+ * the plan flags passed directly (`flags`: GEMM_B_KN or GEMM_B_NK) and no
+ * plan.  It allocates nothing: operands that break the 16-byte TMA rule are
+ * packed into a fixed scratch array of GEMM_NOALLOC_SCRATCH_BYTES (minus 256
+ * bytes for a status word) that the library holds on each device; a call
+ * whose packed operands would not fit returns GEMM_ERR_UNSUPPORTED and
+ * launches nothing.  Aligned operands need no scratch at any size.
+ *
+ * `dev_status` (device memory, may be NULL): when given, device-side waits
+ * that run out of time OR a non-zero bit into it (the caller clears it); when
+ * NULL the scratch's own status word is cleared and used, and not reported.
+ *
+ * The first call on each device sets up that device (it looks up the
+ * scratch's device address with cudaGetSymbolAddress and configures the
+ * kernels); make that first call before any stream capture.  All calls on a
+ * device share the scratch, which keeps the last call's contents: calls whose
+ * GPU work overlaps (different streams or threads) race and must be ordered
+ * by the caller.  Returns after enqueueing the work on `stream`. */
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
+                     void* C, int64_t ldc, int epilogue, int dtype, unsigned flags,
+                     int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
