@@ -29,6 +29,8 @@ struct gemm_plan {
     int packing = 1;
     unsigned debug = 0;
     int group_m = 16;
+    unsigned l2_policy = 0;
+    int skinny_per_sm[9] = {0};   // co-resident skinny CTAs per SM, by mpad / 16
     cudaStream_t last_stream = nullptr;
     bool have_stream = false;
 };
@@ -119,6 +121,44 @@ int ensure_workspace(gemm_plan* p, size_t bytes) {
     return GEMM_OK;
 }
 
+// Skinny-M launch: feature tiles of 128 weight rows, split-K over a cluster of
+// S CTAs chosen so the whole grid is resident at once.
+int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* W,
+               int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, int dtype, bool w_nk,
+               CUtensorMapDataType in_dt, cudaStream_t stream) {
+    const int mpad = (int)round_up(M, 16);
+    const int tmem_cols = mpad <= 32 ? 32 : (mpad <= 64 ? 64 : 128);
+    const int64_t n_tiles = (N + 127) / 128;
+    const int64_t nkb = (K + 63) / 64;
+    if (n_tiles > INT32_MAX / 8) return GEMM_ERR_UNSUPPORTED;
+    const int64_t slots = (int64_t)p->sm_count * p->skinny_per_sm[mpad / 16];
+    int S = 1;
+    while (S < 8 && n_tiles * (S * 2) <= slots && S * 2 <= nkb) S *= 2;
+    CUtensorMap tmW, tmX;
+    const bool okw = w_nk ? make_map(&tmW, in_dt, W, (uint64_t)K, (uint64_t)N, (uint64_t)ldw * 2, 64, 128)
+                          : make_map(&tmW, in_dt, W, (uint64_t)N, (uint64_t)K, (uint64_t)ldw * 2, 64, 64);
+    if (!okw) return GEMM_ERR_CUDA;
+    if (!make_map(&tmX, in_dt, X, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, 64, (uint32_t)mpad))
+        return GEMM_ERR_CUDA;
+    SkinnyParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.M = (int32_t)M; sp.N = (int32_t)N; sp.K = (int32_t)K;
+    sp.mpad = mpad; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
+    sp.epi = epi;
+    const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;
+    sp.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((w_nk ? 0u : 1u) << 15) | ((uint32_t)(mpad >> 3) << 17) |
+               ((uint32_t)(128 >> 4) << 24);
+    sp.w_mn_major = w_nk ? 0u : 1u;
+    sp.bias = bias;
+    sp.Y = Y; sp.ldy = ldy;
+    sp.status = p->status_dev;
+    sp.timeout_ns = p->timeout_ns;
+    cudaError_t e = launch_skinny(dtype, tmW, tmX, sp, (int)(n_tiles * S), stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -167,13 +207,26 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
         p->max_singles = n1;
     }
     if (p->max_pairs < 1 || p->max_singles < 1) { delete p; return GEMM_ERR_UNSUPPORTED; }
+    for (int dt = 0; dt < 4; ++dt) {
+        e = skinny_prepare(dt);
+        if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+    }
+    for (int b = 1; b <= 8; ++b) {
+        e = skinny_blocks_per_sm(16 * b, &p->skinny_per_sm[b]);
+        if (e != cudaSuccess || p->skinny_per_sm[b] < 1) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+    }
     e = cudaMalloc(&p->status_dev, sizeof(int));
     if (e != cudaSuccess) { delete p; return GEMM_ERR_NO_MEMORY; }
     e = cudaMemset(p->status_dev, 0, sizeof(int));
     if (e != cudaSuccess) { cudaFree(p->status_dev); delete p; return GEMM_ERR_CUDA; }
+    // tuning overrides for benchmarking sweeps only
     if (const char* s = std::getenv("GB300_GEMM_GROUP_M")) {
         int v = std::atoi(s);
         if (v >= 1 && v <= 1024) p->group_m = v;
+    }
+    if (const char* s = std::getenv("GB300_GEMM_L2_POLICY")) {
+        int v = std::atoi(s);
+        if (v >= 0 && v <= 2) p->l2_policy = (unsigned)v;
     }
     *plan = p;
     return GEMM_OK;
@@ -247,6 +300,20 @@ const char* gemm_strerror(int code) {
     }
 }
 
+int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad, int stride,
+                void* out, int64_t ld_out, int elem_bytes, void* stream) {
+    if (Nb < 0 || H < 0 || W < 0 || C < 0 || R < 1 || S < 1 || pad < 0 || stride < 1) return GEMM_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return GEMM_ERR_INVALID_ARG;
+    const int64_t OH = H + 2 * pad >= R ? (H + 2 * pad - R) / stride + 1 : 0;
+    const int64_t OW = W + 2 * pad >= S ? (W + 2 * pad - S) / stride + 1 : 0;
+    if (Nb == 0 || OH == 0 || OW == 0 || C == 0) return GEMM_OK;
+    if (x == nullptr || out == nullptr || ld_out < (int64_t)R * S * C) return GEMM_ERR_INVALID_ARG;
+    cudaError_t e = launch_im2col(x, Nb, H, W, C, R, S, pad, stride, out, ld_out, elem_bytes,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+    return GEMM_OK;
+}
+
 int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
              int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, void* stream_v) {
     if (!p) return GEMM_ERR_INVALID_ARG;
@@ -269,8 +336,11 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     }
 
     int kernel = p->forced_kernel;
-    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128) ? GEMM_KERNEL_TC_SINGLE : GEMM_KERNEL_TC_PAIR;
-    if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && M > 128) return GEMM_ERR_UNSUPPORTED;
+    if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
+        return GEMM_ERR_UNSUPPORTED;
+    const bool skinny = kernel == GEMM_KERNEL_SKINNY;
     const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
 
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
@@ -278,7 +348,8 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
     const bool a_ok = aligned16(A) && (lda * 2) % 16 == 0;
     const bool b_ok = aligned16(B) && (ldb * 2) % 16 == 0;
-    const bool c_ok = aligned16(C) && (ldc * ob) % 16 == 0;
+    // the skinny kernel stores C with plain stores: any pitch is fine
+    const bool c_ok = skinny || (aligned16(C) && (ldc * ob) % 16 == 0);
     const void* A_use = A; int64_t lda_use = lda;
     const void* B_use = B; int64_t ldb_use = ldb;
     void* C_use = C; int64_t ldc_use = ldc;
@@ -307,6 +378,13 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     }
 
     const CUtensorMapDataType in_dt = in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (skinny) {
+        rc = run_skinny(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, dtype, b_nk, in_dt, stream);
+        if (rc != GEMM_OK) return rc;
+        p->last_kernel = kernel;
+        p->last_stream = stream; p->have_stream = true;
+        return GEMM_OK;
+    }
     const CUtensorMapDataType out_dt = (ob == 4) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                  : (in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     CUtensorMap tmA, tmB, tmC;
@@ -333,6 +411,7 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     prm.status = p->status_dev;
     prm.timeout_ns = p->timeout_ns;
     prm.debug = p->debug;
+    prm.l2_policy = p->l2_policy;
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t units = tiles < (cg == 2 ? p->max_pairs : p->max_singles) ? tiles : (cg == 2 ? p->max_pairs : p->max_singles);

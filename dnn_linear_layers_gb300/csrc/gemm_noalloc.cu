@@ -191,6 +191,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     prm.status = status;
     prm.timeout_ns = 1000000000ull;
     prm.debug = 0;
+    prm.l2_policy = 0;
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t cap = (cg == 2) ? s->max_pairs : s->max_singles;

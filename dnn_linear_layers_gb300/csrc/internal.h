@@ -44,6 +44,7 @@ struct TcParams {
     int* status;           // device status word (StatusBits)
     uint64_t timeout_ns;   // bound on any single wait
     uint32_t debug;        // DebugFlags
+    uint32_t l2_policy;    // 0: A evict_last, B evict_normal; 1: A normal, B last; 2: both normal
 };
 
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the
@@ -58,6 +59,29 @@ int tc_smem_bytes(int cta_group);
 // co-resident clusters (cta_group 2) or CTAs (cta_group 1) on this device.
 cudaError_t tc_prepare(int cta_group, int dtype, int* max_units);
 
+// Skinny-M (M <= 128) Linear layer: weight-streaming tcgen05 kernel ------
+struct SkinnyParams {
+    int32_t M, N, K;
+    int32_t mpad;          // M rounded up to a multiple of 16 (MMA N), <= 128
+    int32_t splits;        // k-slices per feature tile = cluster size (1, 2, 4, 8)
+    int32_t num_k_blocks;  // ceil(K / 64)
+    int32_t tmem_cols;     // TMEM columns allocated (power of two >= 32, >= mpad)
+    uint32_t epi;          // EpiFlags
+    uint32_t idesc;        // tcgen05 instruction descriptor (M = 128, N = mpad)
+    uint32_t w_mn_major;   // 1: W stored K x N (features contiguous); 0: N x K
+    const void* bias;      // N elements of the input type, or null
+    void* Y;               // output, M x N, row pitch ldy (elements)
+    int64_t ldy;
+    int* status;
+    uint64_t timeout_ns;
+};
+
+int skinny_smem_bytes(int mpad);
+cudaError_t skinny_prepare(int dtype);
+cudaError_t skinny_blocks_per_sm(int mpad, int* out);
+cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,
+                          int grid, cudaStream_t stream);
+
 // Auxiliary kernels ------------------------------------------------------
 // C[i][j] = epilogue(0) for K == 0 (bias and/or ReLU of an empty sum).
 cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,
@@ -66,5 +90,10 @@ cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bi
 // Copy a rows x cols matrix of elem_bytes-sized elements between strides.
 cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
                           int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+// im2col of an NHWC tensor for an R x S convolution (zero padding `pad`,
+// stride `stride`): out[(n*OH + oh)*OW + ow][(r*S + s)*C + c], row pitch ld_out.
+cudaError_t launch_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad,
+                          int stride, void* out, int64_t ld_out, int elem_bytes, cudaStream_t stream);
 
 }  // namespace gb300

@@ -7,7 +7,10 @@
 //    copy a padded result back out.  Padding rows to an aligned length is the
 //    "pad to a multiple of 16" advice of youngju.dev "GEMM to FlashAttention"
 //    (PyTorch tips) and the tile/burst alignment remark of the devpress.csdn.net
-//    notes, section 3.6.
+//    notes, section 3.6;
+//  * im2col: the explicit-GEMM form of a convolution, each R x S x C
+//    neighbourhood flattened into one row (CMU 15-418 notes, section 2.3), used
+//    to set up the convolution-as-GEMM workload.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -40,6 +43,41 @@ __global__ void copy2d_kernel(const T* __restrict__ src, int64_t ld_src, T* __re
         for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
              c += (int64_t)gridDim.x * blockDim.x)
             d[c] = s[c];
+    }
+}
+
+// im2col for a stride-s, zero-padded R x S convolution on NHWC input: one warp
+// per output row (n, oh, ow); the row is R*S segments of C contiguous input
+// channels, each copied in 16-byte pieces (or zero-filled outside the image).
+template <typename V>
+__global__ void im2col_kernel(const uint8_t* __restrict__ x, int64_t Nb, int64_t H, int64_t W, int64_t C,
+                              int R, int S, int pad, int stride, int64_t OH, int64_t OW,
+                              uint8_t* __restrict__ out, int64_t ld_out_bytes, int elem_bytes) {
+    const int64_t rows = Nb * OH * OW;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t seg_bytes = C * elem_bytes;
+    const int64_t vec_per_seg = seg_bytes / (int64_t)sizeof(V);
+    for (int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += warps) {
+        const int64_t n = row / (OH * OW);
+        const int64_t rem = row - n * OH * OW;
+        const int64_t oh = rem / OW, ow = rem - (rem / OW) * OW;
+        uint8_t* orow = out + row * ld_out_bytes;
+        for (int r = 0; r < R; ++r) {
+            const int64_t ih = oh * stride + r - pad;
+            for (int s = 0; s < S; ++s) {
+                const int64_t iw = ow * stride + s - pad;
+                V* dst = reinterpret_cast<V*>(orow + (int64_t)(r * S + s) * seg_bytes);
+                if (ih < 0 || ih >= H || iw < 0 || iw >= W) {
+                    V z;
+                    memset(&z, 0, sizeof(V));
+                    for (int64_t v = lane; v < vec_per_seg; v += 32) dst[v] = z;
+                } else {
+                    const V* src = reinterpret_cast<const V*>(x + ((n * H + ih) * W + iw) * seg_bytes);
+                    for (int64_t v = lane; v < vec_per_seg; v += 32) dst[v] = src[v];
+                }
+            }
+        }
     }
 }
 
@@ -95,6 +133,31 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
                                                               ld_dst, rows, cols);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad,
+                          int stride, void* out, int64_t ld_out, int elem_bytes, cudaStream_t stream) {
+    const int64_t OH = (H + 2 * pad - R) / stride + 1, OW = (W + 2 * pad - S) / stride + 1;
+    const int64_t rows = Nb * OH * OW;
+    if (rows <= 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    const int64_t seg = C * elem_bytes;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out) |
+                         (uintptr_t)(ld_out * elem_bytes) | (uintptr_t)seg;
+    if ((al & 15u) == 0)
+        im2col_kernel<uint4><<<(int)blocks, threads, 0, stream>>>((const uint8_t*)x, Nb, H, W, C, R, S, pad, stride,
+                                                                 OH, OW, (uint8_t*)out, ld_out * elem_bytes, elem_bytes);
+    else if ((al & 1u) == 0)
+        im2col_kernel<uint16_t><<<(int)blocks, threads, 0, stream>>>((const uint8_t*)x, Nb, H, W, C, R, S, pad,
+                                                                    stride, OH, OW, (uint8_t*)out,
+                                                                    ld_out * elem_bytes, elem_bytes);
+    else
+        im2col_kernel<uint8_t><<<(int)blocks, threads, 0, stream>>>((const uint8_t*)x, Nb, H, W, C, R, S, pad,
+                                                                   stride, OH, OW, (uint8_t*)out,
+                                                                   ld_out * elem_bytes, elem_bytes);
     return cudaGetLastError();
 }
 

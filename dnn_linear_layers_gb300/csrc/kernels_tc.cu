@@ -187,8 +187,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
             const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_PRODUCER};
-            const uint64_t pol_a = l2_policy_evict_normal();
-            const uint64_t pol_b = l2_policy_evict_last();
+            // The group walk reuses each A panel across every N tile of the group and
+            // each B panel only across the group's rows, so A is the operand to keep.
+            const uint64_t pol_a = p.l2_policy == 0 ? l2_policy_evict_last() : l2_policy_evict_normal();
+            const uint64_t pol_b = p.l2_policy == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
             uint32_t it = 0;
             bool ok = true;
             for (int tile = unit; tile < num_tiles && ok; tile += num_units) {

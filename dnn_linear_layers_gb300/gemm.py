@@ -39,6 +39,7 @@ SIGNATURES = {
     "gemm_plan_set_debug": (_int, [_vp, _uint]),
     "gemm_plan_workspace_bytes": (_i64, [_vp]),
     "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
+    "gemm_im2col": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp, _i64, _int, _vp]),
     "gemm_run_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _uint, _vp, _vp]),
 }
 
@@ -216,3 +217,17 @@ def linear(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None = No
     if out is None:
         out = torch.empty(x.shape[0], weight.shape[0], device=x.device, dtype=out_dtype)
     return _plan_for(x.device, "nk").run(x, weight, out, bias, relu)
+
+
+def im2col(x: torch.Tensor, R: int, S: int, pad: int = 0, stride: int = 1, out: torch.Tensor | None = None):
+    """Explicit-GEMM matrix of an R x S convolution of the NHWC tensor ``x``."""
+    if x.dim() != 4 or not x.is_contiguous() or x.device.type != "cuda":
+        raise ValueError("x must be a contiguous NHWC CUDA tensor")
+    Nb, H, W, C = x.shape
+    OH = (H + 2 * pad - R) // stride + 1
+    OW = (W + 2 * pad - S) // stride + 1
+    if out is None:
+        out = torch.empty((Nb * OH * OW, R * S * C), dtype=x.dtype, device=x.device)
+    _check(lib().gemm_im2col(x.data_ptr(), Nb, H, W, C, R, S, pad, stride, out.data_ptr(), _ld(out),
+                             x.element_size(), _stream_handle(None)), "gemm_im2col")
+    return out

@@ -110,6 +110,19 @@ int gemm_plan_destroy(gemm_plan_t plan);
 /* Static description of a return code. */
 const char* gemm_strerror(int code);
 
+/* Explicit-GEMM (im2col) matrix of a convolution (CMU 15-418 "DNNs and ML
+ * accelerators" notes, section 2.3: each R x S x C input neighbourhood becomes
+ * one row; weights w[f][r][s][c] then form the N x K operand of gemm_run with
+ * GEMM_B_NK).  x is NHWC (Nb x H x W x C, contiguous, device memory); out is
+ * (Nb*OH*OW) x (R*S*C) row-major with row pitch ld_out >= R*S*C elements,
+ * OH = (H + 2 pad - R) / stride + 1 (OW likewise):
+ *     out[(n*OH + oh)*OW + ow][(r*S + s)*C + c] = x[n][oh*stride+r-pad][ow*stride+s-pad][c]
+ * or 0 outside the image.  elem_bytes is the element size (2 for bf16/fp16).
+ * Enqueued on `stream`; both buffers are caller-owned; returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG or GEMM_ERR_CUDA. */
+int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad, int stride,
+                void* out, int64_t ld_out, int elem_bytes, void* stream);
+
 /* --- controls and introspection (benchmarks and tests) ------------------ */
 
 /* Force a kernel (GEMM_KERNEL_*); GEMM_KERNEL_AUTO restores the dispatcher. */

@@ -1,0 +1,86 @@
+"""Convolution as explicit GEMM on the GPU: the im2col kernel against the
+oracle's im2col (exact copy), and the im2col matrix times the weights against
+the oracle's direct seven-loop convolution.
+
+The full-size case is the 3 x 3, stride 1, pad 1 convolution of a batch of 32
+56 x 56 x 256 NHWC activations (ReLU(N(0,1))) with 256 filters w[f][r][s][c]
+~ N(0, 2/2304): M = 100352, K = 2304, N = 256.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dnn_linear_layers_gb300 import gemm as G
+from dnn_linear_layers_gb300.inputs import CONV, GemmCase, conv_tensors, int_bf16
+
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plan():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from dnn_linear_layers_gb300 import build
+    build.build()
+    p = G.Plan(0, "nk")
+    yield p
+    p.close()
+
+
+@pytest.mark.parametrize("shape", [(2, 9, 9, 16, 3, 3, 1, 1), (1, 7, 5, 3, 3, 3, 1, 1), (2, 8, 8, 8, 3, 3, 0, 2),
+                                   (1, 6, 6, 24, 5, 5, 2, 1), (3, 4, 4, 8, 1, 1, 0, 1)])
+def test_im2col_matches_oracle(plan, shape):
+    Nb, H, W, C, R, S, pad, stride = shape
+    x = int_bf16((Nb, H, W, C), sum(shape))
+    cols = G.im2col(x.cuda(), R, S, pad, stride)
+    torch.cuda.synchronize()
+    if stride == 1:
+        ref = oracle.im2col(x, R, S, pad)
+    else:   # the oracle's im2col is stride 1; pick the strided rows of a stride-1 matrix
+        full = oracle.im2col(x, R, S, pad)
+        OH1 = H + 2 * pad - R + 1; OW1 = W + 2 * pad - S + 1
+        OH = (H + 2 * pad - R) // stride + 1; OW = (W + 2 * pad - S) // stride + 1
+        idx = [(n * OH1 + oh * stride) * OW1 + ow * stride for n in range(Nb) for oh in range(OH) for ow in range(OW)]
+        ref = full[idx]
+    assert np.array_equal(cols.double().cpu().numpy(), ref)
+
+
+def test_small_conv_as_gemm_exact(plan):
+    x = int_bf16((2, 9, 9, 16), 5)
+    w = int_bf16((32, 3, 3, 16), 6)
+    cols = G.im2col(x.cuda(), 3, 3, 1, 1)
+    Y = torch.empty(cols.shape[0], 32, device="cuda")
+    plan.run(cols, w.reshape(32, -1).cuda(), Y)
+    assert plan.status() == 0
+    pos = [(n, oh, ow) for n in range(2) for oh in range(9) for ow in range(9)]
+    ref = oracle.conv2d_at(x, w, 1, pos)
+    assert np.array_equal(Y.double().cpu().numpy(), ref)
+
+
+def test_full_conv_config_sampled(plan):
+    Nb, H, W, Cin, Cout = CONV["Nb"], CONV["H"], CONV["W"], CONV["Cin"], CONV["Cout"]
+    x, w = conv_tensors()
+    xd = x.cuda()
+    cols = G.im2col(xd, 3, 3, 1, 1)                       # 100352 x 2304
+    Wm = w.reshape(Cout, -1)
+    Y = torch.empty(cols.shape[0], Cout, dtype=torch.bfloat16, device="cuda")
+    plan.set_kernel(G.KERNEL_AUTO)
+    plan.run(cols, Wm.cuda(), Y)
+    assert plan.status() == 0
+    rng = np.random.default_rng(4)
+    # border and interior positions of several images
+    pos = {(n, oh, ow) for n in (0, Nb - 1) for oh in (0, 1, H // 2, H - 1) for ow in (0, 1, W // 2, W - 1)}
+    pos |= {(int(rng.integers(Nb)), int(rng.integers(H)), int(rng.integers(W))) for _ in range(48)}
+    pos = sorted(pos)
+    rows = np.array([(n * H + oh) * W + ow for n, oh, ow in pos])
+    # the GPU im2col rows are the oracle's im2col rows, bit for bit
+    A_rows = oracle.im2col_rows(x, 3, 3, 1, rows)
+    assert np.array_equal(cols[torch.from_numpy(rows).cuda()].double().cpu().numpy(), A_rows)
+    C_ref, S = oracle.gemm(A_rows, Wm, b_nk=True, with_mag=True)
+    direct = oracle.conv2d_at(x, w, 1, pos)
+    assert np.all(np.abs(direct - C_ref) <= 1e-12 * (S + 1))
+    case = GemmCase("conv", len(rows), Cout, 9 * Cin, b_nk=True, out="bf16")
+    compare(case, Y[torch.from_numpy(rows).cuda()].cpu(), C_ref, S)

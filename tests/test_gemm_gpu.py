@@ -17,7 +17,8 @@ from parity import alloc_with_guard, compare, guard_intact, oracle_full, run_cas
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = {"single": G.KERNEL_TC_SINGLE, "pair": G.KERNEL_TC_PAIR}
+KERNELS = {"single": G.KERNEL_TC_SINGLE, "pair": G.KERNEL_TC_PAIR, "skinny": G.KERNEL_SKINNY,
+           "auto": G.KERNEL_AUTO}
 
 
 @pytest.fixture(scope="module")
@@ -39,6 +40,8 @@ def plan_for(plans, case):
 def check(plans, case, kernel=None):
     p = plan_for(plans, case)
     A, B, bias, C = run_case(p, case, kernel=KERNELS.get(kernel, kernel) if kernel else G.KERNEL_AUTO)
+    if kernel and kernel != "auto":
+        assert p.last_kernel == KERNELS.get(kernel, kernel)
     C_ref, S = oracle_full(case, A, B, bias)
     return compare(case, C, C_ref, S)
 
@@ -89,11 +92,43 @@ def test_fp16_inputs(plans, out, integer):
 TAILS = [1, 7, 127, 129, 255, 257]
 
 
+@pytest.mark.parametrize("kernel", ["auto", "single", "pair"])
 @pytest.mark.parametrize("M", TAILS)
 @pytest.mark.parametrize("N", [8, 129, 264])
 @pytest.mark.parametrize("K", [8, 72, 264])
-def test_tails_integer_exact(plans, M, N, K):
-    check(plans, GemmCase("tails", M, N, K, out="f32", integer=True, seed=M + N + K))
+def test_tails_integer_exact(plans, M, N, K, kernel):
+    check(plans, GemmCase("tails", M, N, K, out="f32", integer=True, seed=M + N + K), kernel)
+
+
+# ------------------------------------------------------------ skinny-M path
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 64, 100, 128])
+@pytest.mark.parametrize("b_nk", [True, False])
+def test_skinny_integer_exact(plans, M, b_nk):
+    check(plans, GemmCase("skinny_int", M, 1000, 1000, b_nk=b_nk, bias=True, relu=True, out="bf16",
+                          integer=True, seed=M), "skinny")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 4096), (3, 300, 520), (16, 4096, 64), (33, 700, 2000), (128, 257, 8)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_skinny_float_within_tolerance(plans, M, N, K, out):
+    check(plans, GemmCase("skinny_f", M, N, K, b_nk=True, bias=True, out=out, b_std=K ** -0.5, seed=N), "skinny")
+
+
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_skinny_fp16(plans, out):
+    check(plans, GemmCase("skinny_h", 16, 520, 1000, b_nk=True, in_dtype="f16", out=out, integer=True,
+                          bias=True, seed=4), "skinny")
+
+
+def test_skinny_is_auto_choice_for_small_m(plans):
+    p = plans["nk"]
+    A = torch.ones(4, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.ones(512, 256, dtype=torch.bfloat16, device="cuda")
+    C = torch.empty(4, 512, device="cuda")
+    p.set_kernel(G.KERNEL_AUTO)
+    p.run(A, W, C)
+    assert p.status() == 0 and p.last_kernel == G.KERNEL_SKINNY
+    assert torch.all(C == 256.0)
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (129, 77, 1000), (257, 1001, 99)])
