@@ -179,7 +179,8 @@ def run_ours(args):
     A, B = A_h.to(dev), B_h.to(dev)
     bias = bias_h.to(dev) if bias_h is not None else None
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    plan = G.Plan(local_rank, lay)
+    # Linear-layer weights are constant model parameters: say so to the plan
+    plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"))
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
     nbytes_step = R.gemm_bytes(M, N, K, 2, 2, 2, 2 if has_bias else 0)
@@ -193,42 +194,72 @@ def run_ours(args):
     def step():
         a, b, c = copies[counter[0] % n_copies]
         counter[0] += 1
-        plan.run(a, b, c, bias, relu, stream=stream)
+        plan.run(a, b, c, bias, relu)          # on torch's current stream
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert plan.status() == 0, "device status after warm-up"
 
+    # The K timed steps are captured once into a CUDA graph and replayed, so
+    # the GPU runs them back to back with no host launch gaps between steps
+    # (short decode-like kernels would otherwise time the Python launch path).
+    graph = None
+    launches0 = plan.launch_count
+    if not args.no_graph:
+        try:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                step()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize()
+            launches0 = plan.launch_count
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(args.steps):
+                    step()
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture unsupported: time eager launches instead
+            graph = None
+            print(f"# graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            torch.cuda.synchronize()
+    launches_per_run = plan.launch_count - launches0
+
+    def timed_run():
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(args.steps):
+                step()
+
+    timed_run()
+    torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if not args.no_clocks else None
     # keep the GPU busy ~1 s (untimed) so the sampler is running and clocks settle
     t_end = time.time() + (1.0 if sampler else 0.0)
     while time.time() < t_end:
-        for _ in range(20):
-            step()
+        timed_run()
         torch.cuda.synchronize()
 
     launches0 = plan.launch_count
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
+    timed_run()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    launches = plan.launch_count - launches0
+    launches = launches_per_run if graph is not None else plan.launch_count - launches0
     if sampler:
         sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
-    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    # steps run back to back on one stream: the average launch lasts total / K
+    # (for single-kernel steps; with packing, a step also holds the copies)
+    kernel_ms = total_ms / args.steps
     st = plan.status()
     assert st == 0, f"device status {st}"
 
@@ -247,7 +278,7 @@ def run_ours(args):
     def e2e_step():
         A_e.copy_(A_p, non_blocking=True)
         B_e.copy_(B_p, non_blocking=True)
-        plan.run(A_e, B_e, C_e, bias, relu, stream=stream)
+        plan.run(A_e, B_e, C_e, bias, relu)
         C_p.copy_(C_e, non_blocking=True)
 
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -295,7 +326,8 @@ def run_ours(args):
                        "l2": (f"inputs larger than L2 ({nbytes / 1e6:.1f} MB > {l2 / 1e6:.0f} MB), no flush"
                               if n_copies == 1 else
                               f"{n_copies} rotating operand copies ({n_copies * nbytes / 1e6:.0f} MB > 2 x L2)"),
-                       "kernel": {1: "tc_pair", 2: "tc_single"}.get(plan.last_kernel, str(plan.last_kernel))},
+                       "kernel": {1: "tc_pair", 2: "tc_single", 4: "skinny"}.get(plan.last_kernel, str(plan.last_kernel)),
+                       "timing": "CUDA graph of the K steps, one replay" if graph is not None else "eager launches"},
             "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                          "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
                          "frac": round(achieved / peak, 4),
@@ -390,6 +422,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a graph replay")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

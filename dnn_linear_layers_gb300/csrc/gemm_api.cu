@@ -3,6 +3,7 @@
 // youngju.dev "GEMM to FlashAttention" ("GEMM interface": m, n, k, lda, ldb,
 // ldc, transb) and the handle create/use/destroy pattern of its cuBLAS
 // example, for row-major operands and alpha = 1, beta = 0.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -30,7 +31,13 @@ struct gemm_plan {
     unsigned debug = 0;
     int group_m = 16;
     unsigned l2_policy = 0;
-    int skinny_per_sm[9] = {0};   // co-resident skinny CTAs per SM, by mpad / 16
+    unsigned pdl = 1;             // programmatic dependent launch of the GEMM kernels
+    int debug_log = 0;            // GB300_GEMM_DEBUG=1: one line per launch on stderr
+    int skinny_splits = 0;        // 0: automatic; otherwise forced split count (sweeps)
+    int skinny_stages = 0;        // 0: automatic; otherwise forced ring depth (sweeps)
+    int skinny_x_lsu = 0;         // 1: skinny kernel copies X with cp.async (sweeps)
+    int smem_per_sm = 0;          // shared memory of one SM (bytes)
+    int smem_reserved = 0;        // shared memory the system reserves per CTA (bytes)
     cudaStream_t last_stream = nullptr;
     bool have_stream = false;
 };
@@ -131,9 +138,44 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     const int64_t n_tiles = (N + 127) / 128;
     const int64_t nkb = (K + 63) / 64;
     if (n_tiles > INT32_MAX / 8) return GEMM_ERR_UNSUPPORTED;
-    const int64_t slots = (int64_t)p->sm_count * p->skinny_per_sm[mpad / 16];
-    int S = 1;
-    while (S < 8 && n_tiles * (S * 2) <= slots && S * 2 <= nkb) S *= 2;
+    // Weight bytes in flight decide the bandwidth, and only resident CTAs have
+    // loads in flight: take the largest split count S whose grid (n_tiles * S
+    // CTAs) fits on the SMs at once with a ring of at least 3 stages.
+    // Bandwidth follows the weight bytes in flight, and only resident CTAs have
+    // loads in flight.  Candidates (splits S <= 8, ring depth >= 3) are kept
+    // when the whole grid fits on the SMs with 20% headroom for placing
+    // clusters inside GPCs; the one with the most weight bytes in flight
+    // (counting at most four stages per CTA) wins, ties going to more CTAs.  (Measured on GB300: grids at the residency
+    // limit fall into a second wave, and 16-CTA clusters were slower.)
+    const int64_t stage_bytes = 16384 + (int64_t)mpad * 128;
+    int S = 1, stages = 2;
+    int64_t best = -1;
+    for (int cand = 8; cand >= 1; cand /= 2) {
+        if (cand > nkb && cand > 1) continue;
+        if (p->skinny_splits && cand != p->skinny_splits) continue;
+        const int64_t ctas = n_tiles * cand;
+        const int64_t kb_per_slice = nkb / cand;
+        for (int st = 8; st >= 2; --st) {
+            if (p->skinny_stages && st != p->skinny_stages) continue;
+            if (st < 3 && !p->skinny_stages && cand > 1) continue;
+            const int64_t smem = skinny_smem_bytes(mpad, st);
+            if (smem > 227 * 1024) continue;
+            int64_t per_sm = p->smem_per_sm / (smem + p->smem_reserved);
+            if (per_sm > 2048 / 192) per_sm = 2048 / 192;
+            if (per_sm > 512 / tmem_cols) per_sm = 512 / tmem_cols;
+            if (ctas * 10 > (int64_t)p->sm_count * per_sm * 8) continue;   // not resident with headroom
+            // depth beyond four stages earns nothing: more CTAs beat a deeper ring
+            int64_t depth = st < kb_per_slice ? st : kb_per_slice;
+            if (depth > 4) depth = 4;
+            const int64_t score = ctas * depth;
+            if (score > best) { best = score; S = cand; stages = st; }
+            break;
+        }
+    }
+    if (best < 0) {   // nothing resident in one wave: one slice per tile, shallow ring, several waves
+        S = p->skinny_splits ? (int)(p->skinny_splits <= nkb ? p->skinny_splits : 1) : 1;
+        stages = p->skinny_stages ? p->skinny_stages : 3;
+    }
     CUtensorMap tmW, tmX;
     const bool okw = w_nk ? make_map(&tmW, in_dt, W, (uint64_t)K, (uint64_t)N, (uint64_t)ldw * 2, 64, 128)
                           : make_map(&tmW, in_dt, W, (uint64_t)N, (uint64_t)K, (uint64_t)ldw * 2, 64, 64);
@@ -143,7 +185,12 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     SkinnyParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.M = (int32_t)M; sp.N = (int32_t)N; sp.K = (int32_t)K;
-    sp.mpad = mpad; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
+    sp.mpad = mpad; sp.stages = stages;
+    sp.w_prefetch = (p->pdl && (p->flags & GEMM_B_CONST)) ? 1u : 0u;
+    // X by TMA; the cp.async loader in the epilogue warps measured equal for
+    // M <= 16 and slower for M = 128 on GB300, so it is only a sweep option
+    sp.x_lsu = p->skinny_x_lsu ? 1u : 0u;
+    sp.X = X; sp.ldx = ldx; sp.pdl = p->pdl; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
     sp.epi = epi;
     const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;
     sp.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((w_nk ? 0u : 1u) << 15) | ((uint32_t)(mpad >> 3) << 17) |
@@ -153,6 +200,10 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     sp.Y = Y; sp.ldy = ldy;
     sp.status = p->status_dev;
     sp.timeout_ns = p->timeout_ns;
+    if (p->debug_log)
+        std::fprintf(stderr, "[gemm] skinny M=%lld N=%lld K=%lld mpad=%d tiles=%lld splits=%d stages=%d smem=%d "
+                     "prefetch=%u pdl=%u x_lsu=%u\n", (long long)M, (long long)N, (long long)K, mpad, (long long)n_tiles, S,
+                     stages, skinny_smem_bytes(mpad, stages), sp.w_prefetch, sp.pdl, sp.x_lsu);
     cudaError_t e = launch_skinny(dtype, tmW, tmX, sp, (int)(n_tiles * S), stream);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
@@ -168,7 +219,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
     if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_F16_F16OUT) return GEMM_ERR_INVALID_ARG;
-    if (flags & ~GEMM_B_NK) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~(GEMM_B_NK | GEMM_B_CONST)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
     if ((epilogue & GEMM_EPI_BIAS) && bias == nullptr) return GEMM_ERR_INVALID_ARG;
@@ -182,7 +233,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
 }
 
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
-    if (plan == nullptr || device < 0 || (flags & ~GEMM_B_NK)) return GEMM_ERR_INVALID_ARG;
+    if (plan == nullptr || device < 0 || (flags & ~(GEMM_B_NK | GEMM_B_CONST))) return GEMM_ERR_INVALID_ARG;
     int ndev = 0;
     cudaError_t e = cudaGetDeviceCount(&ndev);
     if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
@@ -211,10 +262,8 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
         e = skinny_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
     }
-    for (int b = 1; b <= 8; ++b) {
-        e = skinny_blocks_per_sm(16 * b, &p->skinny_per_sm[b]);
-        if (e != cudaSuccess || p->skinny_per_sm[b] < 1) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
-    }
+    p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
+    p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
     e = cudaMalloc(&p->status_dev, sizeof(int));
     if (e != cudaSuccess) { delete p; return GEMM_ERR_NO_MEMORY; }
     e = cudaMemset(p->status_dev, 0, sizeof(int));
@@ -223,6 +272,19 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     if (const char* s = std::getenv("GB300_GEMM_GROUP_M")) {
         int v = std::atoi(s);
         if (v >= 1 && v <= 1024) p->group_m = v;
+    }
+    if (const char* s = std::getenv("GB300_GEMM_DEBUG")) p->debug_log = std::atoi(s) != 0;
+    if (const char* s = std::getenv("GB300_GEMM_SKINNY_X_LSU")) p->skinny_x_lsu = std::atoi(s) != 0;
+    if (const char* s = std::getenv("GB300_GEMM_SKINNY_SPLITS")) {
+        int v = std::atoi(s);
+        if (v == 1 || v == 2 || v == 4 || v == 8) p->skinny_splits = v;
+    }
+    if (const char* s = std::getenv("GB300_GEMM_SKINNY_STAGES")) {
+        int v = std::atoi(s);
+        if (v >= 2 && v <= 8) p->skinny_stages = v;
+    }
+    if (const char* s = std::getenv("GB300_GEMM_NO_PDL")) {
+        if (std::atoi(s) != 0) p->pdl = 0;
     }
     if (const char* s = std::getenv("GB300_GEMM_L2_POLICY")) {
         int v = std::atoi(s);
@@ -412,9 +474,14 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     prm.timeout_ns = p->timeout_ns;
     prm.debug = p->debug;
     prm.l2_policy = p->l2_policy;
+    prm.pdl = p->pdl;
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t units = tiles < (cg == 2 ? p->max_pairs : p->max_singles) ? tiles : (cg == 2 ? p->max_pairs : p->max_singles);
+    if (p->debug_log)
+        std::fprintf(stderr, "[gemm] tc cta_group=%d M=%lld N=%lld K=%lld tiles=%lld grid=%lld packed=%d%d%d\n", cg,
+                     (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(units * cg),
+                     A_use != A, B_use != B, C_use != C);
     e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;

@@ -45,6 +45,7 @@ struct TcParams {
     uint64_t timeout_ns;   // bound on any single wait
     uint32_t debug;        // DebugFlags
     uint32_t l2_policy;    // 0: A evict_last, B evict_normal; 1: A normal, B last; 2: both normal
+    uint32_t pdl;          // host only: launch with programmatic stream serialisation
 };
 
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the
@@ -63,6 +64,7 @@ cudaError_t tc_prepare(int cta_group, int dtype, int* max_units);
 struct SkinnyParams {
     int32_t M, N, K;
     int32_t mpad;          // M rounded up to a multiple of 16 (MMA N), <= 128
+    int32_t stages;        // depth of the operand ring (2..8)
     int32_t splits;        // k-slices per feature tile = cluster size (1, 2, 4, 8)
     int32_t num_k_blocks;  // ceil(K / 64)
     int32_t tmem_cols;     // TMEM columns allocated (power of two >= 32, >= mpad)
@@ -74,11 +76,15 @@ struct SkinnyParams {
     int64_t ldy;
     int* status;
     uint64_t timeout_ns;
+    uint32_t pdl;          // host only: launch with programmatic stream serialisation
+    uint32_t w_prefetch;   // 1: W may be read before the previous kernel of the stream ends
+    uint32_t x_lsu;        // 1: the epilogue warps copy X with cp.async instead of TMA
+    const void* X;         // X (M x K, row pitch ldx elements), for the cp.async path
+    int64_t ldx;
 };
 
-int skinny_smem_bytes(int mpad);
+int skinny_smem_bytes(int mpad, int stages);
 cudaError_t skinny_prepare(int dtype);
-cudaError_t skinny_blocks_per_sm(int mpad, int* out);
 cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,
                           int grid, cudaStream_t stream);
 
@@ -88,6 +94,8 @@ cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bi
                                  void* C, int64_t ldc, cudaStream_t stream);
 
 // Copy a rows x cols matrix of elem_bytes-sized elements between strides.
+// When the destination is 16-byte aligned with ld_dst >= cols rounded up to
+// 16 bytes, the columns up to that boundary are zero-filled as well.
 cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
                           int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
 

@@ -46,6 +46,39 @@ __global__ void copy2d_kernel(const T* __restrict__ src, int64_t ld_src, T* __re
     }
 }
 
+// Vectorised 2-D copy where one side is 16-byte aligned (the plan's packed
+// workspace): each thread moves one 16-byte piece of a row.  Packing
+// (dst_aligned) gathers the piece from the unaligned source element by element
+// and writes it in one store, zero-filling the columns past `cols` up to the
+// 16-byte boundary of the padded row; unpacking reads the aligned piece in one
+// load and stores only the elements inside `cols`.
+template <typename T>
+__global__ void copy2d_vec_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
+                                  int64_t rows, int64_t cols, int dst_aligned) {
+    constexpr int V = 16 / sizeof(T);
+    const int64_t chunks = (cols + V - 1) / V;
+    const int64_t total = rows * chunks;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / chunks;
+        const int64_t c0 = (t - r * chunks) * V;
+        const T* s = src + r * ld_src + c0;
+        T* d = dst + r * ld_dst + c0;
+        if (dst_aligned) {
+            union { uint4 u; T e[V]; } v;
+#pragma unroll
+            for (int j = 0; j < V; ++j) v.e[j] = (c0 + j < cols) ? s[j] : T(0);
+            *reinterpret_cast<uint4*>(d) = v.u;
+        } else {
+            union { uint4 u; T e[V]; } v;
+            v.u = *reinterpret_cast<const uint4*>(s);
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (c0 + j < cols) d[j] = v.e[j];
+        }
+    }
+}
+
 // im2col for a stride-s, zero-padded R x S convolution on NHWC input: one warp
 // per output row (n, oh, ow); the row is R*S segments of C contiguous input
 // channels, each copied in 16-byte pieces (or zero-filled outside the image).
@@ -121,6 +154,23 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
                           int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     const int threads = 256;
+    const int64_t V = 16 / elem_bytes;
+    const int64_t padded = (cols + V - 1) / V * V;
+    const bool dst_vec = ((reinterpret_cast<uintptr_t>(dst) | (uintptr_t)(ld_dst * elem_bytes)) & 15u) == 0 &&
+                         ld_dst >= padded;
+    const bool src_vec = ((reinterpret_cast<uintptr_t>(src) | (uintptr_t)(ld_src * elem_bytes)) & 15u) == 0 &&
+                         ld_src >= padded;
+    if ((elem_bytes == 2 || elem_bytes == 4) && (dst_vec || src_vec)) {
+        int64_t blocks = (rows * (padded / V) + threads - 1) / threads;
+        if (blocks > 152 * 32) blocks = 152 * 32;
+        if (elem_bytes == 2)
+            copy2d_vec_kernel<uint16_t><<<(int)blocks, threads, 0, stream>>>(
+                (const uint16_t*)src, ld_src, (uint16_t*)dst, ld_dst, rows, cols, dst_vec ? 1 : 0);
+        else
+            copy2d_vec_kernel<uint32_t><<<(int)blocks, threads, 0, stream>>>(
+                (const uint32_t*)src, ld_src, (uint32_t*)dst, ld_dst, rows, cols, dst_vec ? 1 : 0);
+        return cudaGetLastError();
+    }
     int64_t bx = (cols + threads - 1) / threads;
     if (bx > 64) bx = 64;
     int64_t by = rows < 65535 ? rows : 65535;

@@ -31,12 +31,35 @@ namespace gb300 {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 6;
+constexpr int kMaxStages = 8;
 constexpr int kWStage = 128 * 64 * 2;      // 128 features x 64 k, 16 KB
+constexpr int kMiscBytes = 1024;
 
 __device__ __forceinline__ void cluster_arrive_wait() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16-byte global -> shared copy through the load/store path; bytes past
+// `src_bytes` (0..16) are written as zeros.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// wait until at most `n` (0..7) of this thread's copy groups are still pending
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+    }
 }
 
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
@@ -97,16 +120,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
     const int mpad = p.mpad;                          // 16..128, multiple of 16
+    const int kStages = p.stages;                     // 2..kMaxStages
     const uint32_t x_stage = (uint32_t)mpad * 128u;   // mpad tokens x 64 k x 2 B
     const uint32_t off_x = kStages * kWStage;
     const uint32_t off_misc = off_x + kStages * x_stage;   // multiple of 1024
     const uint32_t misc = base + off_misc;
     auto bar_full = [&](int s) { return misc + 8u * s; };
-    auto bar_empty = [&](int s) { return misc + 8u * (kStages + s); };
-    const uint32_t bar_acc = misc + 8u * (2 * kStages);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + off_misc + 8 * (2 * kStages + 1));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + off_misc + 8 * (2 * kStages + 1) + 4);
-    // partial tile red[m][f] (fp32, token-major) reuses the front of the W ring
+    auto bar_empty = [&](int s) { return misc + 8u * (kMaxStages + s); };
+    const uint32_t bar_acc = misc + 8u * (2 * kMaxStages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + off_misc + 8 * (2 * kMaxStages + 1));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + off_misc + 8 * (2 * kMaxStages + 1) + 4);
+    // partial tile red[m][f] (fp32, token-major, mpad x 128 x 4 B) reuses the
+    // front of the operand ring, which is at least that large for mpad <= 128
     float* red = reinterpret_cast<float*>(base_ptr);
     const uint32_t red_addr = base;
 
@@ -120,8 +145,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int kb_end = (int)(((int64_t)(rank + 1) * nkb) / S);
 
     if (threadIdx.x == 0) {
+        // a stage is full once the producer's W bytes have landed and, when the
+        // epilogue warps copy X, each of those four warps has arrived
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full(s), 1);
+            mbar_init(bar_full(s), p.x_lsu ? 5 : 1);
             mbar_init(bar_empty(s), 1);
         }
         mbar_init(bar_acc, 1);
@@ -138,27 +165,50 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Everything above overlaps the previous kernel's tail; no global memory
+    // (operands, bias, output) is touched before the stream's earlier work is
+    // done -- except W, which the producer may start streaming first when the
+    // caller declared it constant.
+    const bool producer = warp == 0 && lane == 0;
+    if (!producer) grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
             const BoundedWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_PRODUCER};
             const uint64_t pol_w = l2_policy_evict_normal();   // streamed once
             const uint64_t pol_x = l2_policy_evict_last();     // read by every CTA
-            bool ok = true;
-            for (int kb = kb_begin, it = 0; kb < kb_end; ++kb, ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!w(bar_empty(s), ph ^ 1u)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar_full(s), kWStage + x_stage);
+            auto load_w = [&](int s, int k0) {
                 const uint32_t sw = base + s * kWStage;
-                const int k0 = kb * 64;
                 if (p.w_mn_major) {
                     tma_load_2d(sw, &tmW, bar_full(s), f0, k0, pol_w);
                     tma_load_2d(sw + 8192, &tmW, bar_full(s), f0 + 64, k0, pol_w);
                 } else {
                     tma_load_2d(sw, &tmW, bar_full(s), k0, f0, pol_w);
                 }
-                tma_load_2d(base + off_x + s * x_stage, &tmX, bar_full(s), k0, 0, pol_x);
+            };
+            // first ring of W before the dependency wait (constant weights only);
+            // the ring's stages start empty, so no empty-barrier wait is needed
+            const int nk = kb_end - kb_begin;
+            const int pre = p.w_prefetch ? (nk < kStages ? nk : kStages) : 0;
+            const uint32_t tx = kWStage + (p.x_lsu ? 0u : x_stage);
+            for (int it = 0; it < pre; ++it) {
+                mbar_arrive_expect_tx(bar_full(it), tx);
+                load_w(it, (kb_begin + it) * 64);
+            }
+            grid_dependency_wait();
+            if (!p.x_lsu)
+                for (int it = 0; it < pre; ++it)
+                    tma_load_2d(base + off_x + it * x_stage, &tmX, bar_full(it), (kb_begin + it) * 64, 0, pol_x);
+            bool ok = true;
+            for (int it = pre; it < nk; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                if (!w(bar_empty(s), ph ^ 1u)) { ok = false; break; }
+                mbar_arrive_expect_tx(bar_full(s), tx);
+                const int k0 = (kb_begin + it) * 64;
+                load_w(s, k0);
+                if (!p.x_lsu) tma_load_2d(base + off_x + s * x_stage, &tmX, bar_full(s), k0, 0, pol_x);
             }
             if (!ok) {
                 const uint64_t t0 = globaltimer_ns();
@@ -187,6 +237,52 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // signals the epilogue once every MMA above has completed
             tc_commit_1(bar_acc);
         }
+    }
+
+    // ---- X tiles through the load/store path (epilogue warps, idle until the
+    // accumulator is ready), leaving the TMA unit to the weight stream.  Each
+    // 16-byte piece j of token row r lands at the 128-byte-swizzled position
+    // r*128 + ((j ^ (r % 8)) * 16) the MMA descriptor expects; pieces past M or
+    // K are zero-filled.  A stage is handed over (proxy fence, then one arrival
+    // per warp) once its copies are complete, up to stages-1 stages behind the
+    // issue (the producer of a stage needs the MMA to have drained the stage
+    // issued `stages` earlier, which this lag guarantees has been handed over).
+    if (warp >= 2 && p.x_lsu) {
+        const int lag = kStages - 1;
+        const BoundedWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
+        const int et = (int)threadIdx.x - 64;          // 0..127
+        const int nk = kb_end - kb_begin;
+        const char* X = reinterpret_cast<const char*>(p.X);
+        auto hand_over = [&](int it) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(bar_full(it % kStages));
+        };
+        bool ok = true;
+        for (int it = 0; it < nk; ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            const bool free_slot = w(bar_empty(s), ph ^ 1u);
+            if (!__all_sync(0xffffffffu, free_slot)) { ok = false; break; }
+            const int k0 = (kb_begin + it) * 64;
+            const uint32_t xs = base + off_x + s * x_stage;
+            for (int c = et; c < mpad * 8; c += 128) {
+                const int r = c >> 3, j = c & 7;
+                const int kk = k0 + j * 8;
+                uint32_t bytes = 0;
+                if (r < p.M && kk < p.K) bytes = (p.K - kk) >= 8 ? 16u : (uint32_t)(p.K - kk) * 2u;
+                const void* src = bytes ? (const void*)(X + ((int64_t)r * p.ldx + kk) * 2) : p.X;
+                cp_async_16(xs + r * 128 + ((j ^ (r & 7)) << 4), src, bytes);
+            }
+            cp_async_commit();
+            if (it >= lag) {
+                cp_async_wait_n(lag);
+                hand_over(it - lag);
+            }
+        }
+        cp_async_wait<0>();
+        if (ok)
+            for (int it = nk - lag < 0 ? 0 : nk - lag; it < nk; ++it) hand_over(it);
     }
 
     // ---- partial tile: TMEM -> smem (all MMAs done, ring no longer in use)
@@ -250,31 +346,37 @@ cudaError_t launch_skinny_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, c
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = skinny_smem_bytes(p.mpad);
+    cfg.dynamicSmemBytes = skinny_smem_bytes(p.mpad, p.stages);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.splits;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<InT, OutT>, tmW, tmX, p);
 }
 
 template <typename InT, typename OutT>
 cudaError_t prepare_skinny_impl() {
+    const int most = 227 * 1024;   // rings are sized on the host; this is the per-CTA ceiling
     cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         skinny_smem_bytes(128));
+                                         most);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 }  // namespace
 
-int skinny_smem_bytes(int mpad) {
-    return kStages * kWStage + kStages * mpad * 128 + 1024 /*misc*/ + 1024 /*alignment*/;
+int skinny_smem_bytes(int mpad, int stages) {
+    return stages * (kWStage + mpad * 128) + kMiscBytes + 1024 /*alignment*/;
 }
+
 
 cudaError_t skinny_prepare(int dtype) {
     switch (dtype) {
@@ -286,10 +388,7 @@ cudaError_t skinny_prepare(int dtype) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t skinny_blocks_per_sm(int mpad, int* out) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemm_skinny_kernel<__nv_bfloat16, __nv_bfloat16>,
-                                                         kThreads, skinny_smem_bytes(mpad));
-}
+
 
 cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,
                           int grid, cudaStream_t stream) {

@@ -179,6 +179,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_ptr_smem;
+    // The prologue above may overlap the previous kernel of the stream; no
+    // operand, bias or output is touched until that kernel has finished.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int num_tiles = p.num_m_tiles * p.num_n_tiles;
     const int nkb = p.num_k_blocks;
@@ -392,13 +396,15 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TcCfg<CG>::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, InT, OutT>, tmA, tmB, tmC, p);
 }
 

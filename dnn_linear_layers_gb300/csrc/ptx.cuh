@@ -58,6 +58,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                  :: "r"(cluster_bar) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch ----
+// Block until the grids this one depends on (the previous kernels of the
+// stream, when launched with programmatic stream serialisation) have finished
+// and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel of the stream to start its prologue on free SMs.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- cluster ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

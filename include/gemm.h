@@ -69,6 +69,11 @@ typedef enum {
 /* Plan flags. */
 #define GEMM_B_KN 0u   /* B is K x N (default) */
 #define GEMM_B_NK 1u   /* B is a Linear weight W, N x K */
+/* B is constant while the plan's kernels may run (model weights): no earlier
+ * work on the stream writes it.  Lets the small-M kernel start streaming B
+ * while the previous kernel of the stream is still finishing; A, bias and C
+ * are still touched only after that kernel is done. */
+#define GEMM_B_CONST 2u
 
 /* Kernel selection (gemm_plan_set_kernel / gemm_plan_last_kernel). */
 #define GEMM_KERNEL_AUTO 0
@@ -86,7 +91,8 @@ typedef enum {
 #define GEMM_ERR_DEVICE_TIMEOUT (-5)  /* a device-side wait ran out of time    */
 #define GEMM_ERR_NO_MEMORY (-6)       /* workspace allocation failed           */
 
-/* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK.
+/* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK,
+ * optionally | GEMM_B_CONST.
  * Allocates the plan and its device status word; restores the caller's
  * current device before returning.  *plan is set only on success. */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);

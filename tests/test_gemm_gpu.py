@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from dnn_linear_layers_gb300 import gemm as G
-from dnn_linear_layers_gb300.inputs import GemmCase, SMALL_F32
+from dnn_linear_layers_gb300.inputs import GemmCase, SMALL_F32, int_bf16
 
 from parity import alloc_with_guard, compare, guard_intact, oracle_full, run_case
 
@@ -118,6 +118,36 @@ def test_skinny_float_within_tolerance(plans, M, N, K, out):
 def test_skinny_fp16(plans, out):
     check(plans, GemmCase("skinny_h", 16, 520, 1000, b_nk=True, in_dtype="f16", out=out, integer=True,
                           bias=True, seed=4), "skinny")
+
+
+@pytest.mark.parametrize("b_const", [False, True])
+def test_skinny_chained_layers_see_previous_outputs(plans, b_const):
+    """Back-to-back layers on one stream, each reading the previous layer's
+    output: with programmatic dependent launch (and constant-weight prefetch)
+    no kernel may read its input before the producing kernel is done.
+    Integer data keeps every value exact (|y1| <= 128 fits bf16)."""
+    p = G.Plan(0, "nk", b_const=b_const)
+    p.set_kernel(G.KERNEL_SKINNY)
+    M, D = 16, 128
+    Ws = [int_bf16((D, D), 40 + i, lo=-1, hi=1) for i in range(6)]
+    x = int_bf16((M, D), 39, lo=-1, hi=1)
+    Wd = [w.cuda() for w in Ws]
+    h = x.cuda()
+    outs = []
+    for i, w in enumerate(Wd):       # alternate a 0/1 clamp layer to keep values small
+        y = torch.empty(M, D, dtype=torch.bfloat16, device="cuda")
+        p.run(h, w, y, relu=True)
+        h = torch.clamp(y, max=1.0) if i % 2 else y
+        outs.append(h)
+    assert p.status() == 0
+    ref = x.double().numpy()
+    for i, w in enumerate(Ws):
+        ref = oracle.gemm(ref, w, relu=True, b_nk=True)
+        ref = oracle.bf16_round(ref)
+        if i % 2:
+            ref = np.minimum(ref, 1.0)
+        assert np.array_equal(outs[i].double().cpu().numpy(), ref), f"layer {i}"
+    p.close()
 
 
 def test_skinny_is_auto_choice_for_small_m(plans):
