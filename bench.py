@@ -41,6 +41,8 @@ WORKLOADS = {
     # name: (M, N, K, b_layout, epilogue(bias, relu), out, a_std, b_std)
     "square8192_bf16": (8192, 8192, 8192, "kn", (False, False), "bf16", 1.0, 1.0),
     "square4096_bf16": (4096, 4096, 4096, "kn", (False, False), "bf16", 1.0, 1.0),
+    "square8192_nk_bf16": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
+    "square4096_nk_bf16": (4096, 4096, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
     "qkv_8192x4096x12288": (8192, 12288, 4096, "kn", (False, False), "bf16", 1.0, 4096 ** -0.5),
     "ffn_up_8192x4096x14336": (8192, 14336, 4096, "kn", (True, True), "bf16", 1.0, 4096 ** -0.5),
     "ffn_down_8192x14336x4096": (8192, 4096, 14336, "kn", (True, False), "bf16", 1.0, 14336 ** -0.5),

@@ -65,8 +65,9 @@ int setup_device(int dev, DeviceSetup** out) {
         if (e != cudaSuccess || addr == nullptr) { cudaGetLastError(); return GEMM_ERR_CUDA; }
         int n2 = 0, n1 = 0;
         for (int dt = 0; dt < 4; ++dt) {
-            e = gb300::tc_prepare(2, dt, &n2);
-            if (e == cudaSuccess) e = gb300::tc_prepare(1, dt, &n1);
+            int n4 = 0;
+            e = gb300::tc_prepare(2, dt, &n2, &n4);
+            if (e == cudaSuccess) e = gb300::tc_prepare(1, dt, &n1, &n4);
             if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
         }
         if (n2 < 1 || n1 < 1) return GEMM_ERR_UNSUPPORTED;
@@ -192,6 +193,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     prm.timeout_ns = 1000000000ull;
     prm.debug = 0;
     prm.l2_policy = 0;
+    prm.num_full = prm.num_m_tiles * prm.num_n_tiles;   // whole tiles only
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t cap = (cg == 2) ? s->max_pairs : s->max_singles;

@@ -36,6 +36,8 @@ struct TcParams {
     int32_t num_n_tiles;   // tiles of TC_BN columns
     int32_t num_k_blocks;  // ceil(K / TC_BK)
     int32_t group_m;       // rasterisation: m-tiles per group
+    int32_t num_full;      // tiles run whole; the tiles after them run as two N-halves
+    uint32_t idesc_half;   // instruction descriptor for a half tile (N = TC_BN / 2)
     uint32_t epi;          // EpiFlags
     uint32_t idesc;        // tcgen05 instruction descriptor
     uint32_t b_mn_major;   // 1: B is K x N (N contiguous); 0: B is N x K
@@ -46,6 +48,8 @@ struct TcParams {
     uint32_t debug;        // DebugFlags
     uint32_t l2_policy;    // 0: A evict_last, B evict_normal; 1: A normal, B last; 2: both normal
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
+    uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
+    uint32_t multicast;    // 1: clusters of two CTA pairs share B by TMA multicast (cta_group 2)
 };
 
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the
@@ -57,8 +61,9 @@ cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, con
 int tc_smem_bytes(int cta_group);
 
 // Configure kernel attributes (dynamic smem) and report the largest number of
-// co-resident clusters (cta_group 2) or CTAs (cta_group 1) on this device.
-cudaError_t tc_prepare(int cta_group, int dtype, int* max_units);
+// co-resident clusters (cta_group 2: pairs, and clusters of two pairs in
+// *max_quads) or CTAs (cta_group 1) on this device.
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units, int* max_quads);
 
 // Skinny-M (M <= 128) Linear layer: weight-streaming tcgen05 kernel ------
 struct SkinnyParams {

@@ -221,8 +221,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int kb = kb_begin, it = 0; kb < kb_end; ++kb, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!w(bar_full(s), ph)) break;
-                tc_fence_after();
+                if (!w(bar_full(s), ph)) break;   // barrier wait orders the async-proxy bytes
                 const uint32_t sw = base + s * kWStage;
                 const uint32_t sx = base + off_x + s * x_stage;
 #pragma unroll

@@ -105,6 +105,25 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n
     tn = r / rows;
 }
 
+// Work item -> output region.  Items [0, num_full) are whole 256-column
+// tiles in raster order; each later tile is split into two 128-column halves
+// (two consecutive items), which evens out the last, partial wave of the
+// persistent grid.
+__device__ __forceinline__ void work_item(int item, const TcParams& p, int& tm, int& n0, int& nw) {
+    int tile, half = -1;
+    if (item < p.num_full) {
+        tile = item;
+    } else {
+        const int j = item - p.num_full;
+        tile = p.num_full + (j >> 1);
+        half = j & 1;
+    }
+    int tn;
+    tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
+    n0 = tn * TC_BN + (half > 0 ? TC_BN / 2 : 0);
+    nw = half < 0 ? TC_BN : TC_BN / 2;
+}
+
 template <typename OutT> struct OutTraits;
 template <> struct OutTraits<float> {
     static constexpr int kCols = 32;   // 128-byte row chunk
@@ -129,7 +148,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int CG, typename InT, typename OutT>
+// MC = number of CTA pairs in a cluster (1 or 2, CG = 2 only).  With MC = 2
+// the two pairs work on vertically adjacent 256-row tiles of the same 256
+// columns, so their B tiles are identical: each pair fetches half of it and
+// multicasts it to both, halving the B reads out of L2.  A stage may then be
+// refilled only when both pairs' MMAs are done with it.
+template <int CG, int MC, typename InT, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -143,8 +167,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int unit = (CG == 2) ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int num_units = (CG == 2) ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const uint32_t pair = rank >> 1;              // which CTA pair of the cluster
+    const uint32_t lead = rank & ~1u;             // rank of this pair's leader
+    const uint32_t crank = rank & 1u;             // rank within the pair
+    const int unit = (int)(blockIdx.x / (CG * MC));
+    const int num_units = (int)(gridDim.x / (CG * MC));
 
     const uint32_t misc = base + Cfg::kOffMisc;
     auto bar_full = [&](int s) { return misc + Cfg::kBarFull + 8u * s; };
@@ -158,7 +185,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), 1);
+            mbar_init(bar_empty(s), MC);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull(a), 1);
@@ -185,6 +212,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     grid_launch_dependents();
 
     const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+    const int num_items = p.num_full + 2 * (num_tiles - p.num_full);
     const int nkb = p.num_k_blocks;
 
     if (warp == 0) {
@@ -195,37 +223,61 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // each B panel only across the group's rows, so A is the operand to keep.
             const uint64_t pol_a = p.l2_policy == 0 ? l2_policy_evict_last() : l2_policy_evict_normal();
             const uint64_t pol_b = p.l2_policy == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
-            uint32_t it = 0;
+            uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
-                int tm, tn;
-                tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
-                const int m0 = tm * TC_BM * CG + (int)rank * TC_BM;
-                const int nb = tn * TC_BN + (int)rank * Cfg::kBnCta;
+            for (int item = unit; item < num_items && ok; item += num_units, ++tcount) {
+                int tm, n0, nw;
+                work_item(item, p, tm, n0, nw);
+                // serpentine k order: a tile starts on the k-slabs the previous one
+                // ended on, which are the ones most likely still in L2
+                const bool rev = p.k_snake && (tcount & 1u);
+                const int m0 = (tm * MC + (int)pair) * TC_BM * CG + (int)crank * TC_BM;
+                const int nb = n0 + (int)crank * (nw / CG);
+                // K x N operand: one 64-column box per 64 columns this CTA holds;
+                // N x K operand: one full-height box (a half tile uses its top rows),
+                // or 64-row boxes when the two pairs share B
+                const bool boxes64 = p.b_mn_major || MC == 2;
+                const int b_boxes = boxes64 ? nw / CG / 64 : 1;
+                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBStage;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
                     if (!w.wait(bar_empty(s), ph ^ 1u)) { ok = false; break; }
                     const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
                     const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
-                    const int k0 = kb * TC_BK;
-                    if constexpr (CG == 2) {
-                        const uint32_t fb = mapa_shared(bar_full(s), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + Cfg::kBStage));
+                    const int k0 = (rev ? nkb - 1 - kb : kb) * TC_BK;
+                    if constexpr (CG == 2 && MC == 2) {
+                        const uint32_t fb = mapa_shared(bar_full(s), lead);
+                        if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
                         tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
-                        if (p.b_mn_major) {
-#pragma unroll
-                            for (int c = 0; c < Cfg::kBnCta / 64; ++c)
-                                tma_load_2d_pair(sb + c * 8192, &tmB, fb, nb + 64 * c, k0, pol_b);
+                        // B box c goes to this CTA and its counterpart in the other pair;
+                        // pair c issues it (pair 0 issues the only box of a half tile)
+                        const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank + 2)));
+                        for (int c = 0; c < b_boxes; ++c) {
+                            if ((b_boxes == 2 ? c : 0) != (int)pair) continue;
+                            if (p.b_mn_major)
+                                tma_load_2d_pair_mc(sb + c * 8192, &tmB, fb, nb + 64 * c, k0, mask, pol_b);
+                            else
+                                tma_load_2d_pair_mc(sb + c * 8192, &tmB, fb, k0, nb + 64 * c, mask, pol_b);
+                        }
+                    } else if constexpr (CG == 2) {
+                        const uint32_t fb = mapa_shared(bar_full(s), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
+                        tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                        if (boxes64) {
+                            for (int c = 0; c < b_boxes; ++c) {
+                                const int bc = nb + 64 * c;
+                                if (p.b_mn_major) tma_load_2d_pair(sb + c * 8192, &tmB, fb, bc, k0, pol_b);
+                                else tma_load_2d_pair(sb + c * 8192, &tmB, fb, k0, bc, pol_b);
+                            }
                         } else {
                             tma_load_2d_pair(sb, &tmB, fb, k0, nb, pol_b);
                         }
                     } else {
-                        mbar_arrive_expect_tx(bar_full(s), Cfg::kAStage + Cfg::kBStage);
+                        mbar_arrive_expect_tx(bar_full(s), Cfg::kAStage + b_bytes);
                         tma_load_2d(sa, &tmA, bar_full(s), k0, m0, pol_a);
                         if (p.b_mn_major) {
-#pragma unroll
-                            for (int c = 0; c < Cfg::kBnCta / 64; ++c)
+                            for (int c = 0; c < b_boxes; ++c)
                                 tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);
                         } else {
                             tma_load_2d(sb, &tmB, bar_full(s), k0, nb, pol_b);
@@ -241,11 +293,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ----
-        if (rank == 0 && lane == 0) {
+        if (crank == 0 && lane == 0) {
             const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
+            // stage release reaches every CTA whose smem this pair's loads fill
+            const uint16_t empty_mask = (uint16_t)(MC == 2 ? 0xF : 0x3);
+            const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pair));
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++tcount) {
+            for (int item = unit; item < num_items && ok; item += num_units, ++tcount) {
+                const uint32_t idesc = (item < p.num_full) ? p.idesc : p.idesc_half;
                 const uint32_t a = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
                 if (!w.wait(bar_tempty(a), aph ^ 1u)) { ok = false; break; }
@@ -254,8 +310,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
+                    // the stage's bytes arrived through the async proxy that the MMA
+                    // reads with; the barrier wait alone orders them (no tcgen05 fence,
+                    // which would hold the tensor pipe at every k-block)
                     if (!w.wait(bar_full(s), ph)) { ok = false; break; }
-                    tc_fence_after();
                     const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
                     const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
 #pragma unroll
@@ -264,17 +322,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const uint64_t bdesc = p.b_mn_major
                             ? smem_desc_sw128(sb + kk * (kUmmaK * 128), 8192, 1024)
                             : smem_desc_sw128(sb + kk * (kUmmaK * 2), 16, 1024);
-                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if constexpr (CG == 2) tc_commit_2(bar_empty(s), 0x3); else tc_commit_1(bar_empty(s));
+                    if constexpr (CG == 2) tc_commit_2(bar_empty(s), empty_mask); else tc_commit_1(bar_empty(s));
                 }
                 if (!ok) break;
                 if (!((p.debug & DBG_SKIP_FIRST_ACC_COMMIT) && tcount == 0)) {
-                    if constexpr (CG == 2) tc_commit_2(bar_tfull(a), 0x3); else tc_commit_1(bar_tfull(a));
+                    if constexpr (CG == 2) tc_commit_2(bar_tfull(a), pair_mask); else tc_commit_1(bar_tfull(a));
                 }
             }
             // Every MMA this thread issued has finished before TMEM can be released.
-            if constexpr (CG == 2) tc_commit_2(bar_done, 0x1); else tc_commit_1(bar_done);
+            if constexpr (CG == 2) tc_commit_2(bar_done, (uint16_t)(1u << rank)); else tc_commit_1(bar_done);
             const Waiter wd{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
             if (!mbar_try_wait(bar_done, 0)) {
                 const uint64_t t0 = globaltimer_ns();
@@ -286,19 +344,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const uint32_t q = warp & 3u;                 // TMEM lane quarter of this warp
         constexpr int kCols = OutTraits<OutT>::kCols;
-        constexpr int kChunks = TC_BN / kCols;
+
         const uint32_t cbuf0 = base + Cfg::kOffC + (warp - 2) * 2 * Cfg::kCStage;
         const bool has_bias = (p.epi & EPI_BIAS) != 0;
         const bool relu = (p.epi & EPI_RELU) != 0;
         const InT* bias = reinterpret_cast<const InT*>(p.bias);
-        const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), 0) : bar_tempty(0);
-        const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), 0) : bar_tempty(1);
+        const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), lead) : bar_tempty(0);
+        const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), lead) : bar_tempty(1);
         uint32_t tcount = 0, cstore = 0;
-        for (int tile = unit; tile < num_tiles; tile += num_units, ++tcount) {
-            int tm, tn;
-            tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
-            const int m0 = tm * TC_BM * CG + (int)rank * TC_BM;
-            const int n0 = tn * TC_BN;
+        for (int item = unit; item < num_items; item += num_units, ++tcount) {
+            int tm, n0, nw;
+            work_item(item, p, tm, n0, nw);
+            const int kChunks = nw / kCols;
+            const int m0 = (tm * MC + (int)pair) * TC_BM * CG + (int)crank * TC_BM;
             const int row0 = m0 + 32 * (int)q;
             const uint32_t a = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
@@ -388,7 +446,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (CG == 2) cluster_sync_all();
 }
 
-template <int CG, typename InT, typename OutT>
+template <int CG, int MC, typename InT, typename OutT>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const TcParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -398,32 +456,28 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = CG * MC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, InT, OutT>, tmA, tmB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT>, tmA, tmB, tmC, p);
 }
 
-template <int CG, typename InT, typename OutT>
+template <int CG, int MC, typename InT, typename OutT>
 cudaError_t prepare_impl(int* max_units) {
-    auto fn = gemm_tc_kernel<CG, InT, OutT>;
+    auto fn = gemm_tc_kernel<CG, MC, InT, OutT>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<CG>::kSmem);
     if (e != cudaSuccess) return e;
-    if (CG == 2) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-        (void)e;
-    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CG, 1, 1);
+    cfg.gridDim = dim3(CG * MC, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TcCfg<CG>::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = CG * MC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -435,64 +489,51 @@ cudaError_t prepare_impl(int* max_units) {
     return cudaSuccess;
 }
 
+template <int CG, int MC>
+cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                      const TcParams& p, int grid, cudaStream_t stream) {
+    switch (dtype) {
+        case DT_BF16_F32: return launch_impl<CG, MC, __nv_bfloat16, float>(tmA, tmB, tmC, p, grid, stream);
+        case DT_BF16_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(tmA, tmB, tmC, p, grid, stream);
+        case DT_F16_F32: return launch_impl<CG, MC, __half, float>(tmA, tmB, tmC, p, grid, stream);
+        case DT_F16_F16: return launch_impl<CG, MC, __half, __half>(tmA, tmB, tmC, p, grid, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int CG, int MC>
+cudaError_t prepare_dt(int dtype, int* max_units) {
+    switch (dtype) {
+        case DT_BF16_F32: return prepare_impl<CG, MC, __nv_bfloat16, float>(max_units);
+        case DT_BF16_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(max_units);
+        case DT_F16_F32: return prepare_impl<CG, MC, __half, float>(max_units);
+        case DT_F16_F16: return prepare_impl<CG, MC, __half, __half>(max_units);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int tc_smem_bytes(int cta_group) {
     return cta_group == 2 ? TcCfg<2>::kSmem : TcCfg<1>::kSmem;
 }
 
-#define GB300_DISPATCH_DT(CG, CALL)                                                     \
-    switch (dtype) {                                                                    \
-        case DT_BF16_F32: return CALL<CG, __nv_bfloat16, float>;                        \
-        case DT_BF16_BF16: return CALL<CG, __nv_bfloat16, __nv_bfloat16>;               \
-        case DT_F16_F32: return CALL<CG, __half, float>;                                \
-        case DT_F16_F16: return CALL<CG, __half, __half>;                               \
-        default: return cudaErrorInvalidValue;                                          \
-    }
-
 cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream) {
-#define GB300_LAUNCH(CG_, IN_, OUT_) launch_impl<CG_, IN_, OUT_>(tmA, tmB, tmC, p, grid, stream)
-    if (cta_group == 2) {
-        switch (dtype) {
-            case DT_BF16_F32: return GB300_LAUNCH(2, __nv_bfloat16, float);
-            case DT_BF16_BF16: return GB300_LAUNCH(2, __nv_bfloat16, __nv_bfloat16);
-            case DT_F16_F32: return GB300_LAUNCH(2, __half, float);
-            case DT_F16_F16: return GB300_LAUNCH(2, __half, __half);
-        }
-    } else if (cta_group == 1) {
-        switch (dtype) {
-            case DT_BF16_F32: return GB300_LAUNCH(1, __nv_bfloat16, float);
-            case DT_BF16_BF16: return GB300_LAUNCH(1, __nv_bfloat16, __nv_bfloat16);
-            case DT_F16_F32: return GB300_LAUNCH(1, __half, float);
-            case DT_F16_F16: return GB300_LAUNCH(1, __half, __half);
-        }
-    }
-#undef GB300_LAUNCH
+    if (cta_group == 2)
+        return p.multicast ? launch_dt<2, 2>(dtype, tmA, tmB, tmC, p, grid, stream)
+                           : launch_dt<2, 1>(dtype, tmA, tmB, tmC, p, grid, stream);
+    if (cta_group == 1) return launch_dt<1, 1>(dtype, tmA, tmB, tmC, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_prepare(int cta_group, int dtype, int* max_units) {
-#define GB300_PREP(CG_, IN_, OUT_) prepare_impl<CG_, IN_, OUT_>(max_units)
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units, int* max_quads) {
     if (cta_group == 2) {
-        switch (dtype) {
-            case DT_BF16_F32: return GB300_PREP(2, __nv_bfloat16, float);
-            case DT_BF16_BF16: return GB300_PREP(2, __nv_bfloat16, __nv_bfloat16);
-            case DT_F16_F32: return GB300_PREP(2, __half, float);
-            case DT_F16_F16: return GB300_PREP(2, __half, __half);
-        }
-    } else if (cta_group == 1) {
-        switch (dtype) {
-            case DT_BF16_F32: return GB300_PREP(1, __nv_bfloat16, float);
-            case DT_BF16_BF16: return GB300_PREP(1, __nv_bfloat16, __nv_bfloat16);
-            case DT_F16_F32: return GB300_PREP(1, __half, float);
-            case DT_F16_F16: return GB300_PREP(1, __half, __half);
-        }
+        cudaError_t e = prepare_dt<2, 2>(dtype, max_quads);
+        return e != cudaSuccess ? e : prepare_dt<2, 1>(dtype, max_units);
     }
-#undef GB300_PREP
+    if (cta_group == 1) { *max_quads = 0; return prepare_dt<1, 1>(dtype, max_units); }
     return cudaErrorInvalidValue;
 }
-
-#undef GB300_DISPATCH_DT
 
 }  // namespace gb300

@@ -17,7 +17,7 @@ LIB_PATH = _PKG / "libgb300gemm.so"
 
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_BIAS_RELU = 0, 1, 2, 3
 BF16_F32OUT, BF16_BF16OUT, F16_F32OUT, F16_F16OUT = 0, 1, 2, 3
-B_KN, B_NK, B_CONST = 0, 1, 2
+B_KN, B_NK, B_CONST, TC_MULTICAST = 0, 1, 2, 4
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
     0, -1, -2, -3, -4, -5, -6)
@@ -103,12 +103,13 @@ class Plan:
     """Owner of a ``gemm_plan_t``.  ``b_layout`` is "kn" (B is K x N) or "nk"
     (B is a Linear weight W, N x K)."""
 
-    def __init__(self, device: int | torch.device = 0, b_layout: str = "kn", b_const: bool = False):
+    def __init__(self, device: int | torch.device = 0, b_layout: str = "kn", b_const: bool = False,
+                 multicast: bool = False):
         if isinstance(device, torch.device):
             device = device.index if device.index is not None else torch.cuda.current_device()
         self.device = int(device)
         self.b_nk = b_layout == "nk"
-        flags = (B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0)
+        flags = (B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0) | (TC_MULTICAST if multicast else 0)
         h = _vp()
         _check(lib().gemm_plan_create(ctypes.byref(h), self.device, flags), "gemm_plan_create")
         self._h = h

@@ -74,6 +74,11 @@ typedef enum {
  * while the previous kernel of the stream is still finishing; A, bias and C
  * are still touched only after that kernel is done. */
 #define GEMM_B_CONST 2u
+/* Large-M kernel: clusters of two CTA pairs on vertically adjacent tiles
+ * fetch each shared B tile once and multicast it to both pairs (halves the B
+ * reads from L2; on GB300 it lowers power but was not faster at the sizes
+ * measured, so it is off by default). */
+#define GEMM_TC_MULTICAST 4u
 
 /* Kernel selection (gemm_plan_set_kernel / gemm_plan_last_kernel). */
 #define GEMM_KERNEL_AUTO 0
@@ -92,7 +97,7 @@ typedef enum {
 #define GEMM_ERR_NO_MEMORY (-6)       /* workspace allocation failed           */
 
 /* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK,
- * optionally | GEMM_B_CONST.
+ * optionally | GEMM_B_CONST and | GEMM_TC_MULTICAST.
  * Allocates the plan and its device status word; restores the caller's
  * current device before returning.  *plan is set only on success. */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);

@@ -62,7 +62,8 @@ def test_validate_rejects_bad_arguments(lib):
     assert val(K=-5) == G.ERR_INVALID_ARG
     assert val(epi=4) == G.ERR_INVALID_ARG
     assert val(dtype=9) == G.ERR_INVALID_ARG
-    assert val(flags=4) == G.ERR_INVALID_ARG
+    assert val(flags=8) == G.ERR_INVALID_ARG
+    assert val(flags=G.TC_MULTICAST) == G.OK
     assert val(flags=G.B_NK | G.B_CONST, N=32, ldb=64, ldc=32) == G.OK
     assert val(lda=63) == G.ERR_INVALID_ARG               # lda < K
     assert val(ldb=63) == G.ERR_INVALID_ARG               # ldb < N (K x N layout)

@@ -100,6 +100,31 @@ def test_tails_integer_exact(plans, M, N, K, kernel):
     check(plans, GemmCase("tails", M, N, K, out="f32", integer=True, seed=M + N + K), kernel)
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("b_nk", [False, True])
+@pytest.mark.parametrize("shape", [(4096, 4096, 72), (2304, 4352, 40)])
+def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
+    """Shapes whose last persistent wave is partial: its tiles run as two
+    128-column halves (whole tiles first, then halves); every output checked."""
+    M, N, K = shape
+    check(plans, GemmCase("tail_split", M, N, K, b_nk=b_nk, bias=True, out="bf16", integer=True, seed=K), kernel)
+
+
+@pytest.mark.parametrize("b_nk", [False, True])
+@pytest.mark.parametrize("shape", [(600, 700, 333), (1024, 768, 256), (4096, 4096, 72), (1300, 530, 200)])
+def test_multicast_clusters_integer_exact(b_nk, shape):
+    """Clusters of two CTA pairs sharing B by TMA multicast (plan flag): exact
+    on integers, including odd numbers of 256-row tiles and split last waves."""
+    M, N, K = shape
+    p = G.Plan(0, "nk" if b_nk else "kn", multicast=True)
+    case = GemmCase("multicast", M, N, K, b_nk=b_nk, bias=True, relu=True, out="bf16", integer=True, seed=M)
+    A, B, bias, C = run_case(p, case, kernel=G.KERNEL_TC_PAIR)
+    assert p.last_kernel == G.KERNEL_TC_PAIR
+    C_ref, S = oracle_full(case, A, B, bias)
+    compare(case, C, C_ref, S)
+    p.close()
+
+
 # ------------------------------------------------------------ skinny-M path
 @pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 64, 100, 128])
 @pytest.mark.parametrize("b_nk", [True, False])
