@@ -69,6 +69,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of `x` over the ranks of the default process group
+    (the slowest rank's time); `x` itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` independent replica steps; the
+    job took as long as its slowest rank."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in sorted((ROOT / "dnn_linear_layers_gb300" / "csrc").glob("*")):
@@ -183,6 +201,8 @@ def run_ours(args):
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     # Linear-layer weights are constant model parameters: say so to the plan
     plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"))
+    if args.kernel != "auto":
+        plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
     nbytes_step = R.gemm_bytes(M, N, K, 2, 2, 2, 2 if has_bias else 0)
@@ -265,12 +285,9 @@ def run_ours(args):
     st = plan.status()
     assert st == 0, f"device status {st}"
 
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, world, total_ms)
 
     # ---- end to end: pinned host inputs -> device -> gemm_run -> host result
     A_p = A_h.pin_memory(); B_p = B_h.pin_memory()
@@ -296,11 +313,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12 if not args.no_e2e else None
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_throughput(flops, e2e_steps, world, e2e_ms) if not args.no_e2e else None
     assert plan.status() == 0
 
     peaks, src = R.load_peaks()
@@ -425,6 +439,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a graph replay")
+    ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny"], default="auto",
+                    help="force a kernel (sweeps); the default lets the library choose")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
