@@ -180,7 +180,7 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
             const int64_t smem = skinny_smem_bytes(mpad, st);
             if (smem > 227 * 1024) continue;
             int64_t per_sm = p->smem_per_sm / (smem + p->smem_reserved);
-            if (per_sm > 2048 / 192) per_sm = 2048 / 192;
+            if (per_sm > kSkinnyMaxCtasPerSm) per_sm = kSkinnyMaxCtasPerSm;   // registers
             if (per_sm > 512 / tmem_cols) per_sm = 512 / tmem_cols;
             if (ctas * 10 > (int64_t)p->sm_count * per_sm * 8) continue;   // not resident with headroom
             // depth beyond four stages earns nothing: more CTAs beat a deeper ring

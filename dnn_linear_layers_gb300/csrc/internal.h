@@ -88,6 +88,9 @@ struct SkinnyParams {
     int64_t ldx;
 };
 
+// at most this many skinny CTAs share an SM (the kernel's launch bounds size
+// its registers for it)
+constexpr int kSkinnyMaxCtasPerSm = 4;
 int skinny_smem_bytes(int mpad, int stages);
 cudaError_t skinny_prepare(int dtype);
 cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,

@@ -14,8 +14,9 @@
 //     for a bandwidth-bound kernel this keeps every SM streaming W;
 //   * the S partial tiles are reduced through distributed shared memory in a
 //     fixed order (slice 0, 1, ..., S-1), so results are deterministic and no
-//     global workspace is needed; each CTA of the cluster reduces, applies
-//     bias / ReLU / cast and stores 128/S of the features.  The lane-wise
+//     global workspace is needed: each CTA pushes its partial rows to the CTA
+//     that owns them (remote stores, no round trip), and each owner reduces,
+//     applies bias / ReLU / cast and stores 128/S of the features.  The lane-wise
 //     accumulate-then-combine is the warp-shuffle reduction idea of the CMU
 //     15-418 notes, section 3.3, lifted to CTAs.
 //   * W may be N x K (a Linear weight, K contiguous) or K x N (N contiguous);
@@ -62,19 +63,10 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
     }
 }
 
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr) : "memory");
+// 16-byte store into the shared memory of a CTA of this cluster (address from mapa)
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 struct BoundedWait {
@@ -111,7 +103,7 @@ template <> __device__ __forceinline__ __half from_float<__half>(float v) { retu
 // Grid: num_n_tiles * S CTAs, clusters of S along x.  CTA rank r of a cluster
 // owns k-blocks [r*nkb/S, (r+1)*nkb/S) of feature tile blockIdx.x / S.
 template <typename InT, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kSkinnyMaxCtasPerSm)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const SkinnyParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -130,8 +122,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t bar_acc = misc + 8u * (2 * kMaxStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + off_misc + 8 * (2 * kMaxStages + 1));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + off_misc + 8 * (2 * kMaxStages + 1) + 4);
-    // partial tile red[m][f] (fp32, token-major, mpad x 128 x 4 B) reuses the
-    // front of the operand ring, which is at least that large for mpad <= 128
+    // receive buffer recv[slice][f][m] (fp32, S x 128/S x mpad x 4 B = mpad x
+    // 512 B) reuses the front of the operand ring, which holds at least two
+    // stages of 16 KB + mpad x 128 B, hence at least mpad x 512 B for mpad <= 128
     float* red = reinterpret_cast<float*>(base_ptr);
     const uint32_t red_addr = base;
 
@@ -284,59 +277,125 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int it = nk - lag < 0 ? 0 : nk - lag; it < nk; ++it) hand_over(it);
     }
 
-    // ---- partial tile: TMEM -> smem (all MMAs done, ring no longer in use)
+    // ---- split-K reduction.  Every CTA of the cluster has finished its MMAs
+    // once barrier (1) is passed, so all operand rings are free; each CTA then
+    // pushes its partial tile, feature by feature, into the ring of the CTA
+    // that owns the feature (128/S features per CTA) with 16-byte remote
+    // stores, which need no round trip.  After barrier (2) each owner adds the
+    // S partials from its own shared memory in slice order 0, 1, ..., S-1
+    // (deterministic) and applies bias / ReLU / cast.
+    // Receive layout in the owner's ring: recv[slice][feature - first owned
+    // feature][token], fp32, each row of mpad tokens cut into 16-byte chunks
+    // of 4 tokens whose order is XOR-swizzled by the row so that 8 rows read
+    // or written at the same chunk fall on 8 different bank groups.
     bool have_acc = true;
     if (warp >= 2) {
         const BoundedWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const bool ready = w(bar_acc, 0);
         have_acc = __all_sync(0xffffffffu, ready);
-        if (have_acc) {
-            tc_fence_after();
-            const uint32_t q = warp & 3u;
-            const int f = 32 * (int)q + (int)lane;          // feature row within the tile
-            const bool empty_slice = kb_end <= kb_begin;
-            for (int c = 0; c < mpad; c += 16) {
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(tmem + ((32u * q) << 16) + (uint32_t)c, r);
+    }
+    tc_fence_before();
+    __syncwarp();
+    cluster_arrive_wait();   // (1) every ring of the cluster is idle
+    const int per = 128 / S;                          // features owned by each CTA
+    const int mcols = p.M < mpad ? p.M : mpad;        // token columns that matter
+    // chunk swizzle of row fl: rows of a multiple of 128 B use fl % 8; rows of
+    // 64 B (mod 128) alternate halves of a 128-byte window, so use (fl / 2) % 4
+    const bool row128 = (mpad % 32) == 0;
+    auto swz = [&](int fl) { return row128 ? (fl & 7) : ((fl >> 1) & 3); };
+    if (warp >= 2) {
+        tc_fence_after();
+        const uint32_t q = warp & 3u;
+        const int f = 32 * (int)q + (int)lane;        // feature row of the tile (TMEM lane)
+        const uint32_t owner = (uint32_t)(f / per);
+        const int fl = f - (int)owner * per;
+        const int sw = swz(fl);
+        const uint32_t row = mapa_shared(red_addr, owner) + (uint32_t)(((int)rank * per + fl) * mpad * 4);
+        const bool zero = !have_acc || kb_end <= kb_begin;   // warp-uniform
+        // 32 token columns per TMEM load (the allocation holds at least
+        // round_up(mpad, 32) columns); columns past mcols are not sent
+        for (int c = 0; c < mcols; c += 32) {
+            uint32_t r[32];
+            if (!zero) {
+                tmem_ld_32x32b_x32(tmem + ((32u * q) << 16) + (uint32_t)c, r);
                 tmem_ld_wait();
+            } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    red[(c + j) * 128 + f] = empty_slice ? 0.0f : __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int chunk = (c >> 2) + i;
+                if (4 * chunk < mcols)
+                    st_shared_cluster_v4(row + (uint32_t)((chunk ^ sw) << 4), r[4 * i], r[4 * i + 1], r[4 * i + 2],
+                                         r[4 * i + 3]);
             }
         }
     }
     tc_fence_before();
     __syncwarp();
-    cluster_arrive_wait();   // every slice's partial tile is in its shared memory
-
-    // ---- reduction over the cluster in slice order, epilogue, store
-    {
-        const int per = 128 / S;                    // features reduced by this CTA
-        const int fr0 = (int)rank * per;
-        const InT* bias = reinterpret_cast<const InT*>(p.bias);
-        OutT* Y = reinterpret_cast<OutT*>(p.Y);
-        const int total = per * p.M;
-        for (int idx = threadIdx.x; idx < total; idx += kThreads) {
-            const int m = idx / per;
-            const int fl = fr0 + (idx - m * per);
-            const int n = f0 + fl;
-            const uint32_t off = (uint32_t)((m * 128 + fl) * 4);
-            float acc = 0.0f;
-            for (int s = 0; s < S; ++s) acc += ld_shared_cluster_f32(mapa_shared(red_addr + off, (uint32_t)s));
-            if (n < p.N) {
-                if (p.epi & EPI_BIAS) acc += to_float<InT>(bias[n]);
-                if (p.epi & EPI_RELU) acc = fmaxf(acc, 0.0f);
-                Y[(int64_t)m * p.ldy + n] = from_float<OutT>(acc);
-            }
-        }
-    }
-    (void)have_acc;
-    __syncwarp();
-    cluster_arrive_wait();   // no CTA leaves while a peer may still read its smem
+    cluster_arrive_wait();   // (2) all partials delivered (release / acquire)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<1>(tmem, p.tmem_cols);
     }
+    {
+        // thread -> (owned feature fl, token chunks q0, q0 + qstep, ...); two
+        // chunks per pass so that their shared-memory loads overlap
+        const int qstep = kThreads / per;             // 1, 3, 6 or 12
+        const int t = (int)threadIdx.x;
+        if (t < qstep * per) {
+            const int fl = t % per;
+            const int n = f0 + (int)rank * per + fl;
+            const int sw = swz(fl);
+            const bool relu = (p.epi & EPI_RELU) != 0;
+            float b = 0.0f;
+            if ((p.epi & EPI_BIAS) && n < p.N) b = to_float<InT>(reinterpret_cast<const InT*>(p.bias)[n]);
+            const int64_t ldy = p.ldy;
+            OutT* const ycol = reinterpret_cast<OutT*>(p.Y) + n;
+            const float* const rrow = red + fl * mpad;
+            const int slice = per * mpad;             // floats per slice
+            const int nq = (mcols + 3) >> 2;
+            auto load_sum = [&](int qc) {
+                const float* src = rrow + ((qc ^ sw) << 2);
+                float4 acc = *reinterpret_cast<const float4*>(src);
+                for (int s = 1; s < S; ++s) {
+                    const float4 v = *reinterpret_cast<const float4*>(src + s * slice);
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                return acc;
+            };
+            auto emit = [&](int qc, float4 acc) {
+                float o[4] = {acc.x + b, acc.y + b, acc.z + b, acc.w + b};
+                if (relu) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = fmaxf(o[e], 0.0f);
+                }
+                const int m0 = 4 * qc;
+                OutT* yp = ycol + (int64_t)m0 * ldy;
+                if (m0 + 4 <= p.M) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e, yp += ldy) *yp = from_float<OutT>(o[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e, yp += ldy)
+                        if (m0 + e < p.M) *yp = from_float<OutT>(o[e]);
+                }
+            };
+            if (n < p.N) {
+                int qc = t / per;
+                for (; qc + qstep < nq; qc += 2 * qstep) {
+                    const float4 a0 = load_sum(qc);
+                    const float4 a1 = load_sum(qc + qstep);
+                    emit(qc, a0);
+                    emit(qc + qstep, a1);
+                }
+                if (qc < nq) emit(qc, load_sum(qc));
+            }
+        }
+    }
+    // No barrier after the reduction: nothing reads or writes another CTA's
+    // shared memory past barrier (2).
 }
 
 template <typename InT, typename OutT>
