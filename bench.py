@@ -87,22 +87,29 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float)
     return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
 
 
-def kernel_source_hash() -> str:
+# sources each profiled kernel depends on: its translation unit, the shared
+# headers and the dispatcher that sets its launch parameters
+KERNEL_SOURCES = {
+    "tc": ["kernels_tc.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
+    "skinny": ["kernels_skinny.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
+}
+
+
+def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
-    for f in sorted((ROOT / "dnn_linear_layers_gb300" / "csrc").glob("*")):
-        if f.suffix in (".cu", ".cuh", ".h"):
-            h.update(f.read_bytes())
+    for name in files:
+        h.update((ROOT / "dnn_linear_layers_gb300" / "csrc" / name).read_bytes())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):
     """DRAM bytes per launch of the top kernel from the committed ncu summary,
-    valid only if the kernel sources are unchanged since it was taken."""
+    valid only if that kernel's sources are unchanged since it was taken."""
     f = ROOT / "profiles" / "traffic.json"
     try:
         d = json.loads(f.read_text())
         e = d[workload]
-        if e.get("source_hash") == kernel_source_hash():
+        if e.get("source_hash") == kernel_source_hash(KERNEL_SOURCES[e["sources"]]):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         pass
