@@ -47,6 +47,8 @@ WORKLOADS = {
     "ffn_up_8192x4096x14336": (8192, 14336, 4096, "kn", (True, True), "bf16", 1.0, 4096 ** -0.5),
     "ffn_down_8192x14336x4096": (8192, 4096, 14336, "kn", (True, False), "bf16", 1.0, 14336 ** -0.5),
     "conv_im2col_100352x2304x256": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
+    # the same convolution as an implicit GEMM: gemm_conv2d on the NHWC activations
+    "conv_implicit_32x56x56x256_3x3": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
     "odd_3000x5000x2048": (3000, 5000, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
     "odd_4095": (4095, 4095, 4095, "kn", (False, False), "bf16", 1.0, 1.0),
     "odd_1000": (1000, 1000, 1000, "kn", (False, False), "bf16", 1.0, 1.0),
@@ -174,6 +176,11 @@ def make_inputs(name, device, seed=0):
     import torch
     from dnn_linear_layers_gb300.inputs import normal_bf16
     M, N, K, lay, (has_bias, relu), out, a_std, b_std = WORKLOADS[name]
+    if name.startswith("conv_implicit"):
+        # x (NHWC 32x56x56x256, ReLU(N(0,1))) and w[f][r][s][c] as they are
+        from dnn_linear_layers_gb300.inputs import conv_tensors
+        x, w = conv_tensors(seed=seed)
+        return x, w, None
     if name.startswith("conv_im2col"):
         # activations ReLU(N(0,1)) NHWC 32x56x56x256, weights w[f][r][s][c]; the
         # im2col matrix is built on the GPU by the library (setup, untimed)
@@ -212,7 +219,11 @@ def run_ours(args):
         plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
-    nbytes_step = R.gemm_bytes(M, N, K, 2, 2, 2, 2 if has_bias else 0)
+    conv = name.startswith("conv_implicit")
+    if conv:   # activations, weights and output once each (no im2col matrix exists)
+        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + M * N * 2)
+    else:
+        nbytes_step = R.gemm_bytes(M, N, K, 2, 2, 2, 2 if has_bias else 0)
     # Workloads smaller than twice the L2 rotate through enough copies of their
     # operands that each step reads HBM, not the previous step's L2 lines.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -220,10 +231,16 @@ def run_ours(args):
     copies = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n_copies - 1)]
     counter = [0]
 
+    def call(a, b, c):
+        if conv:
+            plan.conv2d(a, b, c, bias, relu, pad=1)
+        else:
+            plan.run(a, b, c, bias, relu)      # on torch's current stream
+
     def step():
         a, b, c = copies[counter[0] % n_copies]
         counter[0] += 1
-        plan.run(a, b, c, bias, relu)          # on torch's current stream
+        call(a, b, c)
 
     for _ in range(args.warmup):
         step()
@@ -304,7 +321,7 @@ def run_ours(args):
     def e2e_step():
         A_e.copy_(A_p, non_blocking=True)
         B_e.copy_(B_p, non_blocking=True)
-        plan.run(A_e, B_e, C_e, bias, relu)
+        call(A_e, B_e, C_e)
         C_p.copy_(C_e, non_blocking=True)
 
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -379,6 +396,19 @@ def _oracle_rows_timer(name, A, B, bias):
     import oracle
     M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
     threads = len(os.sched_getaffinity(0))
+    if name.startswith("conv_implicit"):
+        # the direct seven-loop convolution at n seeded output positions (one thread)
+        Nb, H, W, _ = A.shape
+        rng = np.random.default_rng(0)
+
+        def run_conv(n):
+            idx = rng.choice(M, size=min(M, n), replace=False)
+            pos = [(int(i) // (H * W), (int(i) // W) % H, int(i) % W) for i in idx]
+            t = time.perf_counter()
+            oracle.conv2d_at(A, B, 1, pos)
+            return time.perf_counter() - t, len(pos)
+
+        return run_conv, 1
     Af = A.double().numpy(); Bf = B.double().numpy()
     bf = bias.double().numpy() if bias is not None else None
     rng = np.random.default_rng(0)

@@ -53,6 +53,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn g_encode = nullptr;
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeIm2colFn g_encode_im2col = nullptr;
 
 int record(gemm_plan* p, cudaError_t e) {
     if (p) p->last_cuda_error = (int)e;
@@ -67,6 +72,13 @@ bool get_encode() {
         q != cudaDriverEntryPointSuccess || fn == nullptr)
         return false;
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    // optional: without it, convolutions take the explicit im2col path
+    void* fn2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn2, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess && fn2 != nullptr)
+        g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(fn2);
+    else
+        cudaGetLastError();
     return true;
 }
 
@@ -86,6 +98,32 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+
+// A operand of an implicit-GEMM convolution: NHWC activations read through an
+// im2col tensor map (stride 1, square filter, C a multiple of TC_BK).
+struct ConvA {
+    const void* x;
+    int64_t Nb, H, W, C;
+    int R, S, pad;
+};
+
+// im2col tensor map over x (Nb x H x W x C): tiles of TC_BM consecutive output
+// pixels x TC_BK channels, 128-byte swizzle.  The bounding box holds the
+// top-left pixels of all filter windows: from -pad to (dim - 1) + pad -
+// (filter - 1) in H and in W (equal offsets: the filter is square).
+bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c) {
+    if (!g_encode_im2col) return false;
+    cuuint64_t gdim[4] = {(cuuint64_t)c.C, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.Nb};
+    cuuint64_t gstride[3] = {(cuuint64_t)c.C * 2, (cuuint64_t)(c.W * c.C * 2), (cuuint64_t)(c.H * c.W * c.C * 2)};
+    int lower[2] = {-c.pad, -c.pad};
+    int upper[2] = {c.pad - (c.S - 1), c.pad - (c.R - 1)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode_im2col(m, dt, 4, const_cast<void*>(c.x), gdim, gstride, lower, upper, TC_BK, TC_BM, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -402,15 +440,16 @@ int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int 
     return GEMM_OK;
 }
 
-int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-             int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, void* stream_v) {
-    if (!p) return GEMM_ERR_INVALID_ARG;
-    int rc = gemm_validate(p->flags, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype);
-    if (rc != GEMM_OK) return rc;
-    if (M == 0 || N == 0) return GEMM_OK;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
-    DeviceGuard g(p->device);
-    const bool b_nk = (p->flags & GEMM_B_NK) != 0;
+}  // extern "C"
+
+namespace {
+
+// Validated arguments; M, N > 0.  b_nk: B is N x K.  conv: A is the im2col
+// view of an activation tensor (then A and lda are unused).
+int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+             int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, cudaStream_t stream,
+             const ConvA* conv) {
+    int rc = GEMM_OK;
     const uint32_t epi = (uint32_t)epilogue;   // GEMM_EPI_* == EpiFlags bits
     cudaError_t e;
 
@@ -424,8 +463,8 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     }
 
     int kernel = p->forced_kernel;
-    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
-    if (kernel == GEMM_KERNEL_SKINNY && M > 128) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128 && !conv) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv)) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
         return GEMM_ERR_UNSUPPORTED;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
@@ -436,7 +475,7 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
     const int ob = out_bytes(dtype);
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
-    const bool a_ok = aligned16(A) && (lda * 2) % 16 == 0;
+    const bool a_ok = conv || (aligned16(A) && (lda * 2) % 16 == 0);
     const bool b_ok = aligned16(B) && (ldb * 2) % 16 == 0;
     // the skinny kernel stores C with plain stores: any pitch is fine
     const bool c_ok = skinny || (aligned16(C) && (ldc * ob) % 16 == 0);
@@ -478,8 +517,11 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     const CUtensorMapDataType out_dt = (ob == 4) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                  : (in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     CUtensorMap tmA, tmB, tmC;
-    if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * 2, TC_BK, TC_BM))
+    if (conv) {
+        if (!make_im2col_map(&tmA, in_dt, *conv)) return GEMM_ERR_CUDA;
+    } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * 2, TC_BK, TC_BM)) {
         return GEMM_ERR_CUDA;
+    }
     bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * 2, TC_BK,
                                mc == 2 ? 64 : TC_BN / cg)
                     : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * 2, 64, TC_BK);
@@ -505,6 +547,14 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     prm.l2_policy = p->l2_policy;
     prm.pdl = p->pdl;
     prm.k_snake = p->k_snake ? 1u : 0u;
+    if (conv) {
+        prm.conv = 1u;
+        prm.conv_cb = (int32_t)(conv->C / TC_BK);
+        prm.conv_s = conv->S;
+        prm.conv_pad = conv->pad;
+        prm.conv_out_w = (int32_t)(conv->W + 2 * conv->pad - conv->S + 1);
+        prm.conv_out_hw = (int32_t)((conv->H + 2 * conv->pad - conv->R + 1) * prm.conv_out_w);
+    }
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
     const int64_t cap = mc == 2 ? p->max_quads : (cg == 2 ? p->max_pairs : p->max_singles);
@@ -513,8 +563,8 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
     prm.idesc_half = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN / 2);
     if (p->debug_log)
-        std::fprintf(stderr, "[gemm] tc cta_group=%d mc=%d M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
-                     cg, mc, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
+        std::fprintf(stderr, "[gemm] tc cta_group=%d mc=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
+                     cg, mc, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
                      (long long)(units * cg * mc), A_use != A, B_use != B, C_use != C);
     e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg * mc), stream);
     if (e != cudaSuccess) return record(p, e);
@@ -528,6 +578,56 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     p->last_kernel = kernel;
     p->last_stream = stream; p->have_stream = true;
     return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+             int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, void* stream_v) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    int rc = gemm_validate(p->flags, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceGuard g(p->device);
+    return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype,
+                    reinterpret_cast<cudaStream_t>(stream_v), nullptr);
+}
+
+int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S, int pad,
+                const void* x, const void* w, const void* bias, void* y, int64_t ldy, int epilogue, int dtype,
+                void* stream_v) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
+    if (OH < 0 || OW < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t M = Nb * OH * OW, N = Cout, K = (int64_t)R * S * C;
+    // the weights w[f][r][s][c] are the N x K operand
+    int rc = gemm_validate(GEMM_B_NK, M, N, K, x, K, w, K, bias, y, ldy, epilogue, dtype);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+    DeviceGuard g(p->device);
+    // implicit GEMM: channel blocks of TC_BK, square filter (the map's
+    // bounding box is symmetric), corner offsets in the 8-bit range of a 4-D
+    // im2col map, 16-byte aligned activations, more rows than the small-M path
+    const bool implicit = K > 0 && C % TC_BK == 0 && R == S && pad <= 127 && (S - 1 - pad) <= 128 &&
+                          aligned16(x) && M > 128 && Nb <= INT32_MAX && H <= INT32_MAX && W <= INT32_MAX &&
+                          p->forced_kernel != GEMM_KERNEL_SKINNY && g_encode_im2col != nullptr;
+    if (implicit) {
+        const ConvA cv{x, Nb, H, W, C, R, S, pad};
+        return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epilogue, dtype, stream, &cv);
+    }
+    // otherwise: explicit im2col matrix in the plan workspace, then the GEMM
+    if (K == 0) return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epilogue, dtype, stream, nullptr);
+    const int64_t ldk = round_up(K, 8);
+    rc = ensure_workspace(p, (size_t)(M * ldk * 2));
+    if (rc != GEMM_OK) return rc;
+    cudaError_t e = launch_im2col(x, Nb, H, W, C, R, S, pad, 1, p->workspace, ldk, 2, stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+    return run_impl(p, true, M, N, K, p->workspace, ldk, w, K, bias, y, ldy, epilogue, dtype, stream, nullptr);
 }
 
 }  // extern "C"

@@ -50,6 +50,16 @@ struct TcParams {
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
     uint32_t multicast;    // 1: clusters of two CTA pairs share B by TMA multicast (cta_group 2)
+    // Implicit-GEMM convolution (conv != 0): A is not a matrix but an NHWC
+    // activation tensor read through an im2col tensor map; row m of A is
+    // output pixel m = (n * out_h + oh) * out_w + ow and k-block kb is channel
+    // block kb % conv_cb of filter tap kb / conv_cb = r * conv_s + s (stride 1).
+    uint32_t conv;
+    int32_t conv_cb;       // channel blocks of TC_BK per tap (C / 64)
+    int32_t conv_s;        // filter width S
+    int32_t conv_pad;      // zero padding (rows and columns)
+    int32_t conv_out_w;    // output width  (= W for stride 1, pad (S-1)/2)
+    int32_t conv_out_hw;   // output pixels per image
 };
 
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the

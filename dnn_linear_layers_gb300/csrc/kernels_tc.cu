@@ -233,6 +233,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const bool rev = p.k_snake && (tcount & 1u);
                 const int m0 = (tm * MC + (int)pair) * TC_BM * CG + (int)crank * TC_BM;
                 const int nb = n0 + (int)crank * (nw / CG);
+                // implicit GEMM: base pixel (top-left of the filter window) of row m0
+                int px_n = 0, px_h = 0, px_w = 0;
+                if (p.conv) {
+                    px_n = m0 / p.conv_out_hw;
+                    const int rem = m0 - px_n * p.conv_out_hw;
+                    px_h = rem / p.conv_out_w - p.conv_pad;
+                    px_w = rem % p.conv_out_w - p.conv_pad;
+                }
+                // A tile of k-block k0: a 2-D box of the matrix, or the tap's
+                // channel block through the im2col map
+                auto load_a = [&](uint32_t dst, uint32_t bar, int k0, bool pair_bar) {
+                    if (p.conv) {
+                        const int kbi = k0 / TC_BK;
+                        const int tap = kbi / p.conv_cb;
+                        const int c0 = (kbi - tap * p.conv_cb) * TC_BK;
+                        const int r = tap / p.conv_s;
+                        const uint16_t off_w = (uint16_t)(tap - r * p.conv_s), off_h = (uint16_t)r;
+                        if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                        else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                    } else {
+                        if (pair_bar) tma_load_2d_pair(dst, &tmA, bar, k0, m0, pol_a);
+                        else tma_load_2d(dst, &tmA, bar, k0, m0, pol_a);
+                    }
+                };
                 // K x N operand: one 64-column box per 64 columns this CTA holds;
                 // N x K operand: one full-height box (a half tile uses its top rows),
                 // or 64-row boxes when the two pairs share B
@@ -249,7 +273,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if constexpr (CG == 2 && MC == 2) {
                         const uint32_t fb = mapa_shared(bar_full(s), lead);
                         if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
-                        tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                        load_a(sa, fb, k0, true);
                         // B box c goes to this CTA and its counterpart in the other pair;
                         // pair c issues it (pair 0 issues the only box of a half tile)
                         const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank + 2)));
@@ -263,7 +287,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     } else if constexpr (CG == 2) {
                         const uint32_t fb = mapa_shared(bar_full(s), 0);
                         if (rank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
-                        tma_load_2d_pair(sa, &tmA, fb, k0, m0, pol_a);
+                        load_a(sa, fb, k0, true);
                         if (boxes64) {
                             for (int c = 0; c < b_boxes; ++c) {
                                 const int bc = nb + 64 * c;
@@ -275,7 +299,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                     } else {
                         mbar_arrive_expect_tx(bar_full(s), Cfg::kAStage + b_bytes);
-                        tma_load_2d(sa, &tmA, bar_full(s), k0, m0, pol_a);
+                        load_a(sa, bar_full(s), k0, false);
                         if (p.b_mn_major) {
                             for (int c = 0; c < b_boxes; ++c)
                                 tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);

@@ -118,6 +118,35 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Implicit-GEMM (im2col) loads from an NHWC tensor map made by
+// cuTensorMapEncodeIm2col: starting at pixel (n, h, w) of the map's bounding
+// box, `pixelsPerColumn` consecutive pixels (w fastest, then h, then n) are
+// taken, each shifted by the filter tap (off_w, off_h), and the
+// `channelsPerPixel` channels from c of each become one row of the tile;
+// pixels outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_im2col(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c,
+                                                int32_t w, int32_t h, int32_t n, uint16_t off_w, uint16_t off_h,
+                                                uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8}, %9;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(n), "h"(off_w),
+           "h"(off_h), "l"(policy)
+        : "memory");
+}
+
+// As tma_load_im2col, completion counted on a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar,
+                                                     int32_t c, int32_t w, int32_t h, int32_t n, uint16_t off_w,
+                                                     uint16_t off_h, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8}, %9;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c), "r"(w), "r"(h), "r"(n),
+           "h"(off_w), "h"(off_h), "l"(policy)
+        : "memory");
+}
+
 // As tma_load_2d_pair, multicast: the tile lands at the same offset in every
 // CTA of `mask`, and each destination's pair leader barrier (at the offset of
 // `cluster_bar`, which names a pair leader) counts its bytes.

@@ -41,6 +41,8 @@ SIGNATURES = {
     "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
     "gemm_im2col": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp, _i64, _int, _vp]),
     "gemm_run_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _uint, _vp, _vp]),
+    "gemm_conv2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _i64, _int, _int,
+                           _vp]),
 }
 
 _lib = None
@@ -190,6 +192,31 @@ class Plan:
         _check(rc, "gemm_run")
         return C
 
+    def conv2d(self, x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: torch.Tensor | None = None,
+               relu: bool = False, pad: int = 0, stream=None):
+        """Stride-1 convolution of the NHWC tensor x (Nb x H x W x C) with
+        w (Cout x R x S x C) into y ((Nb*OH*OW) x Cout, row-major)."""
+        if x.dim() != 4 or w.dim() != 4 or not x.is_contiguous() or not w.is_contiguous():
+            raise ValueError("x (NHWC) and w (Cout x R x S x C) must be contiguous 4-D tensors")
+        Nb, H, W, C = x.shape
+        Cout, R, S, Cw = w.shape
+        OH, OW = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+        if Cw != C or tuple(y.shape) != (Nb * OH * OW, Cout):
+            raise ValueError(f"shape mismatch: x {tuple(x.shape)} w {tuple(w.shape)} y {tuple(y.shape)}")
+        if x.dtype != w.dtype or (bias is not None and bias.dtype != x.dtype):
+            raise ValueError("x, w and bias must share one input dtype")
+        for t in (x, w, y) + ((bias,) if bias is not None else ()):
+            if t.device.type != "cuda":
+                raise ValueError("operands must be CUDA tensors")
+        if bias is not None and (bias.dim() != 1 or bias.shape[0] != Cout or bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous vector of length Cout")
+        epi = (EPI_BIAS if bias is not None else 0) | (EPI_RELU if relu else 0)
+        rc = lib().gemm_conv2d(self._h, Nb, H, W, C, Cout, R, S, pad, x.data_ptr(), w.data_ptr(),
+                               bias.data_ptr() if bias is not None else None, y.data_ptr(), _ld(y), epi,
+                               dtype_code(x.dtype, y.dtype), _stream_handle(stream))
+        _check(rc, "gemm_conv2d")
+        return y
+
 
 _plans: dict = {}
 
@@ -218,6 +245,18 @@ def linear(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None = No
     if out is None:
         out = torch.empty(x.shape[0], weight.shape[0], device=x.device, dtype=out_dtype)
     return _plan_for(x.device, "nk").run(x, weight, out, bias, relu)
+
+
+def conv2d(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None, relu: bool = False, pad: int = 0,
+           out_dtype: torch.dtype | None = None, out: torch.Tensor | None = None):
+    """Stride-1 convolution, NHWC activations, weights Cout x R x S x C; returns
+    the (Nb*OH*OW) x Cout output (NHWC flattened)."""
+    Nb, H, W, _ = x.shape
+    Cout, R, S, _ = w.shape
+    if out is None:
+        out = torch.empty(Nb * (H + 2 * pad - R + 1) * (W + 2 * pad - S + 1), Cout, device=x.device,
+                          dtype=out_dtype or x.dtype)
+    return _plan_for(x.device, "nk").conv2d(x, w, out, bias, relu, pad)
 
 
 def im2col(x: torch.Tensor, R: int, S: int, pad: int = 0, stride: int = 1, out: torch.Tensor | None = None):

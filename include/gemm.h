@@ -134,6 +134,27 @@ const char* gemm_strerror(int code);
 int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad, int stride,
                 void* out, int64_t ld_out, int elem_bytes, void* stream);
 
+/* Convolution as an implicit GEMM (CMU 15-418 "DNNs and ML accelerators"
+ * notes, section 2.3: the im2col matrix need not be materialised; the GEMM's
+ * operand tiles are gathered from the activations as they are needed).
+ * Stride 1, zero padding `pad`:
+ *     y[(n*OH + oh)*OW + ow][f] = epilogue( sum_{r<R, s<S, c<C}
+ *         x[n][oh+r-pad][ow+s-pad][c] * w[f][r][s][c]  (+ bias[f]) )
+ * with OH = H + 2 pad - R + 1, OW = W + 2 pad - S + 1 and x read as 0 outside
+ * the image -- exactly gemm_run on gemm_im2col's matrix (M = Nb*OH*OW,
+ * K = R*S*C) and the N x K weight matrix w (N = Cout).  x is NHWC
+ * (Nb x H x W x C, contiguous), w is Cout x R x S x C (contiguous), y is
+ * M x Cout row-major with row pitch ldy >= Cout; all are caller-owned device
+ * memory; bias, epilogue and dtype as for gemm_run.  The plan's B-layout flag
+ * is ignored (w is always N x K).
+ * When C is a multiple of 64, R == S, x is 16-byte aligned and M > 128, the
+ * large-M kernel reads x through a TMA im2col tensor map (no extra memory);
+ * otherwise the im2col matrix is built in the plan's workspace first (the
+ * same result).  Returns as gemm_run. */
+int gemm_conv2d(gemm_plan_t plan, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S, int pad,
+                const void* x, const void* w, const void* bias, void* y, int64_t ldy, int epilogue, int dtype,
+                void* stream);
+
 /* --- controls and introspection (benchmarks and tests) ------------------ */
 
 /* Force a kernel (GEMM_KERNEL_*); GEMM_KERNEL_AUTO restores the dispatcher. */

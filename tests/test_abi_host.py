@@ -106,3 +106,7 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(G, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         G.lib()
+
+
+def test_conv2d_rejects_null_plan(lib):
+    assert G.lib().gemm_conv2d(None, 1, 8, 8, 64, 64, 3, 3, 1, P, P, None, P, 64, 0, 1, None) == G.ERR_INVALID_ARG

@@ -84,3 +84,99 @@ def test_full_conv_config_sampled(plan):
     assert np.all(np.abs(direct - C_ref) <= 1e-12 * (S + 1))
     case = GemmCase("conv", len(rows), Cout, 9 * Cin, b_nk=True, out="bf16")
     compare(case, Y[torch.from_numpy(rows).cuda()].cpu(), C_ref, S)
+
+
+# ---- implicit GEMM (gemm_conv2d): A tiles fetched from the NHWC activations
+# through a TMA im2col tensor map, no im2col matrix in memory
+
+IMPLICIT_SHAPES = [  # Nb, H, W, C, Cout, R(=S), pad
+    (2, 9, 9, 64, 32, 3, 1),        # M = 162: one pair tile, ragged
+    (1, 17, 13, 128, 200, 3, 1),    # two channel blocks per tap, ragged N
+    (3, 8, 8, 64, 64, 1, 0),        # 1 x 1 filter: a plain GEMM over pixels
+    (2, 12, 10, 64, 48, 5, 2),      # 5 x 5, pad 2
+    (2, 11, 11, 64, 16, 3, 0),      # no padding: 9 x 9 outputs
+    (4, 20, 20, 64, 256, 3, 1),     # M = 1600: several tiles, last one partial
+]
+
+
+def conv_out_hw(H, W, R, pad):
+    return H + 2 * pad - R + 1, W + 2 * pad - R + 1
+
+
+@pytest.mark.parametrize("shape", IMPLICIT_SHAPES)
+def test_implicit_conv_exact_every_output(shape):
+    Nb, H, W, C, Cout, R, pad = shape
+    x = int_bf16((Nb, H, W, C), 11 + sum(shape))
+    w = int_bf16((Cout, R, R, C), 12 + sum(shape))
+    OH, OW = conv_out_hw(H, W, R, pad)
+    with G.Plan(0, "kn") as p:   # the plan's B layout does not apply to convolutions
+        y = torch.full((Nb * OH * OW, Cout), float("nan"), device="cuda")
+        p.conv2d(x.cuda(), w.cuda(), y, pad=pad)
+        assert p.status() == 0
+        assert p.last_kernel == G.KERNEL_TC_PAIR
+        assert p.workspace_bytes == 0, "implicit path must not build an im2col matrix"
+    pos = [(n, oh, ow) for n in range(Nb) for oh in range(OH) for ow in range(OW)]
+    ref = oracle.conv2d_at(x, w, pad, pos)
+    assert np.array_equal(y.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_implicit_conv_bitwise_equals_explicit_gemm(out):
+    # same A tiles in the same order to the same MMAs: identical bits
+    Nb, H, W, C, Cout = 3, 23, 19, 128, 96
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(Nb, H, W, C, generator=g).bfloat16().cuda()
+    w = (torch.randn(Cout, 3, 3, C, generator=g) * (2 / (9 * C)) ** 0.5).bfloat16().cuda()
+    b = (torch.randn(Cout, generator=g) * 0.02).bfloat16().cuda()
+    od = torch.bfloat16 if out == "bf16" else torch.float32
+    with G.Plan(0, "nk") as p:
+        y_imp = torch.empty(Nb * H * W, Cout, dtype=od, device="cuda")
+        p.conv2d(x, w, y_imp, bias=b, relu=True, pad=1)
+        cols = G.im2col(x, 3, 3, 1, 1)
+        y_exp = torch.empty_like(y_imp)
+        p.run(cols, w.reshape(Cout, -1), y_exp, b, relu=True)
+        assert p.status() == 0
+    assert torch.equal(y_imp.view(torch.int16 if out == "bf16" else torch.int32),
+                       y_exp.view(torch.int16 if out == "bf16" else torch.int32))
+
+
+@pytest.mark.parametrize("shape", [(2, 9, 9, 16, 32, 3, 1),     # C not a multiple of 64
+                                   (1, 5, 5, 64, 24, 3, 1),     # M = 25: small-M path
+                                   (2, 9, 9, 64, 8, 1, 0)])     # 1 x 1, N = 8
+def test_conv_fallback_paths_exact(shape):
+    Nb, H, W, C, Cout, R, pad = shape
+    x = int_bf16((Nb, H, W, C), 31 + sum(shape))
+    w = int_bf16((Cout, R, R, C), 32 + sum(shape))
+    OH, OW = conv_out_hw(H, W, R, pad)
+    with G.Plan(0, "nk") as p:
+        y = torch.full((Nb * OH * OW, Cout), float("nan"), device="cuda")
+        p.conv2d(x.cuda(), w.cuda(), y, pad=pad)
+        assert p.status() == 0
+    pos = [(n, oh, ow) for n in range(Nb) for oh in range(OH) for ow in range(OW)]
+    assert np.array_equal(y.double().cpu().numpy(), oracle.conv2d_at(x, w, pad, pos))
+
+
+def test_full_conv_config_implicit_sampled(plan):
+    Nb, H, W, Cin, Cout = CONV["Nb"], CONV["H"], CONV["W"], CONV["Cin"], CONV["Cout"]
+    x, w = conv_tensors()
+    xd, wd = x.cuda(), w.cuda()
+    y = torch.empty(Nb * H * W, Cout, dtype=torch.bfloat16, device="cuda")
+    plan.set_kernel(G.KERNEL_AUTO)
+    plan.conv2d(xd, wd, y, pad=1)
+    assert plan.status() == 0
+    assert plan.last_kernel == G.KERNEL_TC_PAIR
+    rng = np.random.default_rng(5)
+    pos = {(n, oh, ow) for n in (0, Nb - 1) for oh in (0, 1, H // 2, H - 1) for ow in (0, 1, W // 2, W - 1)}
+    pos |= {(int(rng.integers(Nb)), int(rng.integers(H)), int(rng.integers(W))) for _ in range(48)}
+    pos = sorted(pos)
+    rows = np.array([(n * H + oh) * W + ow for n, oh, ow in pos])
+    A_rows = oracle.im2col_rows(x, 3, 3, 1, rows)
+    C_ref, S = oracle.gemm(A_rows, w.reshape(Cout, -1), b_nk=True, with_mag=True)
+    case = GemmCase("conv_implicit", len(rows), Cout, 9 * Cin, b_nk=True, out="bf16")
+    compare(case, y[torch.from_numpy(rows).cuda()].cpu(), C_ref, S)
+    # and the whole output equals the explicit path bit for bit
+    cols = G.im2col(xd, 3, 3, 1, 1)
+    y_exp = torch.empty_like(y)
+    plan.run(cols, wd.reshape(Cout, -1), y_exp)
+    assert plan.status() == 0
+    assert torch.equal(y.view(torch.int16), y_exp.view(torch.int16))
