@@ -188,8 +188,8 @@ int64_t tail_split(int64_t T, int64_t U, int enabled) {
 // Skinny-M launch: feature tiles of 128 weight rows, split-K over a cluster of
 // S CTAs chosen so the whole grid is resident at once.
 int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* W,
-               int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, int dtype, bool w_nk,
-               CUtensorMapDataType in_dt, cudaStream_t stream) {
+               int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, const EpiArgs& ex, int dtype,
+               bool w_nk, CUtensorMapDataType in_dt, cudaStream_t stream) {
     const int mpad = (int)round_up(M, 16);
     const int tmem_cols = mpad <= 32 ? 32 : (mpad <= 64 ? 64 : 128);
     const int64_t n_tiles = (N + 127) / 128;
@@ -249,6 +249,7 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     sp.x_lsu = p->skinny_x_lsu ? 1u : 0u;
     sp.X = X; sp.ldx = ldx; sp.pdl = p->pdl; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
     sp.epi = epi;
+    sp.ex = ex;
     const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;
     sp.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((w_nk ? 0u : 1u) << 15) | ((uint32_t)(mpad >> 3) << 17) |
                ((uint32_t)(128 >> 4) << 24);
@@ -444,17 +445,44 @@ int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int 
 
 namespace {
 
+EpiArgs plain_epilogue() {
+    EpiArgs ex;
+    std::memset(&ex, 0, sizeof(ex));
+    ex.alpha = 1.0f;
+    return ex;
+}
+
+// Epilogue flags and operands of gemm_epilogue_args_t; C is also the previous C.
+int extended_epilogue(const gemm_epilogue_args_t* a, int dtype, const void* C, int64_t ldc, uint32_t* flags,
+                      EpiArgs* ex) {
+    *ex = plain_epilogue();
+    uint32_t f = 0;
+    if (a->bias) f |= EPI_BIAS;
+    if (a->relu) f |= EPI_RELU;
+    if (a->scale) { f |= EPI_SCALE; ex->scale = a->scale; ex->scale_vec16 = aligned16(a->scale) ? 1u : 0u; }
+    if (a->alpha != 1.0f) { f |= EPI_ALPHA; ex->alpha = a->alpha; }
+    if (a->beta != 0.0f) {
+        if (C == nullptr) return GEMM_ERR_INVALID_ARG;
+        f |= EPI_BETA;
+        ex->beta = a->beta;
+        ex->c_old = C;
+        ex->ldc_old = ldc;
+        ex->c_old_vec16 = (aligned16(C) && (ldc * out_bytes(dtype)) % 16 == 0) ? 1u : 0u;
+    }
+    *flags = f;
+    return GEMM_OK;
+}
+
 // Validated arguments; M, N > 0.  b_nk: B is N x K.  conv: A is the im2col
 // view of an activation tensor (then A and lda are unused).
 int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-             int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype, cudaStream_t stream,
-             const ConvA* conv) {
+             int64_t ldb, const void* bias, void* C, int64_t ldc, uint32_t epi, const EpiArgs& ex, int dtype,
+             cudaStream_t stream, const ConvA* conv) {
     int rc = GEMM_OK;
-    const uint32_t epi = (uint32_t)epilogue;   // GEMM_EPI_* == EpiFlags bits
     cudaError_t e;
 
     if (K == 0) {
-        e = launch_fill_epilogue(dtype, M, N, bias, epi, C, ldc, stream);
+        e = launch_fill_epilogue(dtype, M, N, bias, epi, ex, C, ldc, stream);
         if (e != cudaSuccess) return record(p, e);
         p->launches += 1;
         p->last_kernel = GEMM_KERNEL_FILL;
@@ -508,7 +536,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
 
     const CUtensorMapDataType in_dt = in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (skinny) {
-        rc = run_skinny(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, dtype, b_nk, in_dt, stream);
+        rc = run_skinny(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, b_nk, in_dt, stream);
         if (rc != GEMM_OK) return rc;
         p->last_kernel = kernel;
         p->last_stream = stream; p->have_stream = true;
@@ -537,6 +565,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     prm.num_k_blocks = (int32_t)((K + TC_BK - 1) / TC_BK);
     prm.group_m = p->group_m;
     prm.epi = epi;
+    prm.ex = ex;
     prm.idesc = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN);
     prm.b_mn_major = b_nk ? 0u : 1u;
     prm.bias = bias;
@@ -591,14 +620,38 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     if (rc != GEMM_OK) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
     DeviceGuard g(p->device);
-    return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype,
+    return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, bias, C, ldc, (uint32_t)epilogue,
+                    plain_epilogue(), dtype, reinterpret_cast<cudaStream_t>(stream_v), nullptr);
+}
+
+int gemm_run_ex(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                int64_t ldb, void* C, int64_t ldc, const gemm_epilogue_args_t* epi, int dtype, void* stream_v) {
+    if (!p || !epi) return GEMM_ERR_INVALID_ARG;
+    uint32_t flags = 0;
+    EpiArgs ex;
+    int rc = extended_epilogue(epi, dtype, C, ldc, &flags, &ex);
+    if (rc != GEMM_OK) return rc;
+    rc = gemm_validate(p->flags, M, N, K, A, lda, B, ldb, epi->bias, C, ldc, (int)(flags & 3u), dtype);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceGuard g(p->device);
+    return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, epi->bias, C, ldc, flags, ex, dtype,
                     reinterpret_cast<cudaStream_t>(stream_v), nullptr);
 }
 
 int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S, int pad,
-                const void* x, const void* w, const void* bias, void* y, int64_t ldy, int epilogue, int dtype,
+                const void* x, const void* w, void* y, int64_t ldy, const gemm_epilogue_args_t* epi_args, int dtype,
                 void* stream_v) {
     if (!p) return GEMM_ERR_INVALID_ARG;
+    uint32_t epi = 0;
+    EpiArgs ex = plain_epilogue();
+    const void* bias = nullptr;
+    if (epi_args) {
+        int rc0 = extended_epilogue(epi_args, dtype, y, ldy, &epi, &ex);
+        if (rc0 != GEMM_OK) return rc0;
+        bias = epi_args->bias;
+    }
+    const int epilogue = (int)(epi & 3u);
     if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
     if (OH < 0 || OW < 0) return GEMM_ERR_INVALID_ARG;
@@ -617,17 +670,17 @@ int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int6
                           p->forced_kernel != GEMM_KERNEL_SKINNY && g_encode_im2col != nullptr;
     if (implicit) {
         const ConvA cv{x, Nb, H, W, C, R, S, pad};
-        return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epilogue, dtype, stream, &cv);
+        return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epi, ex, dtype, stream, &cv);
     }
     // otherwise: explicit im2col matrix in the plan workspace, then the GEMM
-    if (K == 0) return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epilogue, dtype, stream, nullptr);
+    if (K == 0) return run_impl(p, true, M, N, K, nullptr, 0, w, K, bias, y, ldy, epi, ex, dtype, stream, nullptr);
     const int64_t ldk = round_up(K, 8);
     rc = ensure_workspace(p, (size_t)(M * ldk * 2));
     if (rc != GEMM_OK) return rc;
     cudaError_t e = launch_im2col(x, Nb, H, W, C, R, S, pad, 1, p->workspace, ldk, 2, stream);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
-    return run_impl(p, true, M, N, K, p->workspace, ldk, w, K, bias, y, ldy, epilogue, dtype, stream, nullptr);
+    return run_impl(p, true, M, N, K, p->workspace, ldk, w, K, bias, y, ldy, epi, ex, dtype, stream, nullptr);
 }
 
 }  // extern "C"

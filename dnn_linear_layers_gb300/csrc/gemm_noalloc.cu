@@ -135,7 +135,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     const uint32_t epi = (uint32_t)epilogue;
 
     if (K == 0) {
-        e = gb300::launch_fill_epilogue(dtype, M, N, bias, epi, C, ldc, stream);
+        gb300::EpiArgs ex;
+        std::memset(&ex, 0, sizeof(ex));
+        e = gb300::launch_fill_epilogue(dtype, M, N, bias, epi, ex, C, ldc, stream);
         return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 

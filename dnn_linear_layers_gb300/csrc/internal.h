@@ -10,7 +10,21 @@ namespace gb300 {
 // Output/input type combinations, same numbering as gemm_dtype_t.
 enum Dtype : int { DT_BF16_F32 = 0, DT_BF16_BF16 = 1, DT_F16_F32 = 2, DT_F16_F16 = 3 };
 
-enum EpiFlags : uint32_t { EPI_BIAS = 1u, EPI_RELU = 2u };
+// Epilogue on the fp32 accumulator, in this order: t = alpha * acc (EPI_ALPHA);
+// t *= scale[n] (EPI_SCALE); t += bias[n] (EPI_BIAS); t += beta * C_old[m][n]
+// (EPI_BETA); t = max(t, 0) (EPI_RELU); then the single cast to the output type.
+enum EpiFlags : uint32_t { EPI_BIAS = 1u, EPI_RELU = 2u, EPI_SCALE = 4u, EPI_ALPHA = 8u, EPI_BETA = 16u };
+
+// Operands of the extended epilogue (unused fields are ignored).
+struct EpiArgs {
+    float alpha;           // EPI_ALPHA
+    float beta;            // EPI_BETA
+    const void* scale;     // EPI_SCALE: N per-column factors of the input type
+    const void* c_old;     // EPI_BETA: previous C (output type), row pitch ldc_old elements
+    int64_t ldc_old;
+    uint32_t scale_vec16;  // scale is 16-byte aligned
+    uint32_t c_old_vec16;  // c_old and ldc_old * element size are 16-byte aligned
+};
 
 // Bits written into the device status word by a wait that ran out of time.
 enum StatusBits : int {
@@ -50,6 +64,7 @@ struct TcParams {
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
     uint32_t multicast;    // 1: clusters of two CTA pairs share B by TMA multicast (cta_group 2)
+    EpiArgs ex;            // alpha / scale / beta operands of the epilogue
     // Implicit-GEMM convolution (conv != 0): A is not a matrix but an NHWC
     // activation tensor read through an im2col tensor map; row m of A is
     // output pixel m = (n * out_h + oh) * out_w + ow and k-block kb is channel
@@ -96,6 +111,7 @@ struct SkinnyParams {
     uint32_t x_lsu;        // 1: the epilogue warps copy X with cp.async instead of TMA
     const void* X;         // X (M x K, row pitch ldx elements), for the cp.async path
     int64_t ldx;
+    EpiArgs ex;            // alpha / scale / beta operands of the epilogue
 };
 
 // at most this many skinny CTAs share an SM (the kernel's launch bounds size
@@ -109,7 +125,7 @@ cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& 
 // Auxiliary kernels ------------------------------------------------------
 // C[i][j] = epilogue(0) for K == 0 (bias and/or ReLU of an empty sum).
 cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,
-                                 void* C, int64_t ldc, cudaStream_t stream);
+                                 const EpiArgs& ex, void* C, int64_t ldc, cudaStream_t stream);
 
 // Copy a rows x cols matrix of elem_bytes-sized elements between strides.
 // When the destination is 16-byte aligned with ld_dst >= cols rounded up to

@@ -21,13 +21,15 @@ namespace gb300 {
 namespace {
 
 template <typename InT, typename OutT>
-__global__ void fill_epilogue_kernel(int64_t M, int64_t N, const InT* bias, uint32_t epi, OutT* C, int64_t ldc) {
+__global__ void fill_epilogue_kernel(int64_t M, int64_t N, const InT* bias, uint32_t epi, float beta,
+                                     const OutT* c_old, int64_t ldc_old, OutT* C, int64_t ldc) {
     const int64_t total = M * N;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = t / N, j = t - i * N;
-        float v = 0.0f;
+        float v = 0.0f;   // alpha * (empty sum) * scale = 0
         if (epi & EPI_BIAS) v += static_cast<float>(bias[j]);
+        if (epi & EPI_BETA) v += beta * static_cast<float>(c_old[i * ldc_old + j]);
         if (epi & EPI_RELU) v = fmaxf(v, 0.0f);
         C[i * ldc + j] = static_cast<OutT>(v);
     }
@@ -124,25 +126,25 @@ int blocks_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,
-                                 void* C, int64_t ldc, cudaStream_t stream) {
+                                 const EpiArgs& ex, void* C, int64_t ldc, cudaStream_t stream) {
     const int threads = 256;
     const int blocks = blocks_for(M * N, threads);
     switch (dtype) {
         case DT_BF16_F32:
             fill_epilogue_kernel<__nv_bfloat16, float><<<blocks, threads, 0, stream>>>(
-                M, N, (const __nv_bfloat16*)bias, epi, (float*)C, ldc);
+                M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const float*)ex.c_old, ex.ldc_old, (float*)C, ldc);
             break;
         case DT_BF16_BF16:
             fill_epilogue_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, threads, 0, stream>>>(
-                M, N, (const __nv_bfloat16*)bias, epi, (__nv_bfloat16*)C, ldc);
+                M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const __nv_bfloat16*)ex.c_old, ex.ldc_old, (__nv_bfloat16*)C, ldc);
             break;
         case DT_F16_F32:
             fill_epilogue_kernel<__half, float><<<blocks, threads, 0, stream>>>(
-                M, N, (const __half*)bias, epi, (float*)C, ldc);
+                M, N, (const __half*)bias, epi, ex.beta, (const float*)ex.c_old, ex.ldc_old, (float*)C, ldc);
             break;
         case DT_F16_F16:
             fill_epilogue_kernel<__half, __half><<<blocks, threads, 0, stream>>>(
-                M, N, (const __half*)bias, epi, (__half*)C, ldc);
+                M, N, (const __half*)bias, epi, ex.beta, (const __half*)ex.c_old, ex.ldc_old, (__half*)C, ldc);
             break;
         default:
             return cudaErrorInvalidValue;

@@ -37,7 +37,7 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kWStage = 128 * 64 * 2;      // 128 features x 64 k, 16 KB
-constexpr int kMiscBytes = 1024;
+constexpr int kMiscBytes = 2048;          // barriers, then bias and scale staging
 
 __device__ __forceinline__ void cluster_arrive_wait() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -101,6 +101,9 @@ template <typename T> __device__ __forceinline__ T from_float(float v);
 template <> __device__ __forceinline__ float from_float<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 template <> __device__ __forceinline__ __half from_float<__half>(float v) { return __float2half_rn(v); }
+__device__ __forceinline__ float out_float(float v) { return v; }
+__device__ __forceinline__ float out_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float out_float(__half v) { return __half2float(v); }
 
 // Grid: num_n_tiles * S CTAs, clusters of S along x.  CTA rank r of a cluster
 // owns k-blocks [r*nkb/S, (r+1)*nkb/S) of feature tile blockIdx.x / S.
@@ -129,7 +132,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // stages of 16 KB + mpad x 128 B, hence at least mpad x 512 B for mpad <= 128
     float* red = reinterpret_cast<float*>(base_ptr);
     const uint32_t red_addr = base;
-    float* bias_s = reinterpret_cast<float*>(base_ptr + off_misc + 512);   // 128 floats: the tile's bias
+    float* bias_s = reinterpret_cast<float*>(base_ptr + off_misc + 512);    // 128 floats: the tile's bias
+    float* scale_s = reinterpret_cast<float*>(base_ptr + off_misc + 1024);  // 128 floats: its scale
 
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
     const int S = p.splits;
@@ -285,9 +289,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // the weight stream at the end)
     if (warp >= 2) {
         const int et = (int)threadIdx.x - 64;
-        float bvl = 0.0f;
+        float bvl = 0.0f, svl = 1.0f;
         if ((p.epi & EPI_BIAS) && f0 + et < p.N) bvl = to_float<InT>(reinterpret_cast<const InT*>(p.bias)[f0 + et]);
+        if ((p.epi & EPI_SCALE) && f0 + et < p.N)
+            svl = to_float<InT>(reinterpret_cast<const InT*>(p.ex.scale)[f0 + et]);
+        if (p.epi & EPI_ALPHA) svl *= p.ex.alpha;   // alpha * acc * scale: one factor per feature
         bias_s[et] = bvl;
+        scale_s[et] = svl;
     }
     // ---- split-K reduction.  Every CTA of the cluster has finished its MMAs
     // once barrier (1) is passed, so all operand rings are free; each CTA then
@@ -353,9 +361,15 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int n = f0 + (int)rank * per + fl;      // first of the 8 features
         const bool relu = (p.epi & EPI_RELU) != 0;
         const bool full8 = n + 8 <= p.N;
-        float bv[8];   // staged by the epilogue warps; ordered by the cluster barriers
+        float bv[8], sv[8];   // staged by the epilogue warps; ordered by the cluster barriers
 #pragma unroll
-        for (int e = 0; e < 8; ++e) bv[e] = bias_s[(int)rank * per + fl + e];
+        for (int e = 0; e < 8; ++e) {
+            bv[e] = bias_s[(int)rank * per + fl + e];
+            sv[e] = scale_s[(int)rank * per + fl + e];
+        }
+        const bool scaled = (p.epi & (EPI_SCALE | EPI_ALPHA)) != 0;
+        const bool beta = (p.epi & EPI_BETA) != 0;
+        const bool vec_c = full8 && p.ex.c_old_vec16;
         OutT* const Y = reinterpret_cast<OutT*>(p.Y);
         const bool vec = full8 && (reinterpret_cast<uintptr_t>(Y) % 16 == 0) &&
                          ((p.ldy * (int64_t)sizeof(OutT)) % 16 == 0);
@@ -371,9 +385,32 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 a1.x += v1.x; a1.y += v1.y; a1.z += v1.z; a1.w += v1.w;
             }
             float o[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float cv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cv[e] = 0.0f;
+            if (beta) {
+                const OutT* crow = reinterpret_cast<const OutT*>(p.ex.c_old) + (int64_t)m * p.ex.ldc_old + n;
+                if (vec_c) {
+                    OutT c8[8];
+                    if (sizeof(OutT) == 2) {
+                        *reinterpret_cast<uint4*>(c8) = *reinterpret_cast<const uint4*>(crow);
+                    } else {
+                        reinterpret_cast<uint4*>(c8)[0] = reinterpret_cast<const uint4*>(crow)[0];
+                        reinterpret_cast<uint4*>(c8)[1] = reinterpret_cast<const uint4*>(crow)[1];
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cv[e] = out_float(c8[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (n + e < p.N) cv[e] = out_float(crow[e]);
+                }
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
+                if (scaled) o[e] *= sv[e];
                 o[e] += bv[e];
+                if (beta) o[e] += p.ex.beta * cv[e];
                 if (relu) o[e] = fmaxf(o[e], 0.0f);
             }
             OutT* yrow = Y + (int64_t)m * p.ldy + n;

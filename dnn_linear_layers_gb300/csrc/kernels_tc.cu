@@ -134,6 +134,9 @@ template <> struct OutTraits<__half> { static constexpr int kCols = 64; };
 template <typename InT> __device__ __forceinline__ float to_f32(InT v);
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+__device__ __forceinline__ float out_to_f32(float v) { return v; }
+__device__ __forceinline__ float out_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float out_to_f32(__half v) { return __half2float(v); }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, __nv_bfloat16*) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -405,9 +408,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
                 }
+                const int cb = n0 + c * kCols;
+                if (p.epi & EPI_ALPHA) {
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) v[j] *= p.ex.alpha;
+                }
+                if (p.epi & EPI_SCALE) {
+                    // per-column factors, like the bias: one broadcast load per vector
+                    const InT* sc = reinterpret_cast<const InT*>(p.ex.scale);
+                    if (p.ex.scale_vec16 && cb + kCols <= p.N) {
+                        const uint4* sv = reinterpret_cast<const uint4*>(sc + cb);
+#pragma unroll
+                        for (int j = 0; j < kCols / 8; ++j) {
+                            const uint4 u = __ldg(sv + j);
+                            const InT* e = reinterpret_cast<const InT*>(&u);
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) v[8 * j + t] *= to_f32<InT>(e[t]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j)
+                            if (cb + j < p.N) v[j] *= to_f32<InT>(sc[cb + j]);
+                    }
+                }
                 if (has_bias) {
                     // every lane reads the same addresses: one broadcast load per vector
-                    const int cb = n0 + c * kCols;
                     if (p.bias_vec16 && cb + kCols <= p.N) {
                         const uint4* bv = reinterpret_cast<const uint4*>(bias + cb);
 #pragma unroll
@@ -421,6 +446,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < kCols; ++j)
                             if (cb + j < p.N) v[j] += to_f32<InT>(bias[cb + j]);
+                    }
+                }
+                if (p.epi & EPI_BETA) {
+                    // lane = row of the chunk: its 128 bytes of the previous C, read
+                    // before this warp's store of the same elements is issued
+                    const int row = row0 + (int)lane;
+                    if (row < p.M) {
+                        const OutT* crow = reinterpret_cast<const OutT*>(p.ex.c_old) + (int64_t)row * p.ex.ldc_old + cb;
+                        if (p.ex.c_old_vec16 && cb + kCols <= p.N) {
+                            constexpr int kPer = 16 / (int)sizeof(OutT);
+#pragma unroll
+                            for (int j = 0; j < kCols / kPer; ++j) {
+                                const uint4 u = *reinterpret_cast<const uint4*>(crow + kPer * j);
+                                const OutT* e = reinterpret_cast<const OutT*>(&u);
+#pragma unroll
+                                for (int t = 0; t < kPer; ++t) v[kPer * j + t] += p.ex.beta * out_to_f32(e[t]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < kCols; ++j)
+                                if (cb + j < p.N) v[j] += p.ex.beta * out_to_f32(crow[j]);
+                        }
                     }
                 }
                 if (relu) {

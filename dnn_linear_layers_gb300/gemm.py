@@ -24,6 +24,16 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOU
 
 # Every symbol include/gemm.h declares, with its ctypes signature.
 _vp, _i64, _int, _uint, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_uint64
+
+
+class EpilogueArgs(ctypes.Structure):
+    """gemm_epilogue_args_t: t = alpha*acc; t *= scale[j]; t += bias[j];
+    t += beta*C_old[i][j]; ReLU; cast."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("scale", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("relu", ctypes.c_int)]
+
+
+_epi_p = ctypes.POINTER(EpilogueArgs)
 SIGNATURES = {
     "gemm_plan_create": (_int, [ctypes.POINTER(_vp), _int, _uint]),
     "gemm_run": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _vp]),
@@ -41,8 +51,9 @@ SIGNATURES = {
     "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
     "gemm_im2col": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp, _i64, _int, _vp]),
     "gemm_run_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _uint, _vp, _vp]),
-    "gemm_conv2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _i64, _int, _int,
+    "gemm_conv2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _epi_p, _int,
                            _vp]),
+    "gemm_run_ex": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _epi_p, _int, _vp]),
 }
 
 _lib = None
@@ -172,8 +183,10 @@ class Plan:
                               epilogue, dtype, _stream_handle(stream))
 
     def run(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, bias: torch.Tensor | None = None,
-            relu: bool = False, stream=None):
-        """C = (A . B (+bias)) (ReLU), written into the caller's C."""
+            relu: bool = False, stream=None, alpha: float = 1.0, beta: float = 0.0,
+            scale: torch.Tensor | None = None):
+        """C = relu?(alpha * (A . B) * scale + bias + beta * C), written into the
+        caller's C (gemm_run, or gemm_run_ex when alpha, beta or scale is set)."""
         M, K = A.shape
         N = B.shape[0] if self.b_nk else B.shape[1]
         if (B.shape[1] if self.b_nk else B.shape[0]) != K or tuple(C.shape) != (M, N):
@@ -185,6 +198,15 @@ class Plan:
                 raise ValueError("operands must be CUDA tensors")
         if bias is not None and (bias.dim() != 1 or bias.shape[0] != N or bias.stride(0) != 1):
             raise ValueError("bias must be a contiguous vector of length N")
+        if scale is not None and (scale.dim() != 1 or scale.shape[0] != N or scale.stride(0) != 1
+                                  or scale.dtype != A.dtype or scale.device.type != "cuda"):
+            raise ValueError("scale must be a contiguous CUDA vector of length N in the input dtype")
+        if alpha != 1.0 or beta != 0.0 or scale is not None:
+            ea = _epilogue_args(alpha, beta, scale, bias, relu)
+            rc = lib().gemm_run_ex(self._h, M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C),
+                                   ctypes.byref(ea), dtype_code(A.dtype, C.dtype), _stream_handle(stream))
+            _check(rc, "gemm_run_ex")
+            return C
         epi = (EPI_BIAS if bias is not None else 0) | (EPI_RELU if relu else 0)
         rc = self.run_raw(M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B),
                           bias.data_ptr() if bias is not None else None, C.data_ptr(), _ld(C), epi,
@@ -193,7 +215,8 @@ class Plan:
         return C
 
     def conv2d(self, x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: torch.Tensor | None = None,
-               relu: bool = False, pad: int = 0, stream=None):
+               relu: bool = False, pad: int = 0, stream=None, alpha: float = 1.0, beta: float = 0.0,
+               scale: torch.Tensor | None = None):
         """Stride-1 convolution of the NHWC tensor x (Nb x H x W x C) with
         w (Cout x R x S x C) into y ((Nb*OH*OW) x Cout, row-major)."""
         if x.dim() != 4 or w.dim() != 4 or not x.is_contiguous() or not w.is_contiguous():
@@ -210,12 +233,20 @@ class Plan:
                 raise ValueError("operands must be CUDA tensors")
         if bias is not None and (bias.dim() != 1 or bias.shape[0] != Cout or bias.stride(0) != 1):
             raise ValueError("bias must be a contiguous vector of length Cout")
-        epi = (EPI_BIAS if bias is not None else 0) | (EPI_RELU if relu else 0)
+        if scale is not None and (scale.dim() != 1 or scale.shape[0] != Cout or scale.stride(0) != 1
+                                  or scale.dtype != x.dtype or scale.device.type != "cuda"):
+            raise ValueError("scale must be a contiguous CUDA vector of length Cout in the input dtype")
+        ea = _epilogue_args(alpha, beta, scale, bias, relu)
         rc = lib().gemm_conv2d(self._h, Nb, H, W, C, Cout, R, S, pad, x.data_ptr(), w.data_ptr(),
-                               bias.data_ptr() if bias is not None else None, y.data_ptr(), _ld(y), epi,
-                               dtype_code(x.dtype, y.dtype), _stream_handle(stream))
+                               y.data_ptr(), _ld(y), ctypes.byref(ea), dtype_code(x.dtype, y.dtype),
+                               _stream_handle(stream))
         _check(rc, "gemm_conv2d")
         return y
+
+
+def _epilogue_args(alpha, beta, scale, bias, relu) -> EpilogueArgs:
+    return EpilogueArgs(float(alpha), float(beta), scale.data_ptr() if scale is not None else None,
+                        bias.data_ptr() if bias is not None else None, int(bool(relu)))
 
 
 _plans: dict = {}

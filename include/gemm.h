@@ -96,6 +96,25 @@ typedef enum {
 #define GEMM_ERR_DEVICE_TIMEOUT (-5)  /* a device-side wait ran out of time    */
 #define GEMM_ERR_NO_MEMORY (-6)       /* workspace allocation failed           */
 
+/* Extended epilogue (gemm_run_ex, gemm_conv2d), applied to the fp32
+ * accumulator acc = sum_k A[i][k] B(k, j) in this order:
+ *     t = alpha * acc;  t = t * scale[j]   (if scale);  t = t + bias[j] (if bias);
+ *     t = t + beta * C_old[i][j]           (if beta != 0);  t = max(0, t) (if relu);
+ *     C[i][j] = cast(t).
+ * With scale = bias = NULL, relu = 0 this is the BLAS update C = alpha A.B +
+ * beta C (youngju.dev "GEMM to FlashAttention", "GEMM interface"); scale, bias
+ * and relu give the per-channel scale / bias / ReLU of a fused convolution
+ * epilogue (CMU 15-418 notes, section 3.1).  C_old is C itself, read before it
+ * is written (element by element, so C may be updated in place); scale and
+ * bias hold N values of the input type (device memory). */
+typedef struct {
+    float alpha;          /* factor on A.B: 1 for the plain product           */
+    float beta;           /* factor on the previous C: 0 = C is only written  */
+    const void* scale;    /* NULL or N per-column factors                     */
+    const void* bias;     /* NULL or N per-column addends                     */
+    int relu;             /* nonzero: ReLU before the cast                    */
+} gemm_epilogue_args_t;
+
 /* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK,
  * optionally | GEMM_B_CONST and | GEMM_TC_MULTICAST.
  * Allocates the plan and its device status word; restores the caller's
@@ -109,6 +128,13 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
 int gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
              void* C, int64_t ldc, int epilogue, int dtype, void* stream);
+
+/* As gemm_run with the extended epilogue `epi` (not NULL; see
+ * gemm_epilogue_args_t).  When epi->beta != 0 the previous contents of C are
+ * read (C must be initialised).  Same returns as gemm_run. */
+int gemm_run_ex(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                const void* A, int64_t lda, const void* B, int64_t ldb,
+                void* C, int64_t ldc, const gemm_epilogue_args_t* epi, int dtype, void* stream);
 
 /* Synchronise the stream of the last gemm_run and report device-side errors:
  * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last call (the
@@ -145,14 +171,15 @@ int gemm_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int 
  * K = R*S*C) and the N x K weight matrix w (N = Cout).  x is NHWC
  * (Nb x H x W x C, contiguous), w is Cout x R x S x C (contiguous), y is
  * M x Cout row-major with row pitch ldy >= Cout; all are caller-owned device
- * memory; bias, epilogue and dtype as for gemm_run.  The plan's B-layout flag
- * is ignored (w is always N x K).
+ * memory; epi is NULL (plain convolution) or the extended epilogue of
+ * gemm_run_ex (per-channel scale, bias, ReLU, beta * y); dtype as for gemm_run.
+ * The plan's B-layout flag is ignored (w is always N x K).
  * When C is a multiple of 64, R == S, x is 16-byte aligned and M > 128, the
  * large-M kernel reads x through a TMA im2col tensor map (no extra memory);
  * otherwise the im2col matrix is built in the plan's workspace first (the
  * same result).  Returns as gemm_run. */
 int gemm_conv2d(gemm_plan_t plan, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S, int pad,
-                const void* x, const void* w, const void* bias, void* y, int64_t ldy, int epilogue, int dtype,
+                const void* x, const void* w, void* y, int64_t ldy, const gemm_epilogue_args_t* epi, int dtype,
                 void* stream);
 
 /* --- controls and introspection (benchmarks and tests) ------------------ */

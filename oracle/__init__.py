@@ -111,6 +111,35 @@ def gemm(A, B, bias=None, relu: bool = False, b_nk: bool = False,
     return (C, S) if with_mag else C
 
 
+def epilogue_ex(P, alpha=1.0, beta=0.0, C0=None, scale=None, bias=None, relu=False):
+    """The extended epilogue written out on a float64 product P (M x N):
+    t = alpha * P; t = t * scale[j]; t = t + bias[j]; t = t + beta * C0[i][j];
+    t = max(0, t) -- each step only when its operand is given (the BLAS update
+    C = alpha A.B + beta C of the youngju.dev "GEMM interface" listing, plus the
+    per-channel scale / bias / ReLU of the CMU 15-418 notes' fused convolution,
+    section 3.1)."""
+    t = float(alpha) * np.asarray(P, dtype=np.float64)
+    if scale is not None:
+        t = t * _f64(scale).reshape(1, -1)
+    if bias is not None:
+        t = t + _f64(bias).reshape(1, -1)
+    if beta != 0.0:
+        t = t + float(beta) * _f64(C0)
+    if relu:
+        t = np.maximum(t, 0.0)
+    return t
+
+
+def gemm_ex(A, B, alpha=1.0, beta=0.0, C0=None, scale=None, bias=None, relu=False, b_nk=False, threads=0):
+    """C = epilogue_ex(A.B) in float64, with the magnitude bound of each output:
+    returns (C, S) where S = |alpha * scale_j| * sum_k |A_ik B_kj| (the part of
+    the parity tolerance that scales with the products)."""
+    P, S = gemm(A, B, b_nk=b_nk, with_mag=True, threads=threads)
+    C = epilogue_ex(P, alpha, beta, C0, scale, bias, relu)
+    f = abs(float(alpha)) * (np.abs(_f64(scale)).reshape(1, -1) if scale is not None else 1.0)
+    return C, S * f
+
+
 def gemm_rows(A, B, rows, bias=None, relu=False, b_nk=False, with_mag=False, threads=0):
     """Full rows ``rows`` of the product (len(rows) x N)."""
     A = _f64(A); B = _f64(B)

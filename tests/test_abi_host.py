@@ -109,4 +109,9 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
 
 
 def test_conv2d_rejects_null_plan(lib):
-    assert G.lib().gemm_conv2d(None, 1, 8, 8, 64, 64, 3, 3, 1, P, P, None, P, 64, 0, 1, None) == G.ERR_INVALID_ARG
+    assert G.lib().gemm_conv2d(None, 1, 8, 8, 64, 64, 3, 3, 1, P, P, P, 64, None, 1, None) == G.ERR_INVALID_ARG
+
+
+def test_run_ex_rejects_null_plan_and_args(lib):
+    ea = G.EpilogueArgs(1.0, 0.0, None, None, 0)
+    assert G.lib().gemm_run_ex(None, 8, 8, 8, P, 8, P, 8, P, 8, ctypes.byref(ea), 1, None) == G.ERR_INVALID_ARG

@@ -318,3 +318,43 @@ def test_input_generators_are_seeded_and_exact():
     assert torch.equal(a, b) and a.dtype == torch.bfloat16
     i = int_bf16((100,), 2)
     assert i.float().abs().max() <= 4 and torch.equal(i.float(), i.float().round())
+
+
+def test_extended_epilogue_exact_against_integer_closed_form():
+    # integers and powers of two: every value below is exact in float64, so the
+    # oracle must equal an independent int64 computation of the same formula
+    rng = np.random.default_rng(41)
+    M, N, K = 9, 13, 17
+    A = rng.integers(-4, 5, size=(M, K)); B = rng.integers(-4, 5, size=(K, N))
+    C0 = rng.integers(-50, 51, size=(M, N))
+    e = rng.integers(0, 4, size=N)                 # scale = 2^e
+    bias = rng.integers(-20, 21, size=N)
+    P = A.astype(np.int64) @ B.astype(np.int64)
+    want = 2 * P * (1 << e)[None, :] + bias[None, :] - 3 * C0     # alpha 2, beta -3
+    got, S = oracle.gemm_ex(A, B, alpha=2.0, beta=-3.0, C0=C0, scale=(2.0 ** e), bias=bias)
+    assert np.array_equal(got, want.astype(np.float64))
+    # the magnitude sum scales with |alpha * scale|
+    S_plain = np.abs(A)[:, :, None] * np.abs(B)[None, :, :]
+    assert np.array_equal(S, 2.0 * (2.0 ** e)[None, :] * S_plain.sum(axis=1))
+    # N x K weight layout gives the same result
+    got_nk, _ = oracle.gemm_ex(A, B.T.copy(), alpha=2.0, beta=-3.0, C0=C0, scale=(2.0 ** e), bias=bias, b_nk=True)
+    assert np.array_equal(got_nk, got)
+
+
+def test_extended_epilogue_order_and_special_cases():
+    A = np.array([[1.0, 2.0]]); B = np.array([[1.0], [1.0]])          # A.B = 3
+    C0 = np.array([[10.0]])
+    # relu comes last: 3 * 1 + (-5) + 1 * 10 = 8 > 0 although 3 - 5 < 0
+    c, _ = oracle.gemm_ex(A, B, beta=1.0, C0=C0, bias=[-5.0], relu=True)
+    assert c[0, 0] == 8.0
+    # scale multiplies the product, not the bias: 3 * 4 + 1 = 13
+    c, _ = oracle.gemm_ex(A, B, scale=[4.0], bias=[1.0])
+    assert c[0, 0] == 13.0
+    # beta only (zero product): beta * C0 + bias
+    c, _ = oracle.gemm_ex(np.zeros((1, 2)), B, beta=0.5, C0=C0, bias=[1.0])
+    assert c[0, 0] == 6.0
+    # defaults reduce to the plain product with bias and ReLU
+    rng = np.random.default_rng(3)
+    A2 = rng.standard_normal((5, 7)); B2 = rng.standard_normal((7, 4)); b = rng.standard_normal(4)
+    c1, _ = oracle.gemm_ex(A2, B2, bias=b, relu=True)
+    assert np.array_equal(c1, oracle.gemm(A2, B2, bias=b, relu=True))
