@@ -128,10 +128,22 @@ bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c) {
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 bool in_is_bf16(int dtype) { return dtype == DT_BF16_F32 || dtype == DT_BF16_BF16; }
-int out_bytes(int dtype) { return (dtype == DT_BF16_F32 || dtype == DT_F16_F32) ? 4 : 2; }
+int in_bytes(int dtype) { return dtype_is_fp8(dtype) ? 1 : 2; }
+int out_bytes(int dtype) {
+    return (dtype == DT_BF16_F32 || dtype == DT_F16_F32 || dtype == DT_E4M3_F32 || dtype == DT_E5M2_F32) ? 4 : 2;
+}
+CUtensorMapDataType in_map_type(int dtype) {
+    if (dtype_is_fp8(dtype)) return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes, read by the MMA as e4m3 / e5m2
+    return in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+CUtensorMapDataType out_map_type(int dtype) {
+    if (out_bytes(dtype) == 4) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return dtype == DT_F16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
 
 uint32_t make_idesc(int dtype, bool b_mn_major, int mma_m, int mma_n) {
-    const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;   // 1 = bf16, 0 = fp16
+    // operand format: kind::f16 bf16 = 1 / fp16 = 0; kind::f8f6f4 e5m2 = 1 / e4m3 = 0
+    const uint32_t ab = (in_is_bf16(dtype) || dtype == DT_E5M2_F32 || dtype == DT_E5M2_BF16) ? 1u : 0u;
     return (1u << 4)                       // accumulator fp32
          | (ab << 7) | (ab << 10)          // A and B formats
          | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness (A is always K-major)
@@ -276,7 +288,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
                   int64_t ldb, const void* bias, const void* C, int64_t ldc, int epilogue, int dtype) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
-    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_F16_F16OUT) return GEMM_ERR_INVALID_ARG;
+    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_E5M2_BF16OUT) return GEMM_ERR_INVALID_ARG;
     if (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
@@ -309,7 +321,7 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     if (e != cudaSuccess) { delete p; return GEMM_ERR_CUDA; }
     if (prop.major * 10 + prop.minor < 100) { delete p; return GEMM_ERR_UNSUPPORTED; }
     p->sm_count = prop.multiProcessorCount;
-    for (int dt = 0; dt < 4; ++dt) {
+    for (int dt = 0; dt < 8; ++dt) {
         int n2 = 0, n1 = 0;
         int n4 = 0, unused = 0;
         e = tc_prepare(2, dt, &n2, &n4);
@@ -490,9 +502,12 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         return GEMM_OK;
     }
 
+    const bool fp8 = dtype_is_fp8(dtype);
+    // fp8: the paired / single-CTA kernel with both operands K-major (B stored N x K)
+    if (fp8 && (!b_nk || conv)) return GEMM_ERR_UNSUPPORTED;
     int kernel = p->forced_kernel;
-    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128 && !conv) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
-    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv)) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128 && !conv && !fp8) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || fp8)) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
         return GEMM_ERR_UNSUPPORTED;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
@@ -503,8 +518,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
     const int ob = out_bytes(dtype);
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
-    const bool a_ok = conv || (aligned16(A) && (lda * 2) % 16 == 0);
-    const bool b_ok = aligned16(B) && (ldb * 2) % 16 == 0;
+    const int es = in_bytes(dtype);                 // element size of A and B
+    const int kbk = 128 / es;                       // elements per 128-byte k-block row
+    const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
+    const bool b_ok = aligned16(B) && (ldb * es) % 16 == 0;
     // the skinny kernel stores C with plain stores: any pitch is fine
     const bool c_ok = skinny || (aligned16(C) && (ldc * ob) % 16 == 0);
     const void* A_use = A; int64_t lda_use = lda;
@@ -512,21 +529,21 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     void* C_use = C; int64_t ldc_use = ldc;
     if (!a_ok || !b_ok || !c_ok) {
         if (!p->packing) return GEMM_ERR_ALIGNMENT;
-        const int64_t lda_p = round_up(K, 8), ldb_p = round_up(b_cols, 8), ldc_p = round_up(N, 16 / ob);
-        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(M * lda_p * 2, 256);
-        const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * 2, 256);
+        const int64_t lda_p = round_up(K, 16 / es), ldb_p = round_up(b_cols, 16 / es), ldc_p = round_up(N, 16 / ob);
+        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(M * lda_p * es, 256);
+        const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * es, 256);
         const size_t c_bytes = c_ok ? 0 : (size_t)round_up(M * ldc_p * ob, 256);
         rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes);
         if (rc != GEMM_OK) return rc;
         char* ws = static_cast<char*>(p->workspace);
         if (!a_ok) {
-            e = launch_copy2d(A, lda, ws, lda_p, M, K, 2, stream);
+            e = launch_copy2d(A, lda, ws, lda_p, M, K, es, stream);
             if (e != cudaSuccess) return record(p, e);
             p->launches += 1;
             A_use = ws; lda_use = lda_p;
         }
         if (!b_ok) {
-            e = launch_copy2d(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, 2, stream);
+            e = launch_copy2d(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, es, stream);
             if (e != cudaSuccess) return record(p, e);
             p->launches += 1;
             B_use = ws + a_bytes; ldb_use = ldb_p;
@@ -534,7 +551,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
     }
 
-    const CUtensorMapDataType in_dt = in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType in_dt = in_map_type(dtype);
     if (skinny) {
         rc = run_skinny(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, b_nk, in_dt, stream);
         if (rc != GEMM_OK) return rc;
@@ -542,15 +559,14 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         p->last_stream = stream; p->have_stream = true;
         return GEMM_OK;
     }
-    const CUtensorMapDataType out_dt = (ob == 4) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                 : (in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const CUtensorMapDataType out_dt = out_map_type(dtype);
     CUtensorMap tmA, tmB, tmC;
     if (conv) {
         if (!make_im2col_map(&tmA, in_dt, *conv)) return GEMM_ERR_CUDA;
-    } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * 2, TC_BK, TC_BM)) {
+    } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * es, kbk, TC_BM)) {
         return GEMM_ERR_CUDA;
     }
-    bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * 2, TC_BK,
+    bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * es, kbk,
                                mc == 2 ? 64 : TC_BN / cg)
                     : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * 2, 64, TC_BK);
     if (!okb) return GEMM_ERR_CUDA;
@@ -562,7 +578,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     prm.M = (int32_t)M; prm.N = (int32_t)N; prm.K = (int32_t)K;
     prm.num_m_tiles = (int32_t)((M + TC_BM * cg * mc - 1) / (TC_BM * cg * mc));
     prm.num_n_tiles = (int32_t)((N + TC_BN - 1) / TC_BN);
-    prm.num_k_blocks = (int32_t)((K + TC_BK - 1) / TC_BK);
+    prm.num_k_blocks = (int32_t)((K + kbk - 1) / kbk);
     prm.group_m = p->group_m;
     prm.epi = epi;
     prm.ex = ex;
@@ -655,6 +671,7 @@ int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int6
     if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
     if (OH < 0 || OW < 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype_is_fp8(dtype)) return GEMM_ERR_UNSUPPORTED;
     const int64_t M = Nb * OH * OW, N = Cout, K = (int64_t)R * S * C;
     // the weights w[f][r][s][c] are the N x K operand
     int rc = gemm_validate(GEMM_B_NK, M, N, K, x, K, w, K, bias, y, ldy, epilogue, dtype);

@@ -7,8 +7,13 @@
 
 namespace gb300 {
 
-// Output/input type combinations, same numbering as gemm_dtype_t.
-enum Dtype : int { DT_BF16_F32 = 0, DT_BF16_BF16 = 1, DT_F16_F32 = 2, DT_F16_F16 = 3 };
+// Output/input type combinations, same numbering as gemm_dtype_t.  The fp8
+// inputs (A and B in one format) take bf16 bias and scale vectors.
+enum Dtype : int {
+    DT_BF16_F32 = 0, DT_BF16_BF16 = 1, DT_F16_F32 = 2, DT_F16_F16 = 3,
+    DT_E4M3_F32 = 4, DT_E4M3_BF16 = 5, DT_E5M2_F32 = 6, DT_E5M2_BF16 = 7
+};
+constexpr bool dtype_is_fp8(int dt) { return dt >= DT_E4M3_F32 && dt <= DT_E5M2_BF16; }
 
 // Epilogue on the fp32 accumulator, in this order: t = alpha * acc (EPI_ALPHA);
 // t *= scale[n] (EPI_SCALE); t += bias[n] (EPI_BIAS); t += beta * C_old[m][n]

@@ -142,6 +142,17 @@ cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bi
             fill_epilogue_kernel<__half, float><<<blocks, threads, 0, stream>>>(
                 M, N, (const __half*)bias, epi, ex.beta, (const float*)ex.c_old, ex.ldc_old, (float*)C, ldc);
             break;
+        case DT_E4M3_F32:
+        case DT_E5M2_F32:
+            fill_epilogue_kernel<__nv_bfloat16, float><<<blocks, threads, 0, stream>>>(
+                M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const float*)ex.c_old, ex.ldc_old, (float*)C, ldc);
+            break;
+        case DT_E4M3_BF16:
+        case DT_E5M2_BF16:
+            fill_epilogue_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, threads, 0, stream>>>(
+                M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const __nv_bfloat16*)ex.c_old, ex.ldc_old,
+                (__nv_bfloat16*)C, ldc);
+            break;
         case DT_F16_F16:
             fill_epilogue_kernel<__half, __half><<<blocks, threads, 0, stream>>>(
                 M, N, (const __half*)bias, epi, ex.beta, (const __half*)ex.c_old, ex.ldc_old, (__half*)C, ldc);
@@ -162,10 +173,13 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
                          ld_dst >= padded;
     const bool src_vec = ((reinterpret_cast<uintptr_t>(src) | (uintptr_t)(ld_src * elem_bytes)) & 15u) == 0 &&
                          ld_src >= padded;
-    if ((elem_bytes == 2 || elem_bytes == 4) && (dst_vec || src_vec)) {
+    if ((elem_bytes == 1 || elem_bytes == 2 || elem_bytes == 4) && (dst_vec || src_vec)) {
         int64_t blocks = (rows * (padded / V) + threads - 1) / threads;
         if (blocks > 152 * 32) blocks = 152 * 32;
-        if (elem_bytes == 2)
+        if (elem_bytes == 1)
+            copy2d_vec_kernel<uint8_t><<<(int)blocks, threads, 0, stream>>>(
+                (const uint8_t*)src, ld_src, (uint8_t*)dst, ld_dst, rows, cols, dst_vec ? 1 : 0);
+        else if (elem_bytes == 2)
             copy2d_vec_kernel<uint16_t><<<(int)blocks, threads, 0, stream>>>(
                 (const uint16_t*)src, ld_src, (uint16_t*)dst, ld_dst, rows, cols, dst_vec ? 1 : 0);
         else
@@ -177,7 +191,10 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
     if (bx > 64) bx = 64;
     int64_t by = rows < 65535 ? rows : 65535;
     dim3 grid((unsigned)bx, (unsigned)by, 1);
-    if (elem_bytes == 2)
+    if (elem_bytes == 1)
+        copy2d_kernel<uint8_t><<<grid, threads, 0, stream>>>((const uint8_t*)src, ld_src, (uint8_t*)dst,
+                                                             ld_dst, rows, cols);
+    else if (elem_bytes == 2)
         copy2d_kernel<uint16_t><<<grid, threads, 0, stream>>>((const uint16_t*)src, ld_src, (uint16_t*)dst,
                                                               ld_dst, rows, cols);
     else if (elem_bytes == 4)

@@ -229,7 +229,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint64_t adesc = p.w_mn_major ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
                                                         : smem_desc_sw128(sw + kk * 32, 16, 1024);
                     const uint64_t bdesc = smem_desc_sw128(sx + kk * 32, 16, 1024);
-                    tc_mma_f16<1>(tmem, adesc, bdesc, p.idesc, (it | kk) != 0 ? 1u : 0u);
+                    tc_mma<1>(tmem, adesc, bdesc, p.idesc, (it | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit_1(bar_empty(s));
             }

@@ -156,7 +156,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // columns, so their B tiles are identical: each pair fetches half of it and
 // multicasts it to both, halving the B reads out of L2.  A stage may then be
 // refilled only when both pairs' MMAs are done with it.
-template <int CG, int MC, typename InT, typename OutT>
+template <int CG, int MC, typename InT, typename OutT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -217,6 +217,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int num_tiles = p.num_m_tiles * p.num_n_tiles;
     const int num_items = p.num_full + 2 * (num_tiles - p.num_full);
     const int nkb = p.num_k_blocks;
+    constexpr int kBk = KIND ? 2 * TC_BK : TC_BK;   // elements per 128-byte k-block row
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -272,7 +273,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (!w.wait(bar_empty(s), ph ^ 1u)) { ok = false; break; }
                     const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
                     const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
-                    const int k0 = (rev ? nkb - 1 - kb : kb) * TC_BK;
+                    const int k0 = (rev ? nkb - 1 - kb : kb) * kBk;
                     if constexpr (CG == 2 && MC == 2) {
                         const uint32_t fb = mapa_shared(bar_full(s), lead);
                         if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
@@ -343,13 +344,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (!w.wait(bar_full(s), ph)) { ok = false; break; }
                     const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
                     const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
+                    // four MMAs per 128-byte k-block row: K = 16 bf16 / fp16 or
+                    // K = 32 fp8 elements, 32 bytes of every row each
 #pragma unroll
-                    for (int kk = 0; kk < TC_BK / kUmmaK; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(sa + kk * (kUmmaK * 2), 16, 1024);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
                         const uint64_t bdesc = p.b_mn_major
                             ? smem_desc_sw128(sb + kk * (kUmmaK * 128), 8192, 1024)
-                            : smem_desc_sw128(sb + kk * (kUmmaK * 2), 16, 1024);
-                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            : smem_desc_sw128(sb + kk * 32, 16, 1024);
+                        tc_mma<CG, KIND>(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     if constexpr (CG == 2) tc_commit_2(bar_empty(s), empty_mask); else tc_commit_1(bar_empty(s));
                 }
@@ -517,7 +520,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (CG == 2) cluster_sync_all();
 }
 
-template <int CG, int MC, typename InT, typename OutT>
+template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const TcParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -534,12 +537,12 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT>, tmA, tmB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT, KIND>, tmA, tmB, tmC, p);
 }
 
-template <int CG, int MC, typename InT, typename OutT>
+template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
 cudaError_t prepare_impl(int* max_units) {
-    auto fn = gemm_tc_kernel<CG, MC, InT, OutT>;
+    auto fn = gemm_tc_kernel<CG, MC, InT, OutT, KIND>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<CG>::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -568,6 +571,11 @@ cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
         case DT_BF16_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(tmA, tmB, tmC, p, grid, stream);
         case DT_F16_F32: return launch_impl<CG, MC, __half, float>(tmA, tmB, tmC, p, grid, stream);
         case DT_F16_F16: return launch_impl<CG, MC, __half, __half>(tmA, tmB, tmC, p, grid, stream);
+        // fp8 operands (the format is in the instruction descriptor); bf16 bias / scale
+        case DT_E4M3_F32:
+        case DT_E5M2_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 1>(tmA, tmB, tmC, p, grid, stream);
+        case DT_E4M3_BF16:
+        case DT_E5M2_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmB, tmC, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -579,6 +587,10 @@ cudaError_t prepare_dt(int dtype, int* max_units) {
         case DT_BF16_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(max_units);
         case DT_F16_F32: return prepare_impl<CG, MC, __half, float>(max_units);
         case DT_F16_F16: return prepare_impl<CG, MC, __half, __half>(max_units);
+        case DT_E4M3_F32:
+        case DT_E5M2_F32: return prepare_impl<CG, MC, __nv_bfloat16, float, 1>(max_units);
+        case DT_E4M3_BF16:
+        case DT_E5M2_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(max_units);
     }
     return cudaErrorInvalidValue;
 }

@@ -17,6 +17,8 @@ LIB_PATH = _PKG / "libgb300gemm.so"
 
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_BIAS_RELU = 0, 1, 2, 3
 BF16_F32OUT, BF16_BF16OUT, F16_F32OUT, F16_F16OUT = 0, 1, 2, 3
+E4M3_F32OUT, E4M3_BF16OUT, E5M2_F32OUT, E5M2_BF16OUT = 4, 5, 6, 7
+FP8_DTYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
 B_KN, B_NK, B_CONST, TC_MULTICAST = 0, 1, 2, 4
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
@@ -92,11 +94,18 @@ def _check(code: int, what: str):
 
 def dtype_code(in_dtype: torch.dtype, out_dtype: torch.dtype) -> int:
     table = {(torch.bfloat16, torch.float32): BF16_F32OUT, (torch.bfloat16, torch.bfloat16): BF16_BF16OUT,
-             (torch.float16, torch.float32): F16_F32OUT, (torch.float16, torch.float16): F16_F16OUT}
+             (torch.float16, torch.float32): F16_F32OUT, (torch.float16, torch.float16): F16_F16OUT,
+             (torch.float8_e4m3fn, torch.float32): E4M3_F32OUT, (torch.float8_e4m3fn, torch.bfloat16): E4M3_BF16OUT,
+             (torch.float8_e5m2, torch.float32): E5M2_F32OUT, (torch.float8_e5m2, torch.bfloat16): E5M2_BF16OUT}
     try:
         return table[(in_dtype, out_dtype)]
     except KeyError:
         raise ValueError(f"unsupported dtype pair {in_dtype} -> {out_dtype}") from None
+
+
+def vector_dtype(in_dtype: torch.dtype) -> torch.dtype:
+    """dtype of the bias and scale vectors for an input dtype (bf16 for fp8 inputs)."""
+    return torch.bfloat16 if in_dtype in FP8_DTYPES else in_dtype
 
 
 def _ld(t: torch.Tensor) -> int:
@@ -191,16 +200,16 @@ class Plan:
         N = B.shape[0] if self.b_nk else B.shape[1]
         if (B.shape[1] if self.b_nk else B.shape[0]) != K or tuple(C.shape) != (M, N):
             raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} C {tuple(C.shape)}")
-        if A.dtype != B.dtype or (bias is not None and bias.dtype != A.dtype):
-            raise ValueError("A, B and bias must share one input dtype")
+        if A.dtype != B.dtype or (bias is not None and bias.dtype != vector_dtype(A.dtype)):
+            raise ValueError("A and B must share one input dtype; bias takes that dtype (bf16 for fp8)")
         for t in (A, B, C) + ((bias,) if bias is not None else ()):
             if t.device.type != "cuda":
                 raise ValueError("operands must be CUDA tensors")
         if bias is not None and (bias.dim() != 1 or bias.shape[0] != N or bias.stride(0) != 1):
             raise ValueError("bias must be a contiguous vector of length N")
         if scale is not None and (scale.dim() != 1 or scale.shape[0] != N or scale.stride(0) != 1
-                                  or scale.dtype != A.dtype or scale.device.type != "cuda"):
-            raise ValueError("scale must be a contiguous CUDA vector of length N in the input dtype")
+                                  or scale.dtype != vector_dtype(A.dtype) or scale.device.type != "cuda"):
+            raise ValueError("scale must be a contiguous CUDA vector of length N in the bias dtype")
         if alpha != 1.0 or beta != 0.0 or scale is not None:
             ea = _epilogue_args(alpha, beta, scale, bias, relu)
             rc = lib().gemm_run_ex(self._h, M, N, K, A.data_ptr(), _ld(A), B.data_ptr(), _ld(B), C.data_ptr(), _ld(C),

@@ -58,12 +58,21 @@ typedef enum {
     GEMM_EPI_BIAS_RELU = 3   /* C = max(0, A.B + bias)  */
 } gemm_epilogue_t;
 
-/* Input type of A, B, bias and output type of C. */
+/* Input type of A, B (and bias, scale) and output type of C.  The fp8 types
+ * (OCP e4m3 / e5m2 bytes, both operands in one format; CMU 15-418 notes,
+ * section 2.7: fewer bytes per operand, fp32 accumulation) take bf16 bias and
+ * scale vectors, need B stored N x K (plan flag GEMM_B_NK: both operands
+ * K-major) and always run on the large-M kernels; per-tensor scale factors go
+ * in gemm_run_ex's alpha. */
 typedef enum {
     GEMM_BF16_F32OUT = 0,
     GEMM_BF16_BF16OUT = 1,
     GEMM_F16_F32OUT = 2,
-    GEMM_F16_F16OUT = 3
+    GEMM_F16_F16OUT = 3,
+    GEMM_E4M3_F32OUT = 4,
+    GEMM_E4M3_BF16OUT = 5,
+    GEMM_E5M2_F32OUT = 6,
+    GEMM_E5M2_BF16OUT = 7
 } gemm_dtype_t;
 
 /* Plan flags. */

@@ -72,12 +72,45 @@ def _load():
     return _lib
 
 
+def e4m3_to_f64(codes) -> np.ndarray:
+    """FP8 E4M3 bytes (the OCP "fn" variant: no infinities) to float64, from the
+    format: bit 7 sign, bits 6..3 exponent with bias 7, bits 2..0 mantissa;
+    exponent 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN (so the largest
+    finite value is 1.75 * 2^8 = 448)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    v = np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+    return sign * v
+
+
+def e5m2_to_f64(codes) -> np.ndarray:
+    """FP8 E5M2 bytes to float64, IEEE-754 style: bit 7 sign, bits 6..2 exponent
+    with bias 15, bits 1..0 mantissa; exponent 0 encodes subnormals m/4 * 2^-14;
+    exponent 31 is infinity (m = 0) or NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = (c & 3).astype(np.float64)
+    v = np.where(e == 0, m / 4.0 * 2.0 ** -14, (1.0 + m / 4.0) * np.exp2(e - 15.0))
+    v = np.where(e == 31, np.where((c & 3) == 0, np.inf, np.nan), v)
+    return sign * v
+
+
 def _f64(x) -> np.ndarray:
-    """Widen to a C-contiguous float64 numpy array (exact for bf16/fp16/fp32/int)."""
+    """Widen to a C-contiguous float64 numpy array (exact for bf16/fp16/fp32/int;
+    fp8 tensors are decoded from their bytes by e4m3_to_f64 / e5m2_to_f64)."""
     try:
         import torch
         if isinstance(x, torch.Tensor):
-            x = x.detach().to("cpu", torch.float64).numpy()
+            x = x.detach().cpu()
+            if x.dtype == torch.float8_e4m3fn:
+                return np.ascontiguousarray(e4m3_to_f64(x.view(torch.uint8).numpy()))
+            if x.dtype == torch.float8_e5m2:
+                return np.ascontiguousarray(e5m2_to_f64(x.view(torch.uint8).numpy()))
+            x = x.to(torch.float64).numpy()
     except ImportError:  # pragma: no cover
         pass
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))

@@ -358,3 +358,38 @@ def test_extended_epilogue_order_and_special_cases():
     A2 = rng.standard_normal((5, 7)); B2 = rng.standard_normal((7, 4)); b = rng.standard_normal(4)
     c1, _ = oracle.gemm_ex(A2, B2, bias=b, relu=True)
     assert np.array_equal(c1, oracle.gemm(A2, B2, bias=b, relu=True))
+
+
+def test_fp8_decoders_pinned():
+    # values fixed by the formats
+    e4 = oracle.e4m3_to_f64
+    assert e4([0x38])[0] == 1.0 and e4([0xB8])[0] == -1.0
+    assert e4([0x7E])[0] == 448.0                      # largest finite: 1.75 * 2^8
+    assert e4([0x01])[0] == 2.0 ** -9                  # smallest subnormal: 1/8 * 2^-6
+    assert e4([0x08])[0] == 2.0 ** -6                  # smallest normal
+    assert np.isnan(e4([0x7F])[0]) and np.isnan(e4([0xFF])[0])
+    assert e4([0x00])[0] == 0.0 and np.signbit(e4([0x80])[0])
+    e5 = oracle.e5m2_to_f64
+    assert e5([0x3C])[0] == 1.0 and e5([0x7B])[0] == 57344.0
+    assert e5([0x01])[0] == 2.0 ** -16 and e5([0x04])[0] == 2.0 ** -14
+    assert e5([0x7C])[0] == np.inf and e5([0xFC])[0] == -np.inf and np.isnan(e5([0x7D])[0])
+    # every code against torch's own float8 conversion (an independent implementation)
+    codes = torch.arange(256, dtype=torch.uint8)
+    for dt, dec in ((torch.float8_e4m3fn, e4), (torch.float8_e5m2, e5)):
+        ref = codes.view(dt).to(torch.float64).numpy()
+        got = dec(codes.numpy())
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_fp8_small_integers_exact_and_gemm_on_decoded_values():
+    # integers -4..4 are exact in both formats, so an fp8 GEMM of them is the
+    # integer GEMM (numpy int64)
+    rng = np.random.default_rng(8)
+    A = rng.integers(-4, 5, size=(6, 40)); B = rng.integers(-4, 5, size=(9, 40))
+    for dt in (torch.float8_e4m3fn, torch.float8_e5m2):
+        At = torch.from_numpy(A).to(dt); Bt = torch.from_numpy(B).to(dt)
+        assert np.array_equal(oracle._f64(At), A)
+        C = oracle.gemm(At, Bt, b_nk=True)
+        assert np.array_equal(C, (A @ B.T).astype(np.float64))
