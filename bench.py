@@ -50,6 +50,9 @@ WORKLOADS = {
     # the same convolution as an implicit GEMM: gemm_conv2d on the NHWC activations
     "conv_implicit_32x56x56x256_3x3": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
     "odd_3000x5000x2048": (3000, 5000, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
+    # fp8 operands (both K-major: B stored N x K), bf16 output
+    "square8192_e4m3": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
+    "square8192_e5m2": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
     "odd_4095": (4095, 4095, 4095, "kn", (False, False), "bf16", 1.0, 1.0),
     "odd_1000": (1000, 1000, 1000, "kn", (False, False), "bf16", 1.0, 1.0),
     # decode-like Linear layers: W stored out x in, bias, M tokens
@@ -172,10 +175,20 @@ class ClockSampler:
                 "samples": len(sms), "power_w_max": max(powers) if powers else None}
 
 
+def fp8_dtype(name):
+    import torch
+    return {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}.get(name.rsplit("_", 1)[-1])
+
+
 def make_inputs(name, device, seed=0):
     import torch
     from dnn_linear_layers_gb300.inputs import normal_bf16
     M, N, K, lay, (has_bias, relu), out, a_std, b_std = WORKLOADS[name]
+    f8 = fp8_dtype(name)
+    if f8 is not None:   # N(0,1) drawn as bf16, then rounded to the fp8 format
+        A = normal_bf16((M, K), 3 * seed, a_std).to(f8)
+        B = normal_bf16((N, K), 3 * seed + 1, b_std).to(f8)
+        return A, B, None
     if name.startswith("conv_implicit"):
         # x (NHWC 32x56x56x256, ReLU(N(0,1))) and w[f][r][s][c] as they are
         from dnn_linear_layers_gb300.inputs import conv_tensors
@@ -220,10 +233,12 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
     conv = name.startswith("conv_implicit")
+    f8 = fp8_dtype(name)
     if conv:   # activations, weights and output once each (no im2col matrix exists)
         nbytes_step = float(A.numel() * 2 + B.numel() * 2 + M * N * 2)
     else:
-        nbytes_step = R.gemm_bytes(M, N, K, 2, 2, 2, 2 if has_bias else 0)
+        es = 1 if f8 is not None else 2
+        nbytes_step = R.gemm_bytes(M, N, K, es, es, 2, 2 if has_bias else 0)
     # Workloads smaller than twice the L2 rotate through enough copies of their
     # operands that each step reads HBM, not the previous step's L2 lines.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -343,11 +358,14 @@ def run_ours(args):
 
     peaks, src = R.load_peaks()
     nbytes = nbytes_step
-    t_roof = R.roofline_time(flops, nbytes, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
-    tensor_bound = flops / (peaks["bf16_tflops"] * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9)
+    # an fp8 contraction takes the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    t_peak = peaks["bf16_tflops"] * (2.0 if f8 is not None else 1.0)
+    t_roof = R.roofline_time(flops, nbytes, t_peak * 1e12, peaks["hbm_gbs"] * 1e9)
+    tensor_bound = flops / (t_peak * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9)
     if tensor_bound:
-        achieved, peak, r_unit = flops / (kernel_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-        peak_src = "MEASURED_PEAKS.json bf16_tflops (burst)"
+        achieved, peak, r_unit = flops / (kernel_ms * 1e-3) / 1e12, t_peak, "TFLOP/s"
+        peak_src = ("MEASURED_PEAKS.json bf16_tflops (burst) x 2, the nominal fp8 / bf16 ratio" if f8 is not None
+                    else "MEASURED_PEAKS.json bf16_tflops (burst)")
     else:
         achieved, peak, r_unit = nbytes / (kernel_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_src = "MEASURED_PEAKS.json hbm_gbs"
@@ -358,8 +376,11 @@ def run_ours(args):
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": name.rsplit("_", 1)[-1] if f8 is not None else "bf16",
+            "data": ("synthetic: N(0,1) drawn as bf16 (torch CPU generator, fixed seeds), rounded to "
+                     f"{name.rsplit('_', 1)[-1]}, resident in HBM" if f8 is not None else
+                     "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM"),
             "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": lay,
                        "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none",
                        "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
@@ -377,8 +398,8 @@ def run_ours(args):
                          "algorithmic_bytes": nbytes, "flops_per_launch": flops,
                          "kernel_ms": round(kernel_ms, 5)},
             "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": int(A_p.numel() * 2 + B_p.numel() * 2),
-                    "d2h_bytes_per_step": int(C_p.numel() * 2), "steps": e2e_steps},
+                    "h2d_bytes_per_step": int(A_p.numel() * A_p.element_size() + B_p.numel() * B_p.element_size()),
+                    "d2h_bytes_per_step": int(C_p.numel() * C_p.element_size()), "steps": e2e_steps},
             "gpu_launches": int(launches),
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -409,7 +430,7 @@ def _oracle_rows_timer(name, A, B, bias):
             return time.perf_counter() - t, len(pos)
 
         return run_conv, 1
-    Af = A.double().numpy(); Bf = B.double().numpy()
+    Af = oracle._f64(A); Bf = oracle._f64(B)   # fp8 bytes decoded by the oracle's own decoders
     bf = bias.double().numpy() if bias is not None else None
     rng = np.random.default_rng(0)
 
