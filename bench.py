@@ -49,6 +49,8 @@ WORKLOADS = {
     "conv_im2col_100352x2304x256": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
     # the same convolution as an implicit GEMM: gemm_conv2d on the NHWC activations
     "conv_implicit_32x56x56x256_3x3": (100352, 256, 2304, "nk", (False, False), "bf16", 1.0, (2 / 2304) ** 0.5),
+    # ... with per-channel bias, ReLU and the 2 x 2 max-pool fused (gemm_conv2d_maxpool)
+    "conv_pool_32x56x56x256_3x3": (100352, 256, 2304, "nk", (True, True), "bf16", 1.0, (2 / 2304) ** 0.5),
     "odd_3000x5000x2048": (3000, 5000, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
     # fp8 operands (both K-major: B stored N x K), bf16 output
     "square8192_e4m3": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
@@ -189,11 +191,12 @@ def make_inputs(name, device, seed=0):
         A = normal_bf16((M, K), 3 * seed, a_std).to(f8)
         B = normal_bf16((N, K), 3 * seed + 1, b_std).to(f8)
         return A, B, None
-    if name.startswith("conv_implicit"):
+    if name.startswith(("conv_implicit", "conv_pool")):
         # x (NHWC 32x56x56x256, ReLU(N(0,1))) and w[f][r][s][c] as they are
         from dnn_linear_layers_gb300.inputs import conv_tensors
         x, w = conv_tensors(seed=seed)
-        return x, w, None
+        bias = normal_bf16((N,), 3 * seed + 2, 0.02) if has_bias else None
+        return x, w, bias
     if name.startswith("conv_im2col"):
         # activations ReLU(N(0,1)) NHWC 32x56x56x256, weights w[f][r][s][c]; the
         # im2col matrix is built on the GPU by the library (setup, untimed)
@@ -225,17 +228,19 @@ def run_ours(args):
     A_h, B_h, bias_h = make_inputs(name, dev, seed=0)
     A, B = A_h.to(dev), B_h.to(dev)
     bias = bias_h.to(dev) if bias_h is not None else None
-    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    pool = name.startswith("conv_pool")
+    # the pooled convolution writes a quarter of the output rows
+    C = torch.empty((M // 4 if pool else M, N), dtype=torch.bfloat16, device=dev)
     # Linear-layer weights are constant model parameters: say so to the plan
     plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"))
     if args.kernel != "auto":
         plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
-    conv = name.startswith("conv_implicit")
+    conv = name.startswith(("conv_implicit", "conv_pool"))
     f8 = fp8_dtype(name)
     if conv:   # activations, weights and output once each (no im2col matrix exists)
-        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + M * N * 2)
+        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2 + (N * 2 if has_bias else 0))
     else:
         es = 1 if f8 is not None else 2
         nbytes_step = R.gemm_bytes(M, N, K, es, es, 2, 2 if has_bias else 0)
@@ -247,7 +252,9 @@ def run_ours(args):
     counter = [0]
 
     def call(a, b, c):
-        if conv:
+        if pool:
+            plan.conv2d_maxpool(a, b, c, bias, relu, pad=1)
+        elif conv:
             plan.conv2d(a, b, c, bias, relu, pad=1)
         else:
             plan.run(a, b, c, bias, relu)      # on torch's current stream
@@ -330,7 +337,7 @@ def run_ours(args):
 
     # ---- end to end: pinned host inputs -> device -> gemm_run -> host result
     A_p = A_h.pin_memory(); B_p = B_h.pin_memory()
-    C_p = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    C_p = torch.empty(tuple(C.shape), dtype=torch.bfloat16).pin_memory()
     A_e = torch.empty_like(A); B_e = torch.empty_like(B); C_e = torch.empty_like(C)
 
     def e2e_step():
@@ -417,7 +424,7 @@ def _oracle_rows_timer(name, A, B, bias):
     import oracle
     M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
     threads = len(os.sched_getaffinity(0))
-    if name.startswith("conv_implicit"):
+    if name.startswith(("conv_implicit", "conv_pool")):
         # the direct seven-loop convolution at n seeded output positions (one thread)
         Nb, H, W, _ = A.shape
         rng = np.random.default_rng(0)

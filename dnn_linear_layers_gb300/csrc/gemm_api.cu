@@ -106,6 +106,9 @@ struct ConvA {
     const void* x;
     int64_t Nb, H, W, C;
     int R, S, pad;
+    bool pool = false;     // fused 2 x 2 max-pool: tiles of two output rows x 64 columns
+    void* pool_y = nullptr;
+    int64_t pool_ldy = 0;
 };
 
 // im2col tensor map over x (Nb x H x W x C): tiles of TC_BM consecutive output
@@ -119,7 +122,9 @@ bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c) {
     int lower[2] = {-c.pad, -c.pad};
     int upper[2] = {c.pad - (c.S - 1), c.pad - (c.R - 1)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode_im2col(m, dt, 4, const_cast<void*>(c.x), gdim, gstride, lower, upper, TC_BK, TC_BM, estr,
+    // pooled tiles take two boxes of 64 pixels (one per output row), others one of 128
+    const cuuint32_t pixels = c.pool ? 64 : TC_BM;
+    CUresult r = g_encode_im2col(m, dt, 4, const_cast<void*>(c.x), gdim, gstride, lower, upper, TC_BK, pixels, estr,
                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -599,6 +604,16 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         prm.conv_pad = conv->pad;
         prm.conv_out_w = (int32_t)(conv->W + 2 * conv->pad - conv->S + 1);
         prm.conv_out_hw = (int32_t)((conv->H + 2 * conv->pad - conv->R + 1) * prm.conv_out_w);
+        if (conv->pool) {
+            prm.conv_pool = 1u;
+            prm.conv_strips = (prm.conv_out_w + 63) / 64;
+            prm.pool_nb = (int32_t)conv->Nb;
+            prm.pool_ph = (int32_t)((conv->H + 2 * conv->pad - conv->R + 1) / 2);
+            prm.pool_pw = prm.conv_out_w / 2;
+            prm.pool_y = conv->pool_y;
+            prm.pool_ldy = conv->pool_ldy;
+            prm.pool_vec16 = (aligned16(conv->pool_y) && (conv->pool_ldy * ob) % 16 == 0) ? 1u : 0u;
+        }
     }
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
@@ -698,6 +713,49 @@ int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int6
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
     return run_impl(p, true, M, N, K, p->workspace, ldk, w, K, bias, y, ldy, epi, ex, dtype, stream, nullptr);
+}
+
+int gemm_conv2d_maxpool(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S,
+                        int pad, const void* x, const void* w, void* y, int64_t ldy,
+                        const gemm_epilogue_args_t* epi_args, int dtype, void* stream_v) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
+    if (OH < 0 || OW < 0 || (OH & 1) || (OW & 1)) return GEMM_ERR_INVALID_ARG;   // whole 2 x 2 windows
+    if (dtype_is_fp8(dtype)) return GEMM_ERR_UNSUPPORTED;
+    uint32_t epi = 0;
+    EpiArgs ex = plain_epilogue();
+    const void* bias = nullptr;
+    if (epi_args) {
+        if (epi_args->beta != 0.0f) return GEMM_ERR_INVALID_ARG;   // the pooled output is only written
+        int rc0 = extended_epilogue(epi_args, dtype, y, ldy, &epi, &ex);
+        if (rc0 != GEMM_OK) return rc0;
+        bias = epi_args->bias;
+    }
+    const int64_t PH = OH / 2, PW = OW / 2;
+    const int64_t rows = Nb * PH * PW, N = Cout, K = (int64_t)R * S * C;
+    int rc = gemm_validate(GEMM_B_NK, rows, N, K, x, K, w, K, bias, y, ldy, (int)(epi & 3u), dtype);
+    if (rc != GEMM_OK) return rc;
+    if (rows == 0 || N == 0) return GEMM_OK;
+    // the fused form needs the implicit-GEMM operand (channel blocks of 64, a
+    // square filter, aligned activations) and K > 0
+    // and the pooled rows are stored with 16-byte vectors (no pack workspace)
+    if (K == 0 || C % TC_BK != 0 || R != S || pad > 127 || (S - 1 - pad) > 128 || !aligned16(x) ||
+        !aligned16(y) || (ldy * out_bytes(dtype)) % 16 != 0 || g_encode_im2col == nullptr || Nb > INT32_MAX / 2)
+        return GEMM_ERR_UNSUPPORTED;
+    DeviceGuard g(p->device);
+    // virtual GEMM rows: one 128-row tile per (image, output-row pair, 64-column
+    // strip); columns past OW in the last strip are computed and dropped.  (Tiles
+    // of 8 or 16 columns x 16 or 8 rows, which hold every window inside one warp,
+    // measured 2.7x slower: one small im2col copy per row makes the loads the limit.)
+    const int64_t units = Nb * PH * ((OW + 63) / 64);
+    if (units > INT32_MAX / TC_BM) return GEMM_ERR_UNSUPPORTED;
+    ConvA cv{x, Nb, H, W, C, R, S, pad};
+    cv.pool = true;
+    cv.pool_y = y;
+    cv.pool_ldy = ldy;
+    return run_impl(p, true, units * TC_BM, N, K, nullptr, 0, w, K, bias, y, ldy, epi, ex, dtype,
+                    reinterpret_cast<cudaStream_t>(stream_v), &cv);
 }
 
 }  // extern "C"

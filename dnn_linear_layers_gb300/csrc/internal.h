@@ -80,6 +80,18 @@ struct TcParams {
     int32_t conv_pad;      // zero padding (rows and columns)
     int32_t conv_out_w;    // output width  (= W for stride 1, pad (S-1)/2)
     int32_t conv_out_hw;   // output pixels per image
+    // Fused 2 x 2 max-pool (conv_pool != 0): a CTA's 128 rows are output rows
+    // 2 ph and 2 ph + 1 of one image, 64 columns each (strip s of conv_strips);
+    // only the pooled values are written, to pool_y (pooled pixel (n, ph, pw)
+    // is row (n * pool_ph + ph) * pool_pw + pw, pitch pool_ldy).
+    uint32_t conv_pool;
+    int32_t conv_strips;   // ceil(out_w / 64)
+    int32_t pool_nb;       // images
+    int32_t pool_ph;       // out_h / 2
+    int32_t pool_pw;       // out_w / 2
+    void* pool_y;
+    int64_t pool_ldy;
+    uint32_t pool_vec16;   // pool_y and pool_ldy * element size are 16-byte aligned
 };
 
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the

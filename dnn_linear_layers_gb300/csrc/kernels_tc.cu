@@ -66,7 +66,11 @@ struct TcCfg {
     static constexpr int kBarDone = kBarTEmpty + 16;
     static constexpr int kTmemPtr = kBarDone + 8;
     static constexpr int kAbort = kTmemPtr + 4;
-    static_assert(kAbort + 4 <= kMiscBytes, "misc layout");
+    // max-pool hand-over between the lane quarters holding the two output rows
+    static constexpr int kBarXFull = (kAbort + 4 + 7) / 8 * 8;
+    static constexpr int kBarXEmpty = kBarXFull + 16;
+    static_assert(kBarXEmpty + 16 <= kMiscBytes, "misc layout");
+    static_assert(kEpiWarps * 2 * kCStage >= 2 * 16384, "pool hand-over needs 16 KB per warp pair");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -127,9 +131,16 @@ __device__ __forceinline__ void work_item(int item, const TcParams& p, int& tm, 
 template <typename OutT> struct OutTraits;
 template <> struct OutTraits<float> {
     static constexpr int kCols = 32;   // 128-byte row chunk
+    static __device__ __forceinline__ float cvt(float v) { return v; }
 };
-template <> struct OutTraits<__nv_bfloat16> { static constexpr int kCols = 64; };
-template <> struct OutTraits<__half> { static constexpr int kCols = 64; };
+template <> struct OutTraits<__nv_bfloat16> {
+    static constexpr int kCols = 64;
+    static __device__ __forceinline__ __nv_bfloat16 cvt(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct OutTraits<__half> {
+    static constexpr int kCols = 64;
+    static __device__ __forceinline__ __half cvt(float v) { return __float2half_rn(v); }
+};
 
 template <typename InT> __device__ __forceinline__ float to_f32(InT v);
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -149,6 +160,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // MC = number of CTA pairs in a cluster (1 or 2, CG = 2 only).  With MC = 2
@@ -182,6 +199,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto bar_tfull = [&](int a) { return misc + Cfg::kBarTFull + 8u * a; };
     auto bar_tempty = [&](int a) { return misc + Cfg::kBarTEmpty + 8u * a; };
     const uint32_t bar_done = misc + Cfg::kBarDone;
+    auto bar_xfull = [&](uint32_t i) { return misc + Cfg::kBarXFull + 8u * i; };
+    auto bar_xempty = [&](uint32_t i) { return misc + Cfg::kBarXEmpty + 8u * i; };
+
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Cfg::kOffMisc + Cfg::kAbort);
     uint32_t* tmem_ptr_smem = reinterpret_cast<uint32_t*>(base_ptr + Cfg::kOffMisc + Cfg::kTmemPtr);
 
@@ -195,6 +215,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(bar_tempty(a), kEpiWarps * CG);
         }
         mbar_init(bar_done, 1);
+        for (uint32_t i = 0; i < 2; ++i) {
+            mbar_init(bar_xfull(i), 1);
+            mbar_init(bar_xempty(i), 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmA);
@@ -239,7 +263,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int nb = n0 + (int)crank * (nw / CG);
                 // implicit GEMM: base pixel (top-left of the filter window) of row m0
                 int px_n = 0, px_h = 0, px_w = 0;
-                if (p.conv) {
+                if (p.conv && p.conv_pool) {
+                    // CTA tile u: image px_n, output rows 2 ph and 2 ph + 1, columns 64 s ..
+                    const int u = m0 / TC_BM;
+                    const int per_img = p.pool_ph * p.conv_strips;
+                    px_n = u / per_img;
+                    const int rem = u - px_n * per_img;
+                    const int ph = rem / p.conv_strips;
+                    px_h = 2 * ph - p.conv_pad;
+                    px_w = (rem - ph * p.conv_strips) * 64 - p.conv_pad;
+                } else if (p.conv) {
                     px_n = m0 / p.conv_out_hw;
                     const int rem = m0 - px_n * p.conv_out_hw;
                     px_h = rem / p.conv_out_w - p.conv_pad;
@@ -254,8 +287,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const int c0 = (kbi - tap * p.conv_cb) * TC_BK;
                         const int r = tap / p.conv_s;
                         const uint16_t off_w = (uint16_t)(tap - r * p.conv_s), off_h = (uint16_t)r;
-                        if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
-                        else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                        if (p.conv_pool) {
+                            // two boxes of 64 pixels, rows 2 ph and 2 ph + 1, 8 KB apart
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t d = dst + (uint32_t)h * 8192u;
+                                if (pair_bar)
+                                    tma_load_im2col_pair(d, &tmA, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
+                                else
+                                    tma_load_im2col(d, &tmA, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
+                            }
+                        } else {
+                            if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                            else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                        }
                     } else {
                         if (pair_bar) tma_load_2d_pair(dst, &tmA, bar, k0, m0, pol_a);
                         else tma_load_2d(dst, &tmA, bar, k0, m0, pol_a);
@@ -395,6 +439,125 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((32u * q) << 16) + a * TC_BN;
+            if (p.conv_pool) {
+                // Lanes 0..63 of the accumulator hold output row 2 ph (pixel 64 s + lane
+                // of the strip), lanes 64..127 row 2 ph + 1.  Every warp applies the
+                // epilogue and takes the max with its horizontal neighbour (lane ^ 1);
+                // the row 2 ph + 1 quarters (q = 2, 3) then leave their even lanes' values
+                // for the whole tile in shared memory (16 KB each, one hand-over per
+                // tile), and the row 2 ph quarters (q = 0, 1) take the vertical max and
+                // store the pooled pixels from their even lanes.
+                const int u = m0 / TC_BM;
+                const int per_img = p.pool_ph * p.conv_strips;
+                const int n_img = u / per_img;
+                const int rem = u - n_img * per_img;
+                const int ph = rem / p.conv_strips;
+                const int s = rem - ph * p.conv_strips;
+                const int pw = (64 * s + 32 * (int)(q & 1u) + (int)lane) >> 1;
+                const bool writer = (q >> 1) != 0;
+                const bool even = (lane & 1u) == 0;
+                // 16 rows (even lanes) x 128 B per 32-column chunk, 16 KB per tile
+                const uint32_t xrow = base + Cfg::kOffC + (q & 1u) * 4 * Cfg::kCStage + (lane >> 1) * 128u;
+                const uint32_t xf = bar_xfull(q & 1u), xe = bar_xempty(q & 1u);
+                const uint32_t xph = tcount & 1u;
+                const bool out_ok = !writer && even && n_img < p.pool_nb && pw < p.pool_pw;
+                OutT* const yrow = reinterpret_cast<OutT*>(p.pool_y) +
+                                   ((int64_t)(n_img * p.pool_ph + ph) * p.pool_pw + pw) * p.pool_ldy;
+                const InT* sc = reinterpret_cast<const InT*>(p.ex.scale);
+                const int chunks = nw / 32;
+                bool ok = true;
+                if (writer) {   // the previous tile's values must have been read
+                    ok = w.wait(xe, xph ^ 1u);
+                    ok = __all_sync(0xffffffffu, ok);
+                } else {        // this tile's values must have been written
+                    ok = w.wait(xf, xph);
+                    ok = __all_sync(0xffffffffu, ok);
+                }
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                    tmem_ld_wait();
+                    if (c == chunks - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+                    }
+                    const int cb = n0 + c * 32;
+                    float sv[32], bv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) { sv[j] = 1.0f; bv[j] = 0.0f; }
+                    if (cb + 32 <= p.N && (!has_bias || p.bias_vec16) && (!(p.epi & EPI_SCALE) || p.ex.scale_vec16)) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (p.epi & EPI_SCALE) {
+                                const uint4 us = __ldg(reinterpret_cast<const uint4*>(sc + cb) + j);
+                                const InT* es = reinterpret_cast<const InT*>(&us);
+#pragma unroll
+                                for (int t = 0; t < 8; ++t) sv[8 * j + t] = to_f32<InT>(es[t]);
+                            }
+                            if (has_bias) {
+                                const uint4 ub = __ldg(reinterpret_cast<const uint4*>(bias + cb) + j);
+                                const InT* eb = reinterpret_cast<const InT*>(&ub);
+#pragma unroll
+                                for (int t = 0; t < 8; ++t) bv[8 * j + t] = to_f32<InT>(eb[t]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (cb + j < p.N) {
+                                if (p.epi & EPI_SCALE) sv[j] = to_f32<InT>(sc[cb + j]);
+                                if (has_bias) bv[j] = to_f32<InT>(bias[cb + j]);
+                            }
+                        }
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        float t = __uint_as_float(r[j]);
+                        if (p.epi & EPI_ALPHA) t *= p.ex.alpha;
+                        t = t * sv[j] + bv[j];
+                        if (relu) t = fmaxf(t, 0.0f);
+                        v[j] = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
+                    }
+                    const uint32_t xa = xrow + (uint32_t)c * 2048u;   // 16 rows x 128 B per chunk
+                    if (writer) {
+                        if (ok && even) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                st_shared_v4(xa + ((j ^ ((lane >> 1) & 7u)) << 4), __float_as_uint(v[4 * j]),
+                                             __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                                             __float_as_uint(v[4 * j + 3]));
+                        }
+                    } else if (ok && out_ok) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 o = ld_shared_v4f(xa + ((j ^ ((lane >> 1) & 7u)) << 4));
+                            v[4 * j] = fmaxf(v[4 * j], o.x); v[4 * j + 1] = fmaxf(v[4 * j + 1], o.y);
+                            v[4 * j + 2] = fmaxf(v[4 * j + 2], o.z); v[4 * j + 3] = fmaxf(v[4 * j + 3], o.w);
+                        }
+                        OutT* dst = yrow + cb;
+                        if (p.pool_vec16 && cb + 32 <= p.N) {
+                            constexpr int kPer = 16 / (int)sizeof(OutT);
+#pragma unroll
+                            for (int j = 0; j < 32 / kPer; ++j) {
+                                OutT o[kPer];
+#pragma unroll
+                                for (int t = 0; t < kPer; ++t) o[t] = OutTraits<OutT>::cvt(v[kPer * j + t]);
+                                *reinterpret_cast<uint4*>(dst + kPer * j) = *reinterpret_cast<const uint4*>(o);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (cb + j < p.N) dst[j] = OutTraits<OutT>::cvt(v[j]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (ok && lane == 0) mbar_arrive_local(writer ? xf : xe);
+                if (!ok) break;
+                continue;
+            }
             for (int c = 0; c < kChunks; ++c) {
                 float v[kCols];
 #pragma unroll

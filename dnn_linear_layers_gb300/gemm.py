@@ -56,6 +56,8 @@ SIGNATURES = {
     "gemm_conv2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _epi_p, _int,
                            _vp]),
     "gemm_run_ex": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _epi_p, _int, _vp]),
+    "gemm_conv2d_maxpool": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _epi_p,
+                                   _int, _vp]),
 }
 
 _lib = None
@@ -250,6 +252,25 @@ class Plan:
                                y.data_ptr(), _ld(y), ctypes.byref(ea), dtype_code(x.dtype, y.dtype),
                                _stream_handle(stream))
         _check(rc, "gemm_conv2d")
+        return y
+
+    def conv2d_maxpool(self, x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: torch.Tensor | None = None,
+                       relu: bool = False, pad: int = 0, stream=None, alpha: float = 1.0,
+                       scale: torch.Tensor | None = None):
+        """Stride-1 convolution, epilogue (alpha, scale, bias, ReLU) and 2 x 2
+        max-pool in one kernel; y is ((Nb*OH/2*OW/2) x Cout)."""
+        if x.dim() != 4 or w.dim() != 4 or not x.is_contiguous() or not w.is_contiguous():
+            raise ValueError("x (NHWC) and w (Cout x R x S x C) must be contiguous 4-D tensors")
+        Nb, H, W, C = x.shape
+        Cout, R, S, Cw = w.shape
+        OH, OW = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+        if Cw != C or tuple(y.shape) != (Nb * (OH // 2) * (OW // 2), Cout):
+            raise ValueError(f"shape mismatch: x {tuple(x.shape)} w {tuple(w.shape)} y {tuple(y.shape)}")
+        ea = _epilogue_args(alpha, 0.0, scale, bias, relu)
+        rc = lib().gemm_conv2d_maxpool(self._h, Nb, H, W, C, Cout, R, S, pad, x.data_ptr(), w.data_ptr(),
+                                       y.data_ptr(), _ld(y), ctypes.byref(ea), dtype_code(x.dtype, y.dtype),
+                                       _stream_handle(stream))
+        _check(rc, "gemm_conv2d_maxpool")
         return y
 
 

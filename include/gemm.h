@@ -191,6 +191,23 @@ int gemm_conv2d(gemm_plan_t plan, int64_t Nb, int64_t H, int64_t W, int64_t C, i
                 const void* x, const void* w, void* y, int64_t ldy, const gemm_epilogue_args_t* epi, int dtype,
                 void* stream);
 
+/* Convolution fused with its epilogue and a 2 x 2 max-pool (stride 2), the
+ * single-pass conv + scale/bias + ReLU + max-pool of CMU 15-418 "DNNs and ML
+ * accelerators" notes, section 3.1 (example one):
+ *     y[(n*PH + ph)*PW + pw][f] = max over dy, dx in {0, 1} of
+ *         epilogue( conv(x, w)[n][2 ph + dy][2 pw + dx][f] )
+ * with the convolution, OH and OW of gemm_conv2d, PH = OH / 2, PW = OW / 2,
+ * and the epilogue of gemm_epilogue_args_t (alpha, scale, bias, relu; beta must
+ * be 0; epi may be NULL).  OH and OW must be even (GEMM_ERR_INVALID_ARG).
+ * Only the pooled values are written: y is (Nb*PH*PW) x Cout, row pitch ldy.
+ * Runs on the large-M kernel with im2col loads, whose tiles are two output rows
+ * x 64 columns, so every pooling window lies in one accumulator; it needs C a
+ * multiple of 64, R == S, 16-bit inputs, x and y 16-byte aligned and
+ * ldy x element size a multiple of 16 (else GEMM_ERR_UNSUPPORTED). */
+int gemm_conv2d_maxpool(gemm_plan_t plan, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S,
+                        int pad, const void* x, const void* w, void* y, int64_t ldy,
+                        const gemm_epilogue_args_t* epi, int dtype, void* stream);
+
 /* --- controls and introspection (benchmarks and tests) ------------------ */
 
 /* Force a kernel (GEMM_KERNEL_*); GEMM_KERNEL_AUTO restores the dispatcher. */

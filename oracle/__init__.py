@@ -398,5 +398,18 @@ def conv2d_at(x, w, pad: int, positions):
     return out
 
 
+def conv2d_maxpool_at(x, w, pad: int, pooled_positions, alpha=1.0, scale=None, bias=None, relu=False):
+    """Convolution, epilogue and 2 x 2 max-pool at pooled positions (n, ph, pw),
+    the single-pass fused example of the CMU 15-418 notes, section 3.1: the
+    maximum over dy, dx in {0, 1} of epilogue_ex(conv(x, w)[n, 2 ph + dy, 2 pw + dx])."""
+    pos = np.asarray(pooled_positions, dtype=np.int64).reshape(-1, 3)
+    outs = []
+    for dy in (0, 1):
+        for dx in (0, 1):
+            full = [(int(n), int(2 * ph + dy), int(2 * pw + dx)) for n, ph, pw in pos]
+            outs.append(epilogue_ex(conv2d_at(x, w, pad, full), alpha=alpha, scale=scale, bias=bias, relu=relu))
+    return np.maximum(np.maximum(outs[0], outs[1]), np.maximum(outs[2], outs[3]))
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -180,3 +180,57 @@ def test_full_conv_config_implicit_sampled(plan):
     plan.run(cols, wd.reshape(Cout, -1), y_exp)
     assert plan.status() == 0
     assert torch.equal(y.view(torch.int16), y_exp.view(torch.int16))
+
+
+# ---- convolution + epilogue + 2 x 2 max-pool in one kernel (gemm_conv2d_maxpool)
+
+POOL_SHAPES = [  # Nb, H, W, C, Cout, R(=S), pad
+    (2, 8, 8, 64, 32, 3, 1),        # a 64-column strip wider than the row
+    (1, 64, 64, 64, 64, 3, 1),      # 64 x 64 images: one strip per output-row pair
+    (3, 10, 72, 64, 96, 3, 1),      # second strip holds 8 columns
+    (2, 12, 12, 128, 200, 1, 0),    # 1 x 1 filter, ragged N
+    (1, 6, 130, 64, 48, 5, 2),      # 3 strips, odd number of CTA tiles
+]
+
+
+@pytest.mark.parametrize("shape", POOL_SHAPES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_conv_maxpool_exact_every_output(shape, out):
+    Nb, H, W, C, Cout, R, pad = shape
+    x = int_bf16((Nb, H, W, C), 61 + sum(shape))
+    w = int_bf16((Cout, R, R, C), 62 + sum(shape))
+    g = torch.Generator().manual_seed(sum(shape))
+    scale = (2.0 ** torch.randint(0, 3, (Cout,), generator=g)).to(torch.bfloat16)
+    bias = torch.randint(-20, 21, (Cout,), generator=g).to(torch.bfloat16)
+    OH, OW = conv_out_hw(H, W, R, pad)
+    PH, PW = OH // 2, OW // 2
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    y = torch.full((Nb * PH * PW, Cout), float("nan"), dtype=od, device="cuda")
+    with G.Plan(0, "nk") as p:
+        p.conv2d_maxpool(x.cuda(), w.cuda(), y, bias.cuda(), True, pad=pad, scale=scale.cuda())
+        assert p.status() == 0
+        assert p.last_kernel == G.KERNEL_TC_PAIR
+        assert p.workspace_bytes == 0
+    pos = [(n, ph, pw) for n in range(Nb) for ph in range(PH) for pw in range(PW)]
+    ref = oracle.conv2d_maxpool_at(x, w, pad, pos, scale=scale, bias=bias, relu=True)
+    want = oracle.bf16_round(ref) if out == "bf16" else ref
+    got = y.double().cpu().numpy()
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[0]}: {got[tuple(bad[0])]} vs {want[tuple(bad[0])]}"
+
+
+def test_conv_maxpool_refusals():
+    x = torch.zeros(1, 9, 9, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(32, 3, 3, 64, dtype=torch.bfloat16, device="cuda")
+    with G.Plan(0, "nk") as p:
+        # odd output size: incomplete pooling windows
+        y = torch.empty(16, 32, device="cuda")
+        with pytest.raises(G.GemmError) as e:
+            p.conv2d_maxpool(x, w, y, pad=1)
+        assert e.value.code == G.ERR_INVALID_ARG
+        # 16 channels: not the implicit-GEMM operand
+        x16 = torch.zeros(1, 8, 8, 16, dtype=torch.bfloat16, device="cuda")
+        w16 = torch.zeros(32, 3, 3, 16, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(G.GemmError) as e:
+            p.conv2d_maxpool(x16, w16, torch.empty(16, 32, device="cuda"), pad=1)
+        assert e.value.code == G.ERR_UNSUPPORTED

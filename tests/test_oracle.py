@@ -393,3 +393,22 @@ def test_fp8_small_integers_exact_and_gemm_on_decoded_values():
         assert np.array_equal(oracle._f64(At), A)
         C = oracle.gemm(At, Bt, b_nk=True)
         assert np.array_equal(C, (A @ B.T).astype(np.float64))
+
+
+def test_conv_maxpool_closed_forms():
+    # 1 x 1 identity filter: the convolution is x itself, so the fused result is
+    # the 2 x 2 block maximum of x (numpy reshape / max), and with ReLU of it
+    rng = np.random.default_rng(21)
+    Nb, H, W, C = 2, 6, 8, 5
+    x = rng.integers(-9, 10, size=(Nb, H, W, C)).astype(np.float64)
+    w = np.eye(C).reshape(C, 1, 1, C)
+    pos = [(n, ph, pw) for n in range(Nb) for ph in range(H // 2) for pw in range(W // 2)]
+    got = oracle.conv2d_maxpool_at(x, w, 0, pos)
+    want = x.reshape(Nb, H // 2, 2, W // 2, 2, C).max(axis=(2, 4)).reshape(-1, C)
+    assert np.array_equal(got, want)
+    got_relu = oracle.conv2d_maxpool_at(x, w, 0, pos, relu=True)
+    assert np.array_equal(got_relu, np.maximum(want, 0.0))
+    # a negative per-channel scale flips which element wins (max of -x is -min x)
+    s = -np.ones(C)
+    got_neg = oracle.conv2d_maxpool_at(x, w, 0, pos, scale=s)
+    assert np.array_equal(got_neg, -x.reshape(Nb, H // 2, 2, W // 2, 2, C).min(axis=(2, 4)).reshape(-1, C))
