@@ -113,17 +113,27 @@ struct ConvA {
 
 // im2col tensor map over x (Nb x H x W x C): tiles of TC_BM consecutive output
 // pixels x TC_BK channels, 128-byte swizzle.  The bounding box holds the
-// top-left pixels of all filter windows: from -pad to (dim - 1) + pad -
-// (filter - 1) in H and in W (equal offsets: the filter is square).
-bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c) {
+// top-left pixels of the filter windows walked: from -pad to (dim - 1) + pad -
+// (filter - 1) in W and H.  For the fused max-pool, `rows` 1 / 2 gives the
+// maps of the top / bottom rows of the row pairs: 64 pixels per box, two rows
+// per step in H, the bottom map's box one row lower.  Corner arrays run W, H.
+bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c, int rows = 0) {
     if (!g_encode_im2col) return false;
     cuuint64_t gdim[4] = {(cuuint64_t)c.C, (cuuint64_t)c.W, (cuuint64_t)c.H, (cuuint64_t)c.Nb};
     cuuint64_t gstride[3] = {(cuuint64_t)c.C * 2, (cuuint64_t)(c.W * c.C * 2), (cuuint64_t)(c.H * c.W * c.C * 2)};
+    const int oh_last = (int)(c.H + 2 * c.pad - c.R);                // last output row
     int lower[2] = {-c.pad, -c.pad};
     int upper[2] = {c.pad - (c.S - 1), c.pad - (c.R - 1)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    // pooled tiles take two boxes of 64 pixels (one per output row), others one of 128
-    const cuuint32_t pixels = c.pool ? 64 : TC_BM;
+    if (rows == 1) {          // top rows 0, 2, .., OH - 2
+        upper[1] = (oh_last - 1 - c.pad) - (int)(c.H - 1);
+        estr[2] = 2;
+    } else if (rows == 2) {   // bottom rows 1, 3, .., OH - 1
+        lower[1] = 1 - c.pad;
+        upper[1] = (oh_last - c.pad) - (int)(c.H - 1);
+        estr[2] = 2;
+    }
+    const cuuint32_t pixels = rows ? 64 : TC_BM;
     CUresult r = g_encode_im2col(m, dt, 4, const_cast<void*>(c.x), gdim, gstride, lower, upper, TC_BK, pixels, estr,
                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -565,8 +575,11 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         return GEMM_OK;
     }
     const CUtensorMapDataType out_dt = out_map_type(dtype);
-    CUtensorMap tmA, tmB, tmC;
-    if (conv) {
+    CUtensorMap tmA, tmA2, tmB, tmC;
+    if (conv && conv->pool) {
+        if (!make_im2col_map(&tmA, in_dt, *conv, 1) || !make_im2col_map(&tmA2, in_dt, *conv, 2))
+            return GEMM_ERR_CUDA;
+    } else if (conv) {
         if (!make_im2col_map(&tmA, in_dt, *conv)) return GEMM_ERR_CUDA;
     } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * es, kbk, TC_BM)) {
         return GEMM_ERR_CUDA;
@@ -606,10 +619,8 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         prm.conv_out_hw = (int32_t)((conv->H + 2 * conv->pad - conv->R + 1) * prm.conv_out_w);
         if (conv->pool) {
             prm.conv_pool = 1u;
-            prm.conv_strips = (prm.conv_out_w + 63) / 64;
-            prm.pool_nb = (int32_t)conv->Nb;
             prm.pool_ph = (int32_t)((conv->H + 2 * conv->pad - conv->R + 1) / 2);
-            prm.pool_pw = prm.conv_out_w / 2;
+            prm.pool_rows = (int32_t)(conv->Nb * prm.pool_ph * (prm.conv_out_w / 2));
             prm.pool_y = conv->pool_y;
             prm.pool_ldy = conv->pool_ldy;
             prm.pool_vec16 = (aligned16(conv->pool_y) && (conv->pool_ldy * ob) % 16 == 0) ? 1u : 0u;
@@ -626,7 +637,8 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         std::fprintf(stderr, "[gemm] tc cta_group=%d mc=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
                      cg, mc, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
                      (long long)(units * cg * mc), A_use != A, B_use != B, C_use != C);
-    e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg * mc), stream);
+    e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg * mc), stream,
+                       (conv && conv->pool) ? &tmA2 : nullptr);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
 
@@ -744,12 +756,12 @@ int gemm_conv2d_maxpool(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t
         !aligned16(y) || (ldy * out_bytes(dtype)) % 16 != 0 || g_encode_im2col == nullptr || Nb > INT32_MAX / 2)
         return GEMM_ERR_UNSUPPORTED;
     DeviceGuard g(p->device);
-    // virtual GEMM rows: one 128-row tile per (image, output-row pair, 64-column
-    // strip); columns past OW in the last strip are computed and dropped.  (Tiles
-    // of 8 or 16 columns x 16 or 8 rows, which hold every window inside one warp,
-    // measured 2.7x slower: one small im2col copy per row makes the loads the limit.)
-    const int64_t units = Nb * PH * ((OW + 63) / 64);
-    if (units > INT32_MAX / TC_BM) return GEMM_ERR_UNSUPPORTED;
+    // virtual GEMM rows: one 128-row tile per 64 positions of the sequence
+    // (image, row pair, column), top pixels then bottom pixels.  (Tiles of 8 or
+    // 16 columns x 16 or 8 rows, which hold every window inside one warp, measured
+    // 2.7x slower: one small im2col copy per row makes the loads the limit.)
+    const int64_t units = (Nb * PH * OW + 63) / 64;
+    if (units > INT32_MAX / TC_BM || Nb * PH * OW > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     ConvA cv{x, Nb, H, W, C, R, S, pad};
     cv.pool = true;
     cv.pool_y = y;

@@ -80,15 +80,15 @@ struct TcParams {
     int32_t conv_pad;      // zero padding (rows and columns)
     int32_t conv_out_w;    // output width  (= W for stride 1, pad (S-1)/2)
     int32_t conv_out_hw;   // output pixels per image
-    // Fused 2 x 2 max-pool (conv_pool != 0): a CTA's 128 rows are output rows
-    // 2 ph and 2 ph + 1 of one image, 64 columns each (strip s of conv_strips);
-    // only the pooled values are written, to pool_y (pooled pixel (n, ph, pw)
-    // is row (n * pool_ph + ph) * pool_pw + pw, pitch pool_ldy).
+    // Fused 2 x 2 max-pool (conv_pool != 0): the output pixels are taken as
+    // positions k = (n * pool_ph + ph) * out_w + ow of row pairs (2 ph, 2 ph + 1);
+    // CTA tile u holds positions 64 u .. 64 u + 63, rows 0..63 the top pixels
+    // (A through the first im2col map, which steps two rows) and rows 64..127
+    // the bottom pixels (the second map, one row lower).  Only pooled values are
+    // written: position k to row k / 2 of pool_y (pitch pool_ldy).
     uint32_t conv_pool;
-    int32_t conv_strips;   // ceil(out_w / 64)
-    int32_t pool_nb;       // images
     int32_t pool_ph;       // out_h / 2
-    int32_t pool_pw;       // out_w / 2
+    int32_t pool_rows;     // pooled output rows: images * out_h / 2 * out_w / 2
     void* pool_y;
     int64_t pool_ldy;
     uint32_t pool_vec16;   // pool_y and pool_ldy * element size are 16-byte aligned
@@ -97,7 +97,8 @@ struct TcParams {
 // Launch the persistent tcgen05 GEMM.  cta_group is 1 or 2; grid is the
 // number of CTAs (a multiple of cta_group).  Returns the launch's cudaError_t.
 cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream);
+                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream,
+                           const CUtensorMap* tmA2 = nullptr);   // second A map (fused max-pool only)
 
 // Dynamic shared memory the tensor-core kernel needs for a cta_group.
 int tc_smem_bytes(int cta_group);

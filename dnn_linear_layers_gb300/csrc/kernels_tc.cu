@@ -175,7 +175,8 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
 // refilled only when both pairs' MMAs are done with it.
 template <int CG, int MC, typename InT, typename OutT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+               const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     using Cfg = TcCfg<CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -222,6 +223,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmA);
+        if (p.conv_pool) tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmC);
     }
@@ -264,14 +266,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // implicit GEMM: base pixel (top-left of the filter window) of row m0
                 int px_n = 0, px_h = 0, px_w = 0;
                 if (p.conv && p.conv_pool) {
-                    // CTA tile u: image px_n, output rows 2 ph and 2 ph + 1, columns 64 s ..
-                    const int u = m0 / TC_BM;
-                    const int per_img = p.pool_ph * p.conv_strips;
-                    px_n = u / per_img;
-                    const int rem = u - px_n * per_img;
-                    const int ph = rem / p.conv_strips;
+                    // CTA tile u: positions 64 u .. 64 u + 63 of the sequence (image, row
+                    // pair ph, column); the top-row map walks rows 2 ph, the bottom-row
+                    // map rows 2 ph + 1 (both step two rows and run on across images)
+                    const int k0 = (m0 / TC_BM) * 64;
+                    const int per_img = p.pool_ph * p.conv_out_w;
+                    px_n = k0 / per_img;
+                    const int rem = k0 - px_n * per_img;
+                    const int ph = rem / p.conv_out_w;
                     px_h = 2 * ph - p.conv_pad;
-                    px_w = (rem - ph * p.conv_strips) * 64 - p.conv_pad;
+                    px_w = rem - ph * p.conv_out_w - p.conv_pad;
                 } else if (p.conv) {
                     px_n = m0 / p.conv_out_hw;
                     const int rem = m0 - px_n * p.conv_out_hw;
@@ -288,13 +292,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         const int r = tap / p.conv_s;
                         const uint16_t off_w = (uint16_t)(tap - r * p.conv_s), off_h = (uint16_t)r;
                         if (p.conv_pool) {
-                            // two boxes of 64 pixels, rows 2 ph and 2 ph + 1, 8 KB apart
+                            // two boxes of 64 pixels, top rows then bottom rows, 8 KB apart
                             for (int h = 0; h < 2; ++h) {
                                 const uint32_t d = dst + (uint32_t)h * 8192u;
+                                const CUtensorMap* map = h ? &tmA2 : &tmA;
                                 if (pair_bar)
-                                    tma_load_im2col_pair(d, &tmA, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
+                                    tma_load_im2col_pair(d, map, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
                                 else
-                                    tma_load_im2col(d, &tmA, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
+                                    tma_load_im2col(d, map, bar, c0, px_w, px_h + h, px_n, off_w, off_h, pol_a);
                             }
                         } else {
                             if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
@@ -440,29 +445,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((32u * q) << 16) + a * TC_BN;
             if (p.conv_pool) {
-                // Lanes 0..63 of the accumulator hold output row 2 ph (pixel 64 s + lane
-                // of the strip), lanes 64..127 row 2 ph + 1.  Every warp applies the
+                // Lanes 0..63 of the accumulator hold the top pixels of positions
+                // 64 u + lane, lanes 64..127 the bottom pixels of the same positions;
+                // position k is pooled output row k / 2 (OW is even).  Every warp applies the
                 // epilogue and takes the max with its horizontal neighbour (lane ^ 1);
                 // the row 2 ph + 1 quarters (q = 2, 3) then leave their even lanes' values
                 // for the whole tile in shared memory (16 KB each, one hand-over per
                 // tile), and the row 2 ph quarters (q = 0, 1) take the vertical max and
                 // store the pooled pixels from their even lanes.
-                const int u = m0 / TC_BM;
-                const int per_img = p.pool_ph * p.conv_strips;
-                const int n_img = u / per_img;
-                const int rem = u - n_img * per_img;
-                const int ph = rem / p.conv_strips;
-                const int s = rem - ph * p.conv_strips;
-                const int pw = (64 * s + 32 * (int)(q & 1u) + (int)lane) >> 1;
+                const int kpos = (m0 / TC_BM) * 64 + 32 * (int)(q & 1u) + (int)lane;
                 const bool writer = (q >> 1) != 0;
                 const bool even = (lane & 1u) == 0;
                 // 16 rows (even lanes) x 128 B per 32-column chunk, 16 KB per tile
                 const uint32_t xrow = base + Cfg::kOffC + (q & 1u) * 4 * Cfg::kCStage + (lane >> 1) * 128u;
                 const uint32_t xf = bar_xfull(q & 1u), xe = bar_xempty(q & 1u);
                 const uint32_t xph = tcount & 1u;
-                const bool out_ok = !writer && even && n_img < p.pool_nb && pw < p.pool_pw;
-                OutT* const yrow = reinterpret_cast<OutT*>(p.pool_y) +
-                                   ((int64_t)(n_img * p.pool_ph + ph) * p.pool_pw + pw) * p.pool_ldy;
+                const bool out_ok = !writer && even && kpos < 2 * p.pool_rows;
+                OutT* const yrow = reinterpret_cast<OutT*>(p.pool_y) + (int64_t)(kpos >> 1) * p.pool_ldy;
                 const InT* sc = reinterpret_cast<const InT*>(p.ex.scale);
                 const int chunks = nw / 32;
                 bool ok = true;
@@ -684,7 +683,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
-cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const TcParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -700,7 +699,7 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT, KIND>, tmA, tmB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT, KIND>, tmA, tmA2, tmB, tmC, p);
 }
 
 template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
@@ -727,18 +726,18 @@ cudaError_t prepare_impl(int* max_units) {
 }
 
 template <int CG, int MC>
-cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB, const CUtensorMap& tmC,
                       const TcParams& p, int grid, cudaStream_t stream) {
     switch (dtype) {
-        case DT_BF16_F32: return launch_impl<CG, MC, __nv_bfloat16, float>(tmA, tmB, tmC, p, grid, stream);
-        case DT_BF16_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(tmA, tmB, tmC, p, grid, stream);
-        case DT_F16_F32: return launch_impl<CG, MC, __half, float>(tmA, tmB, tmC, p, grid, stream);
-        case DT_F16_F16: return launch_impl<CG, MC, __half, __half>(tmA, tmB, tmC, p, grid, stream);
+        case DT_BF16_F32: return launch_impl<CG, MC, __nv_bfloat16, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_BF16_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_F16_F32: return launch_impl<CG, MC, __half, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_F16_F16: return launch_impl<CG, MC, __half, __half>(tmA, tmA2, tmB, tmC, p, grid, stream);
         // fp8 operands (the format is in the instruction descriptor); bf16 bias / scale
         case DT_E4M3_F32:
-        case DT_E5M2_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 1>(tmA, tmB, tmC, p, grid, stream);
+        case DT_E5M2_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
         case DT_E4M3_BF16:
-        case DT_E5M2_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmB, tmC, p, grid, stream);
+        case DT_E5M2_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -765,11 +764,13 @@ int tc_smem_bytes(int cta_group) {
 }
 
 cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream) {
+                           const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream,
+                           const CUtensorMap* tmA2) {
+    const CUtensorMap& a2 = tmA2 ? *tmA2 : tmA;
     if (cta_group == 2)
-        return p.multicast ? launch_dt<2, 2>(dtype, tmA, tmB, tmC, p, grid, stream)
-                           : launch_dt<2, 1>(dtype, tmA, tmB, tmC, p, grid, stream);
-    if (cta_group == 1) return launch_dt<1, 1>(dtype, tmA, tmB, tmC, p, grid, stream);
+        return p.multicast ? launch_dt<2, 2>(dtype, tmA, a2, tmB, tmC, p, grid, stream)
+                           : launch_dt<2, 1>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
+    if (cta_group == 1) return launch_dt<1, 1>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
