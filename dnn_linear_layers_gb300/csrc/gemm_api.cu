@@ -3,6 +3,7 @@
 // youngju.dev "GEMM to FlashAttention" ("GEMM interface": m, n, k, lda, ldb,
 // ldc, transb) and the handle create/use/destroy pattern of its cuBLAS
 // example, for row-major operands and alpha = 1, beta = 0.
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -98,6 +99,19 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D tensor map over a [n2][n1][n0] row-major tensor of 16-bit elements: boxes
+// of 64 x 128 x 1 elements, 128-byte swizzle, zero fill past the ends.
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t n0, uint64_t n1, uint64_t n2) {
+    cuuint64_t gdim[3] = {n0, n1, n2};
+    cuuint64_t gstride[2] = {n0 * 2, n0 * n1 * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 
 // A operand of an implicit-GEMM convolution: NHWC activations read through an
@@ -348,6 +362,8 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     }
     if (p->max_pairs < 1 || p->max_singles < 1) { delete p; return GEMM_ERR_UNSUPPORTED; }
     for (int dt = 0; dt < 4; ++dt) {
+        e = attention_prepare(dt);
+        if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
         e = skinny_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
     }
@@ -725,6 +741,50 @@ int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int6
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
     return run_impl(p, true, M, N, K, p->workspace, ldk, w, K, bias, y, ldy, epi, ex, dtype, stream, nullptr);
+}
+
+int gemm_attention(gemm_plan_t p, int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D, const void* Q,
+                   const void* K, const void* V, void* O, float scale, int causal, int dtype, void* stream_v) {
+    if (!p || B < 0 || H < 0 || Sq < 0 || Sk < 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_F16_F16OUT) return GEMM_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GEMM_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    if (BH == 0 || Sq == 0) return GEMM_OK;
+    if (O == nullptr || Q == nullptr || (Sk > 0 && (K == nullptr || V == nullptr))) return GEMM_ERR_INVALID_ARG;
+    if (BH > 65535 || Sq > INT32_MAX - 128 || Sk > INT32_MAX - 128) return GEMM_ERR_UNSUPPORTED;
+    if (!aligned16(Q) || !aligned16(O) || (Sk > 0 && (!aligned16(K) || !aligned16(V)))) return GEMM_ERR_ALIGNMENT;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+    DeviceGuard g(p->device);
+    const int ob = out_bytes(dtype);
+    cudaError_t e;
+    if (Sk == 0) {   // every query sees nothing: zeros
+        e = cudaMemsetAsync(O, 0, (size_t)(BH * Sq * D * ob), stream);
+        if (e != cudaSuccess) return record(p, e);
+        p->last_stream = stream; p->have_stream = true;
+        return GEMM_OK;
+    }
+    const CUtensorMapDataType dt = in_map_type(dtype);
+    CUtensorMap tmQ, tmK, tmV;
+    if (!make_map_3d(&tmQ, dt, Q, (uint64_t)D, (uint64_t)Sq, (uint64_t)BH) ||
+        !make_map_3d(&tmK, dt, K, (uint64_t)D, (uint64_t)Sk, (uint64_t)BH) ||
+        !make_map_3d(&tmV, dt, V, (uint64_t)D, (uint64_t)Sk, (uint64_t)BH))
+        return GEMM_ERR_CUDA;
+    AttnParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.BH = (int32_t)BH; ap.Sq = (int32_t)Sq; ap.Sk = (int32_t)Sk;
+    const float s = scale > 0.0f ? scale : 1.0f / std::sqrt((float)D);
+    ap.scale_log2 = s * 1.4426950408889634f;   // log2(e)
+    ap.causal = causal ? 1u : 0u;
+    ap.idesc_s = make_idesc(dtype, false, 128, 128);       // Q K^T: both operands K-major
+    ap.idesc_o = make_idesc(dtype, true, 128, (int)D);     // P V: V is MN-major (D contiguous)
+    ap.O = O;
+    ap.status = p->status_dev;
+    ap.timeout_ns = p->timeout_ns;
+    e = launch_attention(dtype, (int)D, tmQ, tmK, tmV, ap, stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+    p->last_stream = stream; p->have_stream = true;
+    return GEMM_OK;
 }
 
 int gemm_conv2d_maxpool(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S,

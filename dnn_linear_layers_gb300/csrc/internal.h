@@ -140,6 +140,24 @@ cudaError_t skinny_prepare(int dtype);
 cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,
                           int grid, cudaStream_t stream);
 
+// Fused attention forward -------------------------------------------------
+// O = softmax(scale * Q K^T (masked)) V per (batch, head); Q, K, V, O are
+// [B*H][S][D] row-major (D = 64 or 128); one CTA per 128 queries of one head.
+struct AttnParams {
+    int32_t BH;            // batch * heads
+    int32_t Sq, Sk;        // query / key sequence lengths
+    float scale_log2;      // softmax scale * log2(e): scores are taken in base 2
+    uint32_t causal;       // key j visible to query i iff j <= i + (Sk - Sq)
+    uint32_t idesc_s;      // tcgen05 descriptor of S = Q K^T (M 128, N 128, both K-major)
+    uint32_t idesc_o;      // tcgen05 descriptor of O += P V (M 128, N = D, V MN-major)
+    void* O;
+    int* status;
+    uint64_t timeout_ns;
+};
+cudaError_t attention_prepare(int dtype);
+cudaError_t launch_attention(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, const AttnParams& p, cudaStream_t stream);
+
 // Auxiliary kernels ------------------------------------------------------
 // C[i][j] = epilogue(0) for K == 0 (bias and/or ReLU of an empty sum).
 cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bias, uint32_t epi,

@@ -56,6 +56,7 @@ SIGNATURES = {
     "gemm_conv2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _epi_p, _int,
                            _vp]),
     "gemm_run_ex": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _epi_p, _int, _vp]),
+    "gemm_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_float, _int, _int, _vp]),
     "gemm_conv2d_maxpool": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _epi_p,
                                    _int, _vp]),
 }
@@ -253,6 +254,27 @@ class Plan:
                                _stream_handle(stream))
         _check(rc, "gemm_conv2d")
         return y
+
+    def attention(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                  scale: float = 0.0, causal: bool = False, stream=None):
+        """o = softmax(scale * q k^T) v per (batch, head); q, o: [B, H, Sq, D],
+        k, v: [B, H, Sk, D], contiguous; scale 0 means 1 / sqrt(D)."""
+        if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or o.dim() != 4:
+            raise ValueError("q, k, v, o must be [B, H, S, D]")
+        B, H, Sq, D = q.shape
+        Sk = k.shape[2]
+        if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D) or tuple(o.shape) != (B, H, Sq, D):
+            raise ValueError("shape mismatch")
+        for t in (q, k, v, o):
+            if not t.is_contiguous() or t.device.type != "cuda":
+                raise ValueError("q, k, v, o must be contiguous CUDA tensors")
+        if k.dtype != q.dtype or v.dtype != q.dtype:
+            raise ValueError("q, k, v must share one dtype")
+        rc = lib().gemm_attention(self._h, B, H, Sq, Sk, D, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  float(scale), int(bool(causal)), dtype_code(q.dtype, o.dtype),
+                                  _stream_handle(stream))
+        _check(rc, "gemm_attention")
+        return o
 
     def conv2d_maxpool(self, x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: torch.Tensor | None = None,
                        relu: bool = False, pad: int = 0, stream=None, alpha: float = 1.0,

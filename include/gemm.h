@@ -208,6 +208,23 @@ int gemm_conv2d_maxpool(gemm_plan_t plan, int64_t Nb, int64_t H, int64_t W, int6
                         int pad, const void* x, const void* w, void* y, int64_t ldy,
                         const gemm_epilogue_args_t* epi, int dtype, void* stream);
 
+/* Fused attention forward, per (batch, head):
+ *     O = softmax(scale * Q K^T, each row over the visible keys) V
+ * (the online-softmax / FlashAttention recurrence of CMU 15-418 "DNNs and ML
+ * accelerators" notes, section 3.3, and youngju.dev "GEMM to FlashAttention":
+ * the Sq x Sk scores are never written to memory).  Q and O are [B][H][Sq][D],
+ * K and V [B][H][Sk][D], row-major and contiguous, 16-byte aligned device
+ * memory (caller-owned); D is 64 or 128; dtype GEMM_BF16_* / GEMM_F16_*
+ * (inputs, and fp32 or 16-bit O); scale <= 0 means 1 / sqrt(D).  causal != 0:
+ * key j is visible to query i iff j <= i + (Sk - Sq); a query that sees no key
+ * gets zeros.  Products and sums in fp32; the probabilities are rounded to the
+ * input type before they multiply V.  B * H <= 65535.  Returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT, GEMM_ERR_UNSUPPORTED or
+ * GEMM_ERR_CUDA. */
+int gemm_attention(gemm_plan_t plan, int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
+                   const void* Q, const void* K, const void* V, void* O, float scale, int causal, int dtype,
+                   void* stream);
+
 /* --- controls and introspection (benchmarks and tests) ------------------ */
 
 /* Force a kernel (GEMM_KERNEL_*); GEMM_KERNEL_AUTO restores the dispatcher. */

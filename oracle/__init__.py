@@ -411,5 +411,28 @@ def conv2d_maxpool_at(x, w, pad: int, pooled_positions, alpha=1.0, scale=None, b
     return np.maximum(np.maximum(outs[0], outs[1]), np.maximum(outs[2], outs[3]))
 
 
+def attention(Q, K, V, scale=None, causal=False):
+    """Attention in float64 (CMU 15-418 notes, section 3.3: S = scale * Q K^T,
+    each row's softmax, O = P V; the reference that example computes by
+    materialising S).  Q [..., Sq, D], K and V [..., Sk, D].  causal: key j is
+    visible to query i iff j <= i + (Sk - Sq); a row with no visible key gives
+    zeros.  scale None means 1 / sqrt(D)."""
+    Q = _f64(Q); K = _f64(K); V = _f64(V)
+    Sq, D = Q.shape[-2], Q.shape[-1]
+    Sk = K.shape[-2]
+    s = (1.0 / np.sqrt(D)) if scale is None else float(scale)
+    S = np.matmul(Q, np.swapaxes(K, -1, -2)) * s
+    vis = np.ones((Sq, Sk), dtype=bool)
+    if causal:
+        vis = np.arange(Sk)[None, :] <= (np.arange(Sq)[:, None] + (Sk - Sq))
+    S = np.where(vis, S, -np.inf)
+    mx = np.max(S, axis=-1, keepdims=True)
+    mx = np.where(np.isfinite(mx), mx, 0.0)
+    E = np.where(vis, np.exp(S - mx), 0.0)
+    den = E.sum(axis=-1, keepdims=True)
+    P = np.where(den > 0, E / np.where(den > 0, den, 1.0), 0.0)
+    return np.matmul(P, V)
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -1,0 +1,90 @@
+"""Fused attention forward (gemm_attention) against the float64 oracle.
+
+Bound: the kernel rounds the probabilities p = 2^(s - m) to the input type
+before they multiply V, while the row sum l uses the unrounded values, so each
+output moves by at most u * sum_j p_j |V_jd| / l <= u * max_j |V_jd| with u the
+unit roundoff of the input type (2^-9 bf16, 2^-12 fp16); the scores, the
+exponentials and the fp32 sums add far less.  The test allows 2 u max_j |V_jd|
++ 1e-5, plus one ulp of the output type for a 16-bit output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dnn_linear_layers_gb300 import gemm as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plan():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from dnn_linear_layers_gb300 import build
+    build.build()
+    p = G.Plan(0, "nk")
+    yield p
+    p.close()
+
+
+def run(plan, B, H, Sq, Sk, D, causal, in_dtype=torch.bfloat16, out_dtype=torch.float32, seed=0, scale=0.0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, Sq, D, generator=g).to(in_dtype)
+    k = torch.randn(B, H, Sk, D, generator=g).to(in_dtype)
+    v = torch.randn(B, H, Sk, D, generator=g).to(in_dtype)
+    o = torch.full((B, H, Sq, D), float("nan"), dtype=out_dtype, device="cuda")
+    plan.attention(q.cuda(), k.cuda(), v.cuda(), o, scale=scale, causal=causal)
+    assert plan.status() == 0
+    ref = oracle.attention(q, k, v, scale=None if scale <= 0 else scale, causal=causal)
+    got = o.double().cpu().numpy()
+    u = 2.0 ** -9 if in_dtype == torch.bfloat16 else 2.0 ** -12
+    vmax = np.abs(oracle._f64(v)).max(axis=-2, keepdims=True)          # per (b, h, d)
+    bound = 2 * u * vmax + 1e-5
+    if out_dtype == torch.bfloat16:
+        bound = bound + oracle.ulp_bf16(ref)
+    elif out_dtype == torch.float16:
+        bound = bound + np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    worst = float((err / bound).max()) if err.size else 0.0
+    assert np.all(err <= bound), f"worst err/bound {worst:.3f}"
+    return worst
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 128, 128, 64), (1, 1, 300, 300, 128), (2, 3, 257, 513, 64),
+                                   (1, 1, 64, 1000, 128), (1, 2, 513, 200, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_matches_oracle(plan, shape, causal):
+    B, H, Sq, Sk, D = shape
+    run(plan, B, H, Sq, Sk, D, causal, seed=sum(shape) + causal)
+
+
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_attention_fp16_and_bf16_outputs(plan, out):
+    run(plan, 1, 2, 200, 300, 64, False, in_dtype=torch.float16, out_dtype=torch.float16 if out == torch.bfloat16 else out, seed=3)
+    run(plan, 2, 1, 130, 130, 128, True, in_dtype=torch.bfloat16, out_dtype=out, seed=4)
+
+
+def test_attention_scale_and_empty_rows(plan):
+    run(plan, 1, 1, 256, 256, 64, False, seed=5, scale=0.05)
+    # causal with more queries than keys: the first Sq - Sk queries see nothing -> zeros
+    B, H, Sq, Sk, D = 1, 1, 300, 100, 64
+    q = torch.randn(B, H, Sq, D).bfloat16().cuda()
+    k = torch.randn(B, H, Sk, D).bfloat16().cuda()
+    v = torch.randn(B, H, Sk, D).bfloat16().cuda()
+    o = torch.full((B, H, Sq, D), float("nan"), device="cuda")
+    plan.attention(q, k, v, o, causal=True)
+    assert plan.status() == 0
+    assert torch.all(o[:, :, :Sq - Sk] == 0)
+    # no keys at all
+    o2 = torch.full((1, 1, 10, 64), float("nan"), device="cuda")
+    plan.attention(q[:, :, :10], k[:, :, :0], v[:, :, :0], o2)
+    assert torch.all(o2 == 0)
+
+
+def test_attention_rejects_bad_head_dim(plan):
+    q = torch.zeros(1, 1, 8, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(G.GemmError) as e:
+        plan.attention(q, q, q, torch.zeros(1, 1, 8, 96, device="cuda"))
+    assert e.value.code == G.ERR_UNSUPPORTED

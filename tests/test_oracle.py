@@ -412,3 +412,24 @@ def test_conv_maxpool_closed_forms():
     s = -np.ones(C)
     got_neg = oracle.conv2d_maxpool_at(x, w, 0, pos, scale=s)
     assert np.array_equal(got_neg, -x.reshape(Nb, H // 2, 2, W // 2, 2, C).min(axis=(2, 4)).reshape(-1, C))
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(31)
+    Sq, Sk, D = 5, 7, 4
+    Q = rng.standard_normal((Sq, D)); V = rng.standard_normal((Sk, D))
+    # all scores equal: O is the mean of the visible value rows
+    O = oracle.attention(Q, np.zeros((Sk, D)), V)
+    assert np.allclose(O, np.broadcast_to(V.mean(axis=0), (Sq, D)), rtol=0, atol=1e-15)
+    Oc = oracle.attention(Q, np.zeros((Sk, D)), V, causal=True)      # query i sees keys 0 .. i + 2
+    for i in range(Sq):
+        assert np.allclose(Oc[i], V[: i + Sk - Sq + 1].mean(axis=0), rtol=0, atol=1e-15)
+    # two keys with scores 0 and ln 3: weights 1/4 and 3/4
+    O2 = oracle.attention(np.array([[1.0]]), np.array([[0.0], [np.log(3.0)]]), np.array([[4.0], [8.0]]), scale=1.0)
+    assert abs(O2[0, 0] - 7.0) < 1e-14
+    # shifting every key by one vector shifts each query's scores by a constant
+    K = rng.standard_normal((Sk, D))
+    assert np.allclose(oracle.attention(Q, K + rng.standard_normal(D), V), oracle.attention(Q, K, V), atol=1e-12)
+    # a query that sees no key gets zeros (causal, more queries than keys)
+    Oz = oracle.attention(rng.standard_normal((6, D)), K[:3], V[:3], causal=True)
+    assert np.array_equal(Oz[:3], np.zeros((3, D))) and np.all(Oz[3:] != 0)
