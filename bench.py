@@ -52,6 +52,9 @@ WORKLOADS = {
     # ... with per-channel bias, ReLU and the 2 x 2 max-pool fused (gemm_conv2d_maxpool)
     "conv_pool_32x56x56x256_3x3": (100352, 256, 2304, "nk", (True, True), "bf16", 1.0, (2 / 2304) ** 0.5),
     "odd_3000x5000x2048": (3000, 5000, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
+    # fused attention forward, B 4 x H 32 x S 4096 x D 128 (M = B*H*S query rows, N = D, K = S keys)
+    "attention_b4h32s4096d128": (4 * 32 * 4096, 128, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
+    "attention_causal_b4h32s4096d128": (4 * 32 * 4096, 128, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
     # fp8 operands (both K-major: B stored N x K), bf16 output
     "square8192_e4m3": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
     "square8192_e5m2": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
@@ -182,10 +185,26 @@ def fp8_dtype(name):
     return {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}.get(name.rsplit("_", 1)[-1])
 
 
+ATTN_SHAPE = (4, 32, 4096, 128)   # B, H, S, D
+
+
+def attention_flops(causal: bool) -> float:
+    """4 D FLOPs per visible (query, key) pair: 2 D for the score, 2 D for P V."""
+    B, H, S, D = ATTN_SHAPE
+    pairs = S * (S + 1) / 2 if causal else S * S
+    return 4.0 * B * H * D * pairs
+
+
 def make_inputs(name, device, seed=0):
     import torch
     from dnn_linear_layers_gb300.inputs import normal_bf16
     M, N, K, lay, (has_bias, relu), out, a_std, b_std = WORKLOADS[name]
+    if name.startswith(("attention_",)):
+        # q (B, H, S, D) and k, v stacked: (2, B, H, S, D); N(0, 1) bf16
+        B, H, S, D = ATTN_SHAPE
+        q = normal_bf16((B, H, S, D), 3 * seed)
+        kv = torch.stack([normal_bf16((B, H, S, D), 3 * seed + 1), normal_bf16((B, H, S, D), 3 * seed + 2)])
+        return q, kv, None
     f8 = fp8_dtype(name)
     if f8 is not None:   # N(0,1) drawn as bf16, then rounded to the fp8 format
         A = normal_bf16((M, K), 3 * seed, a_std).to(f8)
@@ -229,17 +248,22 @@ def run_ours(args):
     A, B = A_h.to(dev), B_h.to(dev)
     bias = bias_h.to(dev) if bias_h is not None else None
     pool = name.startswith("conv_pool")
-    # the pooled convolution writes a quarter of the output rows
-    C = torch.empty((M // 4 if pool else M, N), dtype=torch.bfloat16, device=dev)
+    attn = name.startswith("attention_")
+    causal = "causal" in name
+    # the pooled convolution writes a quarter of the output rows; attention writes O like q
+    C = (torch.empty(tuple(A.shape), dtype=torch.bfloat16, device=dev) if attn else
+         torch.empty((M // 4 if pool else M, N), dtype=torch.bfloat16, device=dev))
     # Linear-layer weights are constant model parameters: say so to the plan
     plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"))
     if args.kernel != "auto":
         plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
-    flops = 2.0 * M * N * K
+    flops = attention_flops(causal) if attn else 2.0 * M * N * K
     conv = name.startswith(("conv_implicit", "conv_pool"))
     f8 = fp8_dtype(name)
-    if conv:   # activations, weights and output once each (no im2col matrix exists)
+    if attn:   # q, k, v read once, o written once
+        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2)
+    elif conv:   # activations, weights and output once each (no im2col matrix exists)
         nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2 + (N * 2 if has_bias else 0))
     else:
         es = 1 if f8 is not None else 2
@@ -252,7 +276,9 @@ def run_ours(args):
     counter = [0]
 
     def call(a, b, c):
-        if pool:
+        if attn:
+            plan.attention(a, b[0], b[1], c, causal=causal)
+        elif pool:
             plan.conv2d_maxpool(a, b, c, bias, relu, pad=1)
         elif conv:
             plan.conv2d(a, b, c, bias, relu, pad=1)
@@ -424,6 +450,21 @@ def _oracle_rows_timer(name, A, B, bias):
     import oracle
     M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
     threads = len(os.sched_getaffinity(0))
+    if name.startswith("attention_"):
+        # float64 attention of n seeded heads (numpy); each head is a unit of work
+        Bb, Hh, S, D = ATTN_SHAPE
+        causal = "causal" in name
+        rng = np.random.default_rng(0)
+
+        def run_attn(n):
+            heads = rng.choice(Bb * Hh, size=min(Bb * Hh, max(1, n)), replace=False)
+            qf = A.reshape(Bb * Hh, S, D); kf = B[0].reshape(Bb * Hh, S, D); vf = B[1].reshape(Bb * Hh, S, D)
+            t = time.perf_counter()
+            for hd in heads:
+                oracle.attention(qf[hd], kf[hd], vf[hd], causal=causal)
+            return time.perf_counter() - t, len(heads)
+
+        return run_attn, threads
     if name.startswith(("conv_implicit", "conv_pool")):
         # the direct seven-loop convolution at n seeded output positions (one thread)
         Nb, H, W, _ = A.shape
@@ -450,15 +491,25 @@ def _oracle_rows_timer(name, A, B, bias):
     return run, threads
 
 
+def oracle_unit(name):
+    """(FLOPs per unit of oracle work, units in the workload, unit description)."""
+    M, N, K, *_ = WORKLOADS[name]
+    if name.startswith("attention_"):
+        Bb, Hh, S, D = ATTN_SHAPE
+        return attention_flops("causal" in name) / (Bb * Hh), Bb * Hh, f"heads ({S} x {S} scores, D {D})"
+    return 2.0 * N * K, M, f"rows of C (each {N} x {K} MACs)"
+
+
 def cpu_baseline(name, A, B, bias, seconds: float):
     """Oracle (float64 triple loop, OpenMP over rows) on whole rows of C, about `seconds` of work."""
-    M, N, K, *_ = WORKLOADS[name]
+    per, total, what = oracle_unit(name)
     run, threads = _oracle_rows_timer(name, A, B, bias)
-    dt, n = run(threads)                        # calibration: one row per thread
-    n = int(max(threads, min(M, threads * max(1, round(seconds / max(dt, 1e-3))))))
+    cal = 1 if name.startswith("attention_") else threads
+    dt, n = run(cal)                            # calibration: one row per thread (one head)
+    n = int(max(cal, min(total, cal * max(1, round(seconds / max(dt, 1e-3))))))
     dt, n = run(n)
-    return {"value": round(2.0 * n * N * K / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "sample": f"{n} of {M} rows of C (each {N} x {K} MACs), {dt:.1f} s",
+    return {"value": round(per * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"{n} of {total} {what}, {dt:.1f} s",
             "seconds": round(dt, 2)}
 
 
@@ -469,23 +520,25 @@ def run_reference(args):
     name = args.workload
     M, N, K, lay, (has_bias, relu), *_ = WORKLOADS[name]
     A, B, bias = make_inputs(name, None, seed=0)
+    per, total, what = oracle_unit(name)
     run, threads = _oracle_rows_timer(name, A, B, bias)
-    dt, n = run(threads)
+    cal = 1 if name.startswith("attention_") else threads
+    dt, n = run(cal)
     # size every step so the whole run stays within about two minutes
     per_step = min(max(90.0 / (args.warmup + args.steps), 0.05), args.cpu_seconds)
-    n = int(max(threads, min(M, threads * max(1, round(per_step / max(dt, 1e-3))))))
+    n = int(max(cal, min(total, cal * max(1, round(per_step / max(dt, 1e-3))))))
     vals, times = [], []
     for i in range(args.warmup + args.steps):
         dt, n_done = run(n)
         if i >= args.warmup:
-            vals.append(2.0 * n_done * N * K / dt / 1e12); times.append(dt)
+            vals.append(per * n_done / dt / 1e12); times.append(dt)
     value = round(statistics.median(vals), 6)
     res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic: same inputs as the GPU arm", "config": {"workload": name, "M": M, "N": N, "K": K},
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                            "sample": f"{n} of {M} rows of C per step (each {N} x {K} MACs)"},
+                            "sample": f"{n} of {total} {what} per step"},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
     return res

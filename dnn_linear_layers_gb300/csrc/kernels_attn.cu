@@ -7,17 +7,22 @@
 // blocks that stay on chip).
 //
 // Design for sm_103a, one CTA per 128 queries of one head:
-//   * warp 0: TMA producer -- Q once, K_j and V_j (128 keys each) into a
-//     2-stage ring (3-D tensor maps: keys past Sk read as zero);
+//   * warp 0: TMA producer -- Q once, K_j and V_j (128 keys each) into
+//     2-stage rings (3-D tensor maps: keys past Sk read as zero); a K slot is
+//     refilled as soon as its score product is done, a V slot once its PV
+//     product is, so the next K block is on chip well before it is needed;
 //   * warp 1: MMA issuer -- S_j = Q K_j^T into one of two TMEM score buffers
-//     (so S_{j+1} is computed while the softmax works on S_j), then
+//     (S_{j+1} is computed while the softmax works on S_j), then
 //     O += P_j V_j into the TMEM accumulator once P_j is ready;
 //   * warps 2..5: softmax, one thread per query row (TMEM lane), so row max
-//     and row sum need no shuffles: pass 1 reads the row's 128 scores for the
-//     max, pass 2 rereads them, writes P = 2^(s - m) as bf16 / fp16 into a
-//     128-byte-swizzled shared-memory tile (the A operand of the PV product)
-//     and adds up l; the accumulator row is rescaled in TMEM only when some
-//     row of the warp raised its max.  At the end O / l is stored.
+//     and row sum need no shuffles.  The row's 128 scores are read from TMEM
+//     once (the score buffer is handed back at once), P = 2^(s - m) is written
+//     as bf16 / fp16 into one of two 128-byte-swizzled shared-memory tiles
+//     (the A operand of the PV product; two, so P_j is written while P_{j-1} V
+//     runs).  The reference max m of a row moves only when the block max
+//     exceeds it by more than 8 (a factor 2^8): O = sum_j 2^(s_j - m) v_j /
+//     sum_j 2^(s_j - m) holds for any m, so a stale m changes nothing but the
+//     rounding, and the accumulator row is rescaled in TMEM only then.
 // Scores are taken in base 2 (scale * log2 e folded into one factor).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -43,13 +48,14 @@ struct AttnCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;
-    static constexpr int kOffMisc = kOffP + kPBytes;
+    static constexpr int kOffP = kOffV + kStages * kKVBytes;   // two P tiles
+    static constexpr int kOffMisc = kOffP + 2 * kPBytes;
     static constexpr int kMiscBytes = 256;
     static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;   // + alignment slack
-    // barriers (8 bytes each) in the misc region
-    static constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarKVEmpty = 5, kBarSFull = 7, kBarSFree = 9,
-                         kBarP = 11, kBarO = 12, kBarDone = 13, kAbort = 14 * 8, kTmemPtr = kAbort + 4;
+    // barriers (8 bytes each) in the misc region; pairs are indexed by buffer
+    static constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarSFull = 9,
+                         kBarSFree = 11, kBarPFull = 13, kBarODone = 15, kBarDone = 17, kAbort = 18 * 8,
+                         kTmemPtr = kAbort + 4;
     static constexpr int kTmemS = 0;      // two score buffers: columns 0..127 and 128..255
     static constexpr int kTmemO = 256;    // accumulator: columns 256 .. 256 + D - 1
     static_assert(kTmemPtr + 4 <= kMiscBytes, "misc layout");
@@ -96,6 +102,14 @@ __device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 2^x on the special-function unit (ex2.approx: relative error about 2^-22,
+// subnormal results flushed to zero, 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // number of 128-key blocks query block q0 .. q0 + 127 looks at
 __device__ __forceinline__ int key_blocks(const AttnParams& p, int q0) {
     const int all = (p.Sk + kBKey - 1) / kBKey;
@@ -130,12 +144,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(Cfg::kBarK + s), 1);
             mbar_init(bar(Cfg::kBarV + s), 1);
-            mbar_init(bar(Cfg::kBarKVEmpty + s), 1);
+            mbar_init(bar(Cfg::kBarKEmpty + s), 1);
+            mbar_init(bar(Cfg::kBarVEmpty + s), 1);
             mbar_init(bar(Cfg::kBarSFull + s), 1);
             mbar_init(bar(Cfg::kBarSFree + s), 4);   // the four softmax warps
+            mbar_init(bar(Cfg::kBarPFull + s), 4);
+            mbar_init(bar(Cfg::kBarODone + s), 1);
         }
-        mbar_init(bar(Cfg::kBarP), 4);
-        mbar_init(bar(Cfg::kBarO), 1);
         mbar_init(bar(Cfg::kBarDone), 1);
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
@@ -163,12 +178,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tma_load_3d(base + Cfg::kOffQ + b * kBox, &tmQ, bar(Cfg::kBarQ), 64 * b, q0, bh, pol_q);
             for (int j = 0; j < nkb; ++j) {
                 const int s = j & 1;
-                if (!w(bar(Cfg::kBarKVEmpty + s), (((uint32_t)j >> 1) & 1u) ^ 1u)) break;
+                const uint32_t par = (((uint32_t)j >> 1) & 1u) ^ 1u;   // slot s freed by block j - 2
+                if (!w(bar(Cfg::kBarKEmpty + s), par)) break;
                 mbar_arrive_expect_tx(bar(Cfg::kBarK + s), Cfg::kKVBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(base + Cfg::kOffK + s * Cfg::kKVBytes + b * kBox, &tmK, bar(Cfg::kBarK + s), 64 * b,
                                 j * kBKey, bh, pol_kv);
+                if (!w(bar(Cfg::kBarVEmpty + s), par)) break;
                 mbar_arrive_expect_tx(bar(Cfg::kBarV + s), Cfg::kKVBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
@@ -183,8 +200,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t tS = tmem + Cfg::kTmemS, tO = tmem + Cfg::kTmemO;
             for (int j = 0; j <= nkb && ok; ++j) {
                 if (j < nkb) {   // S_j = Q K_j^T
-                    const int sb = j & 1, s = j & 1;
-                    ok = w(bar(Cfg::kBarSFree + sb), (((uint32_t)j >> 1) & 1u) ^ 1u) &&
+                    const int s = j & 1;
+                    ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)j >> 1) & 1u) ^ 1u) &&
                          w(bar(Cfg::kBarK + s), ((uint32_t)j >> 1) & 1u);
                     if (!ok) break;
                     tc_fence_after();
@@ -192,17 +209,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                        tc_mma<1>(tS + (uint32_t)sb * 128u, smem_desc_sw128(kq + off, 16, 1024),
+                        tc_mma<1>(tS + (uint32_t)s * 128u, smem_desc_sw128(kq + off, 16, 1024),
                                   smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
                     }
-                    tc_commit_1(bar(Cfg::kBarSFull + sb));
+                    tc_commit_1(bar(Cfg::kBarSFull + s));
+                    tc_commit_1(bar(Cfg::kBarKEmpty + s));
                 }
                 if (j >= 1) {    // O += P_{j-1} V_{j-1}
                     const int jp = j - 1, s = jp & 1;
-                    ok = w(bar(Cfg::kBarP), (uint32_t)jp & 1u) && w(bar(Cfg::kBarV + s), ((uint32_t)jp >> 1) & 1u);
+                    ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)jp >> 1) & 1u) &&
+                         w(bar(Cfg::kBarV + s), ((uint32_t)jp >> 1) & 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t pp = base + Cfg::kOffP, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
+                    const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBKey / 16; ++kk) {
                         const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
@@ -212,8 +231,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                   smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
                                   (jp | kk) ? 1u : 0u);
                     }
-                    tc_commit_1(bar(Cfg::kBarO));
-                    tc_commit_1(bar(Cfg::kBarKVEmpty + s));
+                    tc_commit_1(bar(Cfg::kBarODone + s));
+                    tc_commit_1(bar(Cfg::kBarVEmpty + s));
                 }
             }
             // every MMA issued has finished before TMEM is released
@@ -229,49 +248,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int i = q0 + r;                              // query index
         const int lim = p.causal ? i + (p.Sk - p.Sq) : p.Sk - 1;   // last visible key
         const uint32_t lrow = (32u * q) << 16;             // TMEM lane offset of this warp
-        const uint32_t prow = base + Cfg::kOffP + (uint32_t)r * 128u;
-        float m = -INFINITY, l = 0.0f;
+        const float c2 = p.scale_log2;
+        float m = -INFINITY, l = 0.0f;                     // reference max (base 2), row sum
         bool ok = true;
         for (int j = 0; j < nkb && ok; ++j) {
             const int sb = j & 1;
             ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ((uint32_t)j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
+            uint32_t v[4][32];
             const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v[c]);
+            tmem_ld_wait();
+            // the scores are in registers: the buffer is free for S_{j+2}
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
             const int k0 = j * kBKey;
-            // pass 1: row max of the visible scores (base 2)
-            float mx = -INFINITY;
+            if (!__all_sync(0xffffffffu, k0 + kBKey - 1 <= lim)) {   // a block on the mask's edge
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v);
-                tmem_ld_wait();
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (k0 + 32 * c + t <= lim) mx = fmaxf(mx, __uint_as_float(v[t]) * p.scale_log2);
+                    for (int t = 0; t < 32; ++t)
+                        if (k0 + 32 * c + t > lim) v[c][t] = __float_as_uint(-INFINITY);
             }
-            const float m_new = fmaxf(m, mx);
-            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;      // nothing visible yet
-            const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_use);
-            // P_j goes where P_{j-1} was, and O is rescaled: PV_{j-1} must be done
-            if (j >= 1) {
-                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarO), (uint32_t)(j - 1) & 1u));
+            // block max of the raw scores, scaled once (the scale is positive)
+            float mp[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) mp[t] = __uint_as_float(v[0][t]);
+#pragma unroll
+            for (int x = 8; x < 128; ++x) mp[x & 7] = fmaxf(mp[x & 7], __uint_as_float(v[x >> 5][x & 31]));
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * c2;
+            const bool grow = mx > m + 8.0f;      // false while nothing is visible
+            float alpha = 1.0f;
+            if (grow) {
+                alpha = ex2_approx(m - mx);       // 0 on the row's first visible block
+                m = mx;
+            }
+            const float mu = (m == -INFINITY) ? 0.0f : m;
+            // P_j goes into the tile that P_{j-2} V_{j-2} read
+            if (j >= 2) {
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + sb), (((uint32_t)j - 2) >> 1) & 1u));
                 if (!ok) break;
                 tc_fence_after();
             }
-            // pass 2: P = 2^(s - m), row sum, P as 16-bit into the swizzled A tile
-            float sum = 0.0f;
+            // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
+            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
+            float sp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v);
-                tmem_ld_wait();
                 float e[32];
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
-                    const bool vis = k0 + 32 * c + t <= lim;
-                    e[t] = vis ? exp2f(__uint_as_float(v[t]) * p.scale_log2 - m_use) : 0.0f;
-                    sum += e[t];
+                    e[t] = ex2_approx(fmaf(__uint_as_float(v[c][t]), c2, -mu));
+                    sp[t & 7] += e[t];
                 }
                 // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
                 const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
@@ -283,37 +315,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                   pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
                 }
             }
-            l = l * alpha + sum;
-            // the score buffer is free for S_{j+2}
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
-            // rescale the accumulator row when the max of some row of the warp grew
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+            l = l * alpha + (((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7])));
+            // a row whose reference max moved rescales its accumulator row, once
+            // P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
+            if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (sb ^ 1)), (((uint32_t)j - 1) >> 1) & 1u));
+                if (!ok) break;
+                tc_fence_after();
                 const uint32_t tO = tmem + lrow + Cfg::kTmemO;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, v);
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-                    tmem_st_32x32b_x32(tO + (uint32_t)c * 32u, v);
+                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    tmem_st_32x32b_x32(tO + (uint32_t)c * 32u, o);
                 }
                 tmem_st_wait();
             }
-            m = m_new;
             // P_j (generic-proxy stores) and the rescaled O are ready for the MMA
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarP));
+            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
         }
         // ---- O / l, stored by row.  The TMEM loads are warp-collective: the
         // whole warp loads (conditions below are warp-uniform); only the stores
         // depend on the row being a real query.
         if (ok && nkb > 0) {
-            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarO), (uint32_t)(nkb - 1) & 1u));
+            ok = __all_sync(0xffffffffu,
+                            w(bar(Cfg::kBarODone + ((nkb - 1) & 1)), (((uint32_t)nkb - 1) >> 1) & 1u));
             if (ok) tc_fence_after();
         }
         const bool store = i < p.Sq;
