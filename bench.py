@@ -102,6 +102,7 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float)
 KERNEL_SOURCES = {
     "tc": ["kernels_tc.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
     "skinny": ["kernels_skinny.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
+    "attn": ["kernels_attn.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
 }
 
 
@@ -414,13 +415,17 @@ def run_ours(args):
             "data": ("synthetic: N(0,1) drawn as bf16 (torch CPU generator, fixed seeds), rounded to "
                      f"{name.rsplit('_', 1)[-1]}, resident in HBM" if f8 is not None else
                      "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM"),
-            "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": lay,
-                       "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none",
+            "config": {"workload": name,
+                       **({"B": ATTN_SHAPE[0], "H": ATTN_SHAPE[1], "Sq": ATTN_SHAPE[2], "Sk": ATTN_SHAPE[2],
+                           "D": ATTN_SHAPE[3], "causal": "causal" in name, "scale": "1/sqrt(D)"} if attn else
+                          {"M": M, "N": N, "K": K, "b_layout": lay,
+                           "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none"}),
                        "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
                        "l2": (f"inputs larger than L2 ({nbytes / 1e6:.1f} MB > {l2 / 1e6:.0f} MB), no flush"
                               if n_copies == 1 else
                               f"{n_copies} rotating operand copies ({n_copies * nbytes / 1e6:.0f} MB > 2 x L2)"),
-                       "kernel": {1: "tc_pair", 2: "tc_single", 4: "skinny"}.get(plan.last_kernel, str(plan.last_kernel)),
+                       "kernel": "attention" if attn else
+                                 {1: "tc_pair", 2: "tc_single", 4: "skinny"}.get(plan.last_kernel, str(plan.last_kernel)),
                        "timing": "CUDA graph of the K steps, one replay" if graph is not None else "eager launches"},
             "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                          "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,

@@ -36,6 +36,7 @@ enum StatusBits : int {
     ST_TIMEOUT_PRODUCER = 1,
     ST_TIMEOUT_MMA = 2,
     ST_TIMEOUT_EPILOGUE = 4,
+    ST_SMEM_LAYOUT = 8,     // shared window too misaligned for the kernel's tiles (it did nothing)
 };
 
 // Fault-injection flags (tests only): make one wait run out on purpose.

@@ -8,15 +8,23 @@
 //
 // Design for sm_103a, one CTA per 128 queries of one head:
 //   * warp 0: TMA producer -- Q once, K_j and V_j (128 keys each) into
-//     2-stage rings (3-D tensor maps: keys past Sk read as zero); a K slot is
-//     refilled as soon as its score product is done, a V slot once its PV
-//     product is, so the next K block is on chip well before it is needed;
-//   * warp 1: MMA issuer -- S_j = Q K_j^T into one of two TMEM score buffers
-//     (S_{j+1} is computed while the softmax works on S_j), then
-//     O += P_j V_j into the TMEM accumulator once P_j is ready;
-//   * warps 2..5: softmax, one thread per query row (TMEM lane), so row max
-//     and row sum need no shuffles.  The row's 128 scores are read from TMEM
-//     once (the score buffer is handed back at once), P = 2^(s - m) is written
+//     2-stage rings (3-D tensor maps: keys past Sk read as zero).  K runs one
+//     block ahead of V (a K slot frees when its score product is done, a V
+//     slot only when its PV product is), so the next K block is on chip before
+//     the tensor core wants it;
+//   * warps 1 and 2: MMA issuers -- warp 1 S_j = Q K_j^T into one of two TMEM
+//     score buffers (S_{j+1} is computed while the softmax works on S_j), warp
+//     2 O += P_j V_j into the TMEM accumulator once P_j is ready.  An MMA
+//     instruction is accepted only as the tensor pipe drains, so one thread
+//     issuing both products would leave the pipe idle while it waited for the
+//     other's operands; two threads keep it fed from whichever is ready;
+//   * warps 3..10: softmax, two threads per query row (TMEM lane), one per
+//     half of the 128 keys (and of the D accumulator columns), so two warps
+//     share each SM sub-partition and hide each other's latency; the halves
+//     swap their block maxima through shared memory behind a (bounded)
+//     mbarrier and keep partial row sums until the end.  Each thread reads its
+//     64 scores from TMEM once (the score buffer is handed back at once),
+//     P = 2^(s - m) is written
 //     as bf16 / fp16 into one of two 128-byte-swizzled shared-memory tiles
 //     (the A operand of the PV product; two, so P_j is written while P_{j-1} V
 //     runs).  The reference max m of a row moves only when the block max
@@ -34,7 +42,7 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 352;
 constexpr int kBQ = 128;          // queries per CTA (TMEM lanes)
 constexpr int kBKey = 128;        // keys per block
 constexpr int kBox = 128 * 128;   // one 128-row x 128-byte swizzled box
@@ -50,15 +58,20 @@ struct AttnCfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffP = kOffV + kStages * kKVBytes;   // two P tiles
     static constexpr int kOffMisc = kOffP + 2 * kPBytes;
-    static constexpr int kMiscBytes = 256;
-    static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;   // + alignment slack
+    static constexpr int kOffXch = 256;   // in misc: float [2 slots][2 halves][128 rows]
+    static constexpr int kMiscBytes = kOffXch + 2 * 2 * kBQ * 4;
+    // the tiles want 1024-byte alignment; a window starting at a multiple of
+    // 256 bytes fits (the kernel checks, and stops with a status bit if not)
+    static constexpr int kSlack = 768;
+    static constexpr int kSmem = kOffMisc + kMiscBytes + kSlack;
     // barriers (8 bytes each) in the misc region; pairs are indexed by buffer
     static constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarSFull = 9,
-                         kBarSFree = 11, kBarPFull = 13, kBarODone = 15, kBarDone = 17, kAbort = 18 * 8,
-                         kTmemPtr = kAbort + 4;
+                         kBarSFree = 11, kBarPFull = 13, kBarODone = 15, kBarDone = 17,
+                         kBarXch = 18,   // [4 lane quarters][2 slots]
+                         kAbort = 26 * 8, kTmemPtr = kAbort + 4;
     static constexpr int kTmemS = 0;      // two score buffers: columns 0..127 and 128..255
     static constexpr int kTmemO = 256;    // accumulator: columns 256 .. 256 + D - 1
-    static_assert(kTmemPtr + 4 <= kMiscBytes, "misc layout");
+    static_assert(kTmemPtr + 4 <= kOffXch, "misc layout");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -110,6 +123,33 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Pairs of fp32 values in one 64-bit register, for the paired fp32
+// instructions of sm_100-class SMs (one instruction does two lanes of work).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max of three (one instruction on sm_100-class SMs)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // number of 128-key blocks query block q0 .. q0 + 127 looks at
 __device__ __forceinline__ int key_blocks(const AttnParams& p, int q0) {
     const int all = (p.Sk + kBKey - 1) / kBKey;
@@ -135,6 +175,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::kOffMisc + Cfg::kTmemPtr);
 
     const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+    if (base - raw > (uint32_t)Cfg::kSlack) {   // same for every thread: nothing started yet
+        if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_LAYOUT);
+        return;
+    }
     const int bh = (int)blockIdx.y;
     const int q0 = (int)blockIdx.x * kBQ;
     const int nkb = key_blocks(p, q0);
@@ -147,11 +191,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(Cfg::kBarKEmpty + s), 1);
             mbar_init(bar(Cfg::kBarVEmpty + s), 1);
             mbar_init(bar(Cfg::kBarSFull + s), 1);
-            mbar_init(bar(Cfg::kBarSFree + s), 4);   // the four softmax warps
-            mbar_init(bar(Cfg::kBarPFull + s), 4);
+            mbar_init(bar(Cfg::kBarSFree + s), 8);   // the eight softmax warps
+            mbar_init(bar(Cfg::kBarPFull + s), 8);
             mbar_init(bar(Cfg::kBarODone + s), 1);
         }
-        mbar_init(bar(Cfg::kBarDone), 1);
+        for (int x = 0; x < 8; ++x) mbar_init(bar(Cfg::kBarXch + x), 64);   // both warps of a quarter
+        mbar_init(bar(Cfg::kBarDone), 2);   // the two MMA issuers
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmQ);
@@ -176,111 +221,138 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
             for (int b = 0; b < D / 64; ++b)
                 tma_load_3d(base + Cfg::kOffQ + b * kBox, &tmQ, bar(Cfg::kBarQ), 64 * b, q0, bh, pol_q);
-            for (int j = 0; j < nkb; ++j) {
+            // block j of K or V: one 128-key box per 64 columns
+            auto load_kv = [&](const CUtensorMap* map, int off, int barid, int j) {
                 const int s = j & 1;
-                const uint32_t par = (((uint32_t)j >> 1) & 1u) ^ 1u;   // slot s freed by block j - 2
-                if (!w(bar(Cfg::kBarKEmpty + s), par)) break;
-                mbar_arrive_expect_tx(bar(Cfg::kBarK + s), Cfg::kKVBytes);
+                mbar_arrive_expect_tx(bar(barid + s), Cfg::kKVBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(base + Cfg::kOffK + s * Cfg::kKVBytes + b * kBox, &tmK, bar(Cfg::kBarK + s), 64 * b,
-                                j * kBKey, bh, pol_kv);
-                if (!w(bar(Cfg::kBarVEmpty + s), par)) break;
-                mbar_arrive_expect_tx(bar(Cfg::kBarV + s), Cfg::kKVBytes);
-#pragma unroll
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(base + Cfg::kOffV + s * Cfg::kKVBytes + b * kBox, &tmV, bar(Cfg::kBarV + s), 64 * b,
-                                j * kBKey, bh, pol_kv);
+                    tma_load_3d(base + off + s * Cfg::kKVBytes + b * kBox, map, bar(barid + s), 64 * b, j * kBKey, bh,
+                                pol_kv);
+            };
+            // order K_0, K_1, V_0, K_2, V_1, ...: slot j & 1 of K frees when S_{j-2}
+            // is done, that of V when P_{j-2} V_{j-2} is
+            if (w(bar(Cfg::kBarKEmpty), 1u)) {
+                load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, 0);
+                for (int j = 0; j < nkb; ++j) {
+                    if (j + 1 < nkb) {
+                        const int jn = j + 1;
+                        if (!w(bar(Cfg::kBarKEmpty + (jn & 1)), (((uint32_t)jn >> 1) & 1u) ^ 1u)) break;
+                        load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, jn);
+                    }
+                    if (!w(bar(Cfg::kBarVEmpty + (j & 1)), (((uint32_t)j >> 1) & 1u) ^ 1u)) break;
+                    load_kv(&tmV, Cfg::kOffV, Cfg::kBarV, j);
+                }
             }
         }
     } else if (warp == 1) {
+        // ---- S issuer: S_j = Q K_j^T into score buffer j & 1
         if (lane == 0 && nkb > 0) {
             const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
             bool ok = w(bar(Cfg::kBarQ), 0);
-            const uint32_t tS = tmem + Cfg::kTmemS, tO = tmem + Cfg::kTmemO;
-            for (int j = 0; j <= nkb && ok; ++j) {
-                if (j < nkb) {   // S_j = Q K_j^T
-                    const int s = j & 1;
-                    ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)j >> 1) & 1u) ^ 1u) &&
-                         w(bar(Cfg::kBarK + s), ((uint32_t)j >> 1) & 1u);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + s * Cfg::kKVBytes;
+            const uint32_t tS = tmem + Cfg::kTmemS;
+            for (int j = 0; j < nkb && ok; ++j) {
+                const int s = j & 1;
+                ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)j >> 1) & 1u) ^ 1u) &&
+                     w(bar(Cfg::kBarK + s), ((uint32_t)j >> 1) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + s * Cfg::kKVBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                        tc_mma<1>(tS + (uint32_t)s * 128u, smem_desc_sw128(kq + off, 16, 1024),
-                                  smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
-                    }
-                    tc_commit_1(bar(Cfg::kBarSFull + s));
-                    tc_commit_1(bar(Cfg::kBarKEmpty + s));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
+                    tc_mma<1>(tS + (uint32_t)s * 128u, smem_desc_sw128(kq + off, 16, 1024),
+                              smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
                 }
-                if (j >= 1) {    // O += P_{j-1} V_{j-1}
-                    const int jp = j - 1, s = jp & 1;
-                    ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)jp >> 1) & 1u) &&
-                         w(bar(Cfg::kBarV + s), ((uint32_t)jp >> 1) & 1u);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBKey / 16; ++kk) {
-                        const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                        // V is K x N = keys x D with D contiguous: MN-major, 64-column
-                        // chunks one box apart, 16 key rows per step
-                        tc_mma<1>(tO, smem_desc_sw128(pp + aoff, 16, 1024),
-                                  smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
-                                  (jp | kk) ? 1u : 0u);
-                    }
-                    tc_commit_1(bar(Cfg::kBarODone + s));
-                    tc_commit_1(bar(Cfg::kBarVEmpty + s));
-                }
+                tc_commit_1(bar(Cfg::kBarSFull + s));
+                tc_commit_1(bar(Cfg::kBarKEmpty + s));
             }
-            // every MMA issued has finished before TMEM is released
             tc_commit_1(bar(Cfg::kBarDone));
+            // every MMA of both issuers has finished before TMEM is released
             const AWait wd{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
             wd(bar(Cfg::kBarDone), 0);
         }
+    } else if (warp == 2) {
+        // ---- PV issuer: O += P_j V_j once the softmax has written P_j
+        if (lane == 0 && nkb > 0) {
+            const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
+            bool ok = true;
+            const uint32_t tO = tmem + Cfg::kTmemO;
+            for (int j = 0; j < nkb && ok; ++j) {
+                const int s = j & 1;
+                ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)j >> 1) & 1u) &&
+                     w(bar(Cfg::kBarV + s), ((uint32_t)j >> 1) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBKey / 16; ++kk) {
+                    const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
+                    // V is K x N = keys x D with D contiguous: MN-major, 64-column
+                    // chunks one box apart, 16 key rows per step
+                    tc_mma<1>(tO, smem_desc_sw128(pp + aoff, 16, 1024),
+                              smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
+                              (j | kk) ? 1u : 0u);
+                }
+                tc_commit_1(bar(Cfg::kBarODone + s));
+                tc_commit_1(bar(Cfg::kBarVEmpty + s));
+            }
+            tc_commit_1(bar(Cfg::kBarDone));
+        }
     } else {
-        // ---- softmax warps: thread = query row r (TMEM lane 32 q + lane)
+        // ---- softmax warps: thread = query row r (TMEM lane 32 q + lane), key half h
         const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const uint32_t q = warp & 3u;
+        const uint32_t h = (warp - 3u) >> 2;
         const int r = 32 * (int)q + (int)lane;
         const int i = q0 + r;                              // query index
         const int lim = p.causal ? i + (p.Sk - p.Sq) : p.Sk - 1;   // last visible key
         const uint32_t lrow = (32u * q) << 16;             // TMEM lane offset of this warp
+        volatile float* const xch = reinterpret_cast<volatile float*>(base_ptr + Cfg::kOffMisc + Cfg::kOffXch);
         const float c2 = p.scale_log2;
-        float m = -INFINITY, l = 0.0f;                     // reference max (base 2), row sum
+        float m = -INFINITY, l = 0.0f;                     // reference max (base 2), this half's row sum
         bool ok = true;
         for (int j = 0; j < nkb && ok; ++j) {
             const int sb = j & 1;
-            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ((uint32_t)j >> 1) & 1u));
+            const uint32_t ph = ((uint32_t)j >> 1) & 1u;
+            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ph));
             if (!ok) break;
             tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v[c]);
+            uint32_t v[2][32];
+            const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u + h * 64u;
+            tmem_ld_32x32b_x32(tS, v[0]);
+            tmem_ld_32x32b_x32(tS + 32u, v[1]);
             tmem_ld_wait();
             // the scores are in registers: the buffer is free for S_{j+2}
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
-            const int k0 = j * kBKey;
-            if (!__all_sync(0xffffffffu, k0 + kBKey - 1 <= lim)) {   // a block on the mask's edge
+            const int k0 = j * kBKey + 64 * (int)h;
+            if (!__all_sync(0xffffffffu, k0 + 63 <= lim)) {   // a block on the mask's edge
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
                         if (k0 + 32 * c + t > lim) v[c][t] = __float_as_uint(-INFINITY);
             }
-            // block max of the raw scores, scaled once (the scale is positive)
+            // max of this half's raw scores, scaled once (the scale is positive)
             float mp[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) mp[t] = __uint_as_float(v[0][t]);
 #pragma unroll
-            for (int x = 8; x < 128; ++x) mp[x & 7] = fmaxf(mp[x & 7], __uint_as_float(v[x >> 5][x & 31]));
-            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * c2;
+            for (int x = 8; x < 64; x += 16)
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    mp[t] = fmax3(mp[t], __uint_as_float(v[(x + t) >> 5][(x + t) & 31]),
+                                  __uint_as_float(v[(x + 8 + t) >> 5][(x + 8 + t) & 31]));
+            const float mh = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7])) * c2;
+            // the block max of the row: both halves take the max of the same two values
+            const uint32_t xb = bar(Cfg::kBarXch + 2 * (int)q + sb);
+            xch[(sb * 2 + (int)h) * kBQ + r] = mh;
+            mbar_arrive_local(xb);
+            ok = __all_sync(0xffffffffu, w(xb, ph));
+            if (!ok) break;
+            const float mx = fmaxf(mh, xch[(sb * 2 + (int)(h ^ 1u)) * kBQ + r]);
             const bool grow = mx > m + 8.0f;      // false while nothing is visible
             float alpha = 1.0f;
             if (grow) {
@@ -294,37 +366,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!ok) break;
                 tc_fence_after();
             }
-            // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
-            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
-            float sp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+            // P = 2^(s - m) as 16-bit into this half's box of the swizzled A tile
+            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + h * (uint32_t)kBox + (uint32_t)r * 128u;
+            const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
+            uint64_t sp[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int t = 0; t < 4; ++t) sp[t] = f2_pack(0.0f, 0.0f);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 float e[32];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    e[t] = ex2_approx(fmaf(__uint_as_float(v[c][t]), c2, -mu));
-                    sp[t & 7] += e[t];
+                for (int t = 0; t < 32; t += 2) {   // s * scale - m for two keys at once
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c][t]), __uint_as_float(v[c][t + 1])), c2x2, nmu2), x0, x1);
+                    e[t] = ex2_approx(x0);
+                    e[t + 1] = ex2_approx(x1);
+                    sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(e[t], e[t + 1]));
                 }
-                // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
-                const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
+                // keys 32 c .. 32 c + 31 of the half: 16-byte pieces 4 c .. 4 c + 3
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t piece = (uint32_t)(4 * (c & 1) + t) ^ ((uint32_t)r & 7u);
-                    st_shared_v4u(box + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
+                    const uint32_t piece = (uint32_t)(4 * c + t) ^ ((uint32_t)r & 7u);
+                    st_shared_v4u(prow + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
                                   pack2<InT>(e[8 * t + 2], e[8 * t + 3]), pack2<InT>(e[8 * t + 4], e[8 * t + 5]),
                                   pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
                 }
             }
-            l = l * alpha + (((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7])));
-            // a row whose reference max moved rescales its accumulator row, once
-            // P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
+            float s0, s1;
+            f2_unpack(f2_add(f2_add(sp[0], sp[1]), f2_add(sp[2], sp[3])), s0, s1);
+            l = l * alpha + (s0 + s1);
+            // a row whose reference max moved rescales its half of the accumulator
+            // row, once P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
             if (j >= 1 && __any_sync(0xffffffffu, grow)) {
                 ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (sb ^ 1)), (((uint32_t)j - 1) >> 1) & 1u));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tO = tmem + lrow + Cfg::kTmemO;
+                const uint32_t tO = tmem + lrow + Cfg::kTmemO + h * (uint32_t)(D / 2);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t o[32];
                     tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, o);
                     tmem_ld_wait();
@@ -340,20 +419,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
         }
-        // ---- O / l, stored by row.  The TMEM loads are warp-collective: the
-        // whole warp loads (conditions below are warp-uniform); only the stores
-        // depend on the row being a real query.
+        // ---- O / l, stored by row, each half its D / 2 columns.  The TMEM loads
+        // are warp-collective: the whole warp loads (conditions below are
+        // warp-uniform); only the stores depend on the row being a real query.
         if (ok && nkb > 0) {
             ok = __all_sync(0xffffffffu,
                             w(bar(Cfg::kBarODone + ((nkb - 1) & 1)), (((uint32_t)nkb - 1) >> 1) & 1u));
             if (ok) tc_fence_after();
         }
+        if (ok) {   // the row sum is the two halves' sums (the slot after the last block's)
+            const int sb = nkb & 1;
+            const uint32_t xb = bar(Cfg::kBarXch + 2 * (int)q + sb);
+            xch[(sb * 2 + (int)h) * kBQ + r] = l;
+            mbar_arrive_local(xb);
+            ok = __all_sync(0xffffffffu, w(xb, ((uint32_t)nkb >> 1) & 1u));
+            if (ok) l += xch[(sb * 2 + (int)(h ^ 1u)) * kBQ + r];
+        }
         const bool store = i < p.Sq;
-        OutT* orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)bh * p.Sq + (store ? i : 0)) * D;
+        OutT* orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)bh * p.Sq + (store ? i : 0)) * D + h * (D / 2);
         const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-        const uint32_t tO = tmem + lrow + Cfg::kTmemO;
+        const uint32_t tO = tmem + lrow + Cfg::kTmemO + h * (uint32_t)(D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
             uint32_t v[32];
             if (ok && nkb > 0) {
                 tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, v);
