@@ -430,6 +430,10 @@ def test_attention_closed_forms():
     # shifting every key by one vector shifts each query's scores by a constant
     K = rng.standard_normal((Sk, D))
     assert np.allclose(oracle.attention(Q, K + rng.standard_normal(D), V), oracle.attention(Q, K, V), atol=1e-12)
+    # the default scale is 1 / sqrt(D): D = 4, q.k1 = 2 ln 3 gives the score ln 3, weights 1/4 and 3/4
+    q = np.array([[2.0 * np.log(3.0), 0.0, 0.0, 0.0]])
+    k = np.array([[0.0, 0.0, 0.0, 0.0], [1.0, 0.0, 0.0, 0.0]])
+    assert abs(oracle.attention(q, k, np.array([[4.0], [8.0]]))[0, 0] - 7.0) < 1e-14
     # a query that sees no key gets zeros (causal, more queries than keys)
     Oz = oracle.attention(rng.standard_normal((6, D)), K[:3], V[:3], causal=True)
     assert np.array_equal(Oz[:3], np.zeros((3, D))) and np.all(Oz[3:] != 0)
