@@ -157,11 +157,13 @@ bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c, int
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 bool in_is_bf16(int dtype) { return dtype == DT_BF16_F32 || dtype == DT_BF16_BF16; }
-int in_bytes(int dtype) { return dtype_is_fp8(dtype) ? 1 : 2; }
+int in_bytes(int dtype) { return dtype_is_fp8(dtype) ? 1 : (dtype_is_tf32(dtype) ? 4 : 2); }
 int out_bytes(int dtype) {
-    return (dtype == DT_BF16_F32 || dtype == DT_F16_F32 || dtype == DT_E4M3_F32 || dtype == DT_E5M2_F32) ? 4 : 2;
+    return (dtype == DT_BF16_F32 || dtype == DT_F16_F32 || dtype == DT_E4M3_F32 || dtype == DT_E5M2_F32 ||
+            dtype == DT_TF32_F32) ? 4 : 2;
 }
 CUtensorMapDataType in_map_type(int dtype) {
+    if (dtype_is_tf32(dtype)) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;   // fp32 bits, read by the MMA as tf32
     if (dtype_is_fp8(dtype)) return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes, read by the MMA as e4m3 / e5m2
     return in_is_bf16(dtype) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
@@ -170,12 +172,15 @@ CUtensorMapDataType out_map_type(int dtype) {
     return dtype == DT_F16_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-uint32_t make_idesc(int dtype, bool b_mn_major, int mma_m, int mma_n) {
-    // operand format: kind::f16 bf16 = 1 / fp16 = 0; kind::f8f6f4 e5m2 = 1 / e4m3 = 0
-    const uint32_t ab = (in_is_bf16(dtype) || dtype == DT_E5M2_F32 || dtype == DT_E5M2_BF16) ? 1u : 0u;
+uint32_t make_idesc(int dtype, bool b_mn_major, int mma_m, int mma_n, bool a_mn_major = false) {
+    // operand format: kind::f16 bf16 = 1 / fp16 = 0; kind::f8f6f4 e5m2 = 1 / e4m3 = 0;
+    // kind::tf32 tf32 = 2
+    const uint32_t ab = dtype_is_tf32(dtype) ? 2u
+                      : (in_is_bf16(dtype) || dtype == DT_E5M2_F32 || dtype == DT_E5M2_BF16) ? 1u : 0u;
     return (1u << 4)                       // accumulator fp32
          | (ab << 7) | (ab << 10)          // A and B formats
-         | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness (A is always K-major)
+         | ((a_mn_major ? 1u : 0u) << 15)  // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
          | ((uint32_t)(mma_n >> 3) << 17)
          | ((uint32_t)(mma_m >> 4) << 24);
 }
@@ -317,14 +322,14 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
                   int64_t ldb, const void* bias, const void* C, int64_t ldc, int epilogue, int dtype) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
-    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_E5M2_BF16OUT) return GEMM_ERR_INVALID_ARG;
-    if (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST)) return GEMM_ERR_INVALID_ARG;
+    if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_TF32_BF16OUT) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST | GEMM_A_KM)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
     if ((epilogue & GEMM_EPI_BIAS) && bias == nullptr) return GEMM_ERR_INVALID_ARG;
     if (K > 0) {
         if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
-        if (lda < K) return GEMM_ERR_INVALID_ARG;
+        if (lda < ((flags & GEMM_A_KM) ? M : K)) return GEMM_ERR_INVALID_ARG;
         if (ldb < ((flags & GEMM_B_NK) ? K : N)) return GEMM_ERR_INVALID_ARG;
     }
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
@@ -332,7 +337,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
 }
 
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
-    if (plan == nullptr || device < 0 || (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST)))
+    if (plan == nullptr || device < 0 || (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST | GEMM_A_KM)))
         return GEMM_ERR_INVALID_ARG;
     int ndev = 0;
     cudaError_t e = cudaGetDeviceCount(&ndev);
@@ -350,7 +355,7 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     if (e != cudaSuccess) { delete p; return GEMM_ERR_CUDA; }
     if (prop.major * 10 + prop.minor < 100) { delete p; return GEMM_ERR_UNSUPPORTED; }
     p->sm_count = prop.multiProcessorCount;
-    for (int dt = 0; dt < 8; ++dt) {
+    for (int dt = 0; dt < kNumDtypes; ++dt) {
         int n2 = 0, n1 = 0;
         int n4 = 0, unused = 0;
         e = tc_prepare(2, dt, &n2, &n4);
@@ -517,10 +522,10 @@ int extended_epilogue(const gemm_epilogue_args_t* a, int dtype, const void* C, i
 }
 
 // Validated arguments; M, N > 0.  b_nk: B is N x K.  conv: A is the im2col
-// view of an activation tensor (then A and lda are unused).
+// view of an activation tensor (then A and lda are unused).  a_km: A is K x M.
 int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
              int64_t ldb, const void* bias, void* C, int64_t ldc, uint32_t epi, const EpiArgs& ex, int dtype,
-             cudaStream_t stream, const ConvA* conv) {
+             cudaStream_t stream, const ConvA* conv, bool a_km = false) {
     int rc = GEMM_OK;
     cudaError_t e;
 
@@ -533,12 +538,14 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         return GEMM_OK;
     }
 
-    const bool fp8 = dtype_is_fp8(dtype);
-    // fp8: the paired / single-CTA kernel with both operands K-major (B stored N x K)
-    if (fp8 && (!b_nk || conv)) return GEMM_ERR_UNSUPPORTED;
+    // fp8 and tf32: the paired / single-CTA kernel with both operands K-major (B stored N x K)
+    const bool fp8 = dtype_is_fp8(dtype) || dtype_is_tf32(dtype);
+    if (fp8 && (!b_nk || conv || a_km)) return GEMM_ERR_UNSUPPORTED;
+    if (a_km && conv) return GEMM_ERR_UNSUPPORTED;
     int kernel = p->forced_kernel;
-    if (kernel == GEMM_KERNEL_AUTO) kernel = (M <= 128 && !conv && !fp8) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
-    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || fp8)) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_AUTO)
+        kernel = (M <= 128 && !conv && !fp8 && !a_km) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || fp8 || a_km)) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
         return GEMM_ERR_UNSUPPORTED;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
@@ -549,6 +556,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
     const int ob = out_bytes(dtype);
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
+    const int64_t a_rows = a_km ? K : M, a_cols = a_km ? M : K;
     const int es = in_bytes(dtype);                 // element size of A and B
     const int kbk = 128 / es;                       // elements per 128-byte k-block row
     const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
@@ -560,15 +568,16 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     void* C_use = C; int64_t ldc_use = ldc;
     if (!a_ok || !b_ok || !c_ok) {
         if (!p->packing) return GEMM_ERR_ALIGNMENT;
-        const int64_t lda_p = round_up(K, 16 / es), ldb_p = round_up(b_cols, 16 / es), ldc_p = round_up(N, 16 / ob);
-        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(M * lda_p * es, 256);
+        const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es),
+                      ldc_p = round_up(N, 16 / ob);
+        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(a_rows * lda_p * es, 256);
         const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * es, 256);
         const size_t c_bytes = c_ok ? 0 : (size_t)round_up(M * ldc_p * ob, 256);
         rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes);
         if (rc != GEMM_OK) return rc;
         char* ws = static_cast<char*>(p->workspace);
         if (!a_ok) {
-            e = launch_copy2d(A, lda, ws, lda_p, M, K, es, stream);
+            e = launch_copy2d(A, lda, ws, lda_p, a_rows, a_cols, es, stream);
             if (e != cudaSuccess) return record(p, e);
             p->launches += 1;
             A_use = ws; lda_use = lda_p;
@@ -597,6 +606,9 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
             return GEMM_ERR_CUDA;
     } else if (conv) {
         if (!make_im2col_map(&tmA, in_dt, *conv)) return GEMM_ERR_CUDA;
+    } else if (a_km) {   // 64 rows (columns of the M x K operand) per box, two boxes per tile
+        if (!make_map(&tmA, in_dt, A_use, (uint64_t)M, (uint64_t)K, (uint64_t)lda_use * es, 64, TC_BK))
+            return GEMM_ERR_CUDA;
     } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * es, kbk, TC_BM)) {
         return GEMM_ERR_CUDA;
     }
@@ -616,8 +628,9 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     prm.group_m = p->group_m;
     prm.epi = epi;
     prm.ex = ex;
-    prm.idesc = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN);
+    prm.idesc = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN, a_km);
     prm.b_mn_major = b_nk ? 0u : 1u;
+    prm.a_mn_major = a_km ? 1u : 0u;
     prm.bias = bias;
     prm.bias_vec16 = (bias != nullptr && aligned16(bias)) ? 1u : 0u;
     prm.status = p->status_dev;
@@ -648,7 +661,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const int64_t units = tiles < cap ? tiles : cap;
     prm.multicast = mc == 2 ? 1u : 0u;
     prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
-    prm.idesc_half = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN / 2);
+    prm.idesc_half = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN / 2, a_km);
     if (p->debug_log)
         std::fprintf(stderr, "[gemm] tc cta_group=%d mc=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
                      cg, mc, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
@@ -680,7 +693,8 @@ int gemm_run(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int6
     if (M == 0 || N == 0) return GEMM_OK;
     DeviceGuard g(p->device);
     return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, bias, C, ldc, (uint32_t)epilogue,
-                    plain_epilogue(), dtype, reinterpret_cast<cudaStream_t>(stream_v), nullptr);
+                    plain_epilogue(), dtype, reinterpret_cast<cudaStream_t>(stream_v), nullptr,
+                    (p->flags & GEMM_A_KM) != 0);
 }
 
 int gemm_run_ex(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
@@ -695,7 +709,7 @@ int gemm_run_ex(gemm_plan_t p, int64_t M, int64_t N, int64_t K, const void* A, i
     if (M == 0 || N == 0) return GEMM_OK;
     DeviceGuard g(p->device);
     return run_impl(p, (p->flags & GEMM_B_NK) != 0, M, N, K, A, lda, B, ldb, epi->bias, C, ldc, flags, ex, dtype,
-                    reinterpret_cast<cudaStream_t>(stream_v), nullptr);
+                    reinterpret_cast<cudaStream_t>(stream_v), nullptr, (p->flags & GEMM_A_KM) != 0);
 }
 
 int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int64_t Cout, int R, int S, int pad,
@@ -714,7 +728,7 @@ int gemm_conv2d(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t C, int6
     if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
     if (OH < 0 || OW < 0) return GEMM_ERR_INVALID_ARG;
-    if (dtype_is_fp8(dtype)) return GEMM_ERR_UNSUPPORTED;
+    if (dtype_is_fp8(dtype) || dtype_is_tf32(dtype)) return GEMM_ERR_UNSUPPORTED;
     const int64_t M = Nb * OH * OW, N = Cout, K = (int64_t)R * S * C;
     // the weights w[f][r][s][c] are the N x K operand
     int rc = gemm_validate(GEMM_B_NK, M, N, K, x, K, w, K, bias, y, ldy, epilogue, dtype);
@@ -794,7 +808,7 @@ int gemm_conv2d_maxpool(gemm_plan_t p, int64_t Nb, int64_t H, int64_t W, int64_t
     if (Nb < 0 || H < 0 || W < 0 || C < 0 || Cout < 0 || R < 1 || S < 1 || pad < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S + 1;
     if (OH < 0 || OW < 0 || (OH & 1) || (OW & 1)) return GEMM_ERR_INVALID_ARG;   // whole 2 x 2 windows
-    if (dtype_is_fp8(dtype)) return GEMM_ERR_UNSUPPORTED;
+    if (dtype_is_fp8(dtype) || dtype_is_tf32(dtype)) return GEMM_ERR_UNSUPPORTED;
     uint32_t epi = 0;
     EpiArgs ex = plain_epilogue();
     const void* bias = nullptr;

@@ -108,7 +108,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
                                 int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype,
                                 unsigned flags, int* dev_status, void* stream_v) {
     int rc = gemm_validate(flags, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype);
-    if (rc == GEMM_OK && gb300::dtype_is_fp8(dtype)) rc = GEMM_ERR_UNSUPPORTED;   // 16-bit inputs only
+    if (rc == GEMM_OK && (gb300::dtype_is_fp8(dtype) || gb300::dtype_is_tf32(dtype)))
+        rc = GEMM_ERR_UNSUPPORTED;   // 16-bit inputs only
+    if (rc == GEMM_OK && (flags & GEMM_A_KM)) rc = GEMM_ERR_UNSUPPORTED;           // M x K A only
     if (rc != GEMM_OK) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
     const bool b_nk = (flags & GEMM_B_NK) != 0;

@@ -11,9 +11,11 @@ namespace gb300 {
 // inputs (A and B in one format) take bf16 bias and scale vectors.
 enum Dtype : int {
     DT_BF16_F32 = 0, DT_BF16_BF16 = 1, DT_F16_F32 = 2, DT_F16_F16 = 3,
-    DT_E4M3_F32 = 4, DT_E4M3_BF16 = 5, DT_E5M2_F32 = 6, DT_E5M2_BF16 = 7
+    DT_E4M3_F32 = 4, DT_E4M3_BF16 = 5, DT_E5M2_F32 = 6, DT_E5M2_BF16 = 7, DT_TF32_F32 = 8, DT_TF32_BF16 = 9
 };
 constexpr bool dtype_is_fp8(int dt) { return dt >= DT_E4M3_F32 && dt <= DT_E5M2_BF16; }
+constexpr bool dtype_is_tf32(int dt) { return dt == DT_TF32_F32 || dt == DT_TF32_BF16; }
+constexpr int kNumDtypes = 10;
 
 // Epilogue on the fp32 accumulator, in this order: t = alpha * acc (EPI_ALPHA);
 // t *= scale[n] (EPI_SCALE); t += bias[n] (EPI_BIAS); t += beta * C_old[m][n]
@@ -61,6 +63,7 @@ struct TcParams {
     uint32_t epi;          // EpiFlags
     uint32_t idesc;        // tcgen05 instruction descriptor
     uint32_t b_mn_major;   // 1: B is K x N (N contiguous); 0: B is N x K
+    uint32_t a_mn_major;   // 1: A is K x M (M contiguous); 0: A is M x K
     const void* bias;      // N elements of the input type, or null
     uint32_t bias_vec16;   // 1: bias is 16-byte aligned (vector loads allowed)
     int* status;           // device status word (StatusBits)

@@ -144,11 +144,13 @@ cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bi
             break;
         case DT_E4M3_F32:
         case DT_E5M2_F32:
+        case DT_TF32_F32:
             fill_epilogue_kernel<__nv_bfloat16, float><<<blocks, threads, 0, stream>>>(
                 M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const float*)ex.c_old, ex.ldc_old, (float*)C, ldc);
             break;
         case DT_E4M3_BF16:
         case DT_E5M2_BF16:
+        case DT_TF32_BF16:
             fill_epilogue_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, threads, 0, stream>>>(
                 M, N, (const __nv_bfloat16*)bias, epi, ex.beta, (const __nv_bfloat16*)ex.c_old, ex.ldc_old,
                 (__nv_bfloat16*)C, ldc);

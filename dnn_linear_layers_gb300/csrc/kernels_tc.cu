@@ -243,7 +243,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int num_tiles = p.num_m_tiles * p.num_n_tiles;
     const int num_items = p.num_full + 2 * (num_tiles - p.num_full);
     const int nkb = p.num_k_blocks;
-    constexpr int kBk = KIND ? 2 * TC_BK : TC_BK;   // elements per 128-byte k-block row
+    // elements per 128-byte k-block row: 64 16-bit, 128 fp8 or 32 tf32
+    constexpr int kBk = KIND == 1 ? 2 * TC_BK : (KIND == 2 ? TC_BK / 2 : TC_BK);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -304,6 +305,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         } else {
                             if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
                             else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
+                        }
+                    } else if (p.a_mn_major) {
+                        // K x M operand: two boxes of 64 rows (M) x 64 k, 8 KB apart
+                        for (int c = 0; c < 2; ++c) {
+                            if (pair_bar) tma_load_2d_pair(dst + (uint32_t)c * 8192u, &tmA, bar, m0 + 64 * c, k0, pol_a);
+                            else tma_load_2d(dst + (uint32_t)c * 8192u, &tmA, bar, m0 + 64 * c, k0, pol_a);
                         }
                     } else {
                         if (pair_bar) tma_load_2d_pair(dst, &tmA, bar, k0, m0, pol_a);
@@ -397,7 +404,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // K = 32 fp8 elements, 32 bytes of every row each
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        // MN-major operands: 16 k-rows of 128 bytes per MMA, 64-wide
+                        // column boxes 8 KB apart
+                        const uint64_t adesc = p.a_mn_major
+                            ? smem_desc_sw128(sa + kk * (kUmmaK * 128), 8192, 1024)
+                            : smem_desc_sw128(sa + kk * 32, 16, 1024);
                         const uint64_t bdesc = p.b_mn_major
                             ? smem_desc_sw128(sb + kk * (kUmmaK * 128), 8192, 1024)
                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
@@ -738,6 +749,9 @@ cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmA2
         case DT_E5M2_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
         case DT_E4M3_BF16:
         case DT_E5M2_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        // fp32 operands multiplied as tf32; bf16 bias / scale
+        case DT_TF32_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_TF32_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -753,6 +767,8 @@ cudaError_t prepare_dt(int dtype, int* max_units) {
         case DT_E5M2_F32: return prepare_impl<CG, MC, __nv_bfloat16, float, 1>(max_units);
         case DT_E4M3_BF16:
         case DT_E5M2_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(max_units);
+        case DT_TF32_F32: return prepare_impl<CG, MC, __nv_bfloat16, float, 2>(max_units);
+        case DT_TF32_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 2>(max_units);
     }
     return cudaErrorInvalidValue;
 }

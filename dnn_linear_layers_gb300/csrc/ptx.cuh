@@ -243,7 +243,8 @@ __device__ __forceinline__ void tc_fence_after() {
 // D[tmem] (+)= A[smem] * B[smem]; kind::f16 (bf16 or fp16 operands, fp32 accumulate).
 // One tcgen05.mma: D (TMEM) (+)= A (smem) x B (smem).  KIND 0: kind::f16
 // (bf16 / fp16 operands, K = 16); KIND 1: kind::f8f6f4 (e4m3 / e5m2
-// operands, K = 32); both read 32 bytes of every operand row.
+// operands, K = 32); KIND 2: kind::tf32 (fp32 operands taken as tf32, K = 8);
+// each reads 32 bytes of every operand row.
 template <int CG, int KIND = 0>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -258,6 +259,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else if constexpr (CG == 1 && KIND == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else if constexpr (CG == 2 && KIND == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
             :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
     else if constexpr (CG == 1)
         asm volatile(

@@ -18,8 +18,9 @@ LIB_PATH = _PKG / "libgb300gemm.so"
 EPI_NONE, EPI_BIAS, EPI_RELU, EPI_BIAS_RELU = 0, 1, 2, 3
 BF16_F32OUT, BF16_BF16OUT, F16_F32OUT, F16_F16OUT = 0, 1, 2, 3
 E4M3_F32OUT, E4M3_BF16OUT, E5M2_F32OUT, E5M2_BF16OUT = 4, 5, 6, 7
+TF32_F32OUT, TF32_BF16OUT = 8, 9   # fp32 A and B, multiplied at tf32 precision
 FP8_DTYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
-B_KN, B_NK, B_CONST, TC_MULTICAST = 0, 1, 2, 4
+B_KN, B_NK, B_CONST, TC_MULTICAST, A_KM = 0, 1, 2, 4, 8
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
     0, -1, -2, -3, -4, -5, -6)
@@ -99,7 +100,8 @@ def dtype_code(in_dtype: torch.dtype, out_dtype: torch.dtype) -> int:
     table = {(torch.bfloat16, torch.float32): BF16_F32OUT, (torch.bfloat16, torch.bfloat16): BF16_BF16OUT,
              (torch.float16, torch.float32): F16_F32OUT, (torch.float16, torch.float16): F16_F16OUT,
              (torch.float8_e4m3fn, torch.float32): E4M3_F32OUT, (torch.float8_e4m3fn, torch.bfloat16): E4M3_BF16OUT,
-             (torch.float8_e5m2, torch.float32): E5M2_F32OUT, (torch.float8_e5m2, torch.bfloat16): E5M2_BF16OUT}
+             (torch.float8_e5m2, torch.float32): E5M2_F32OUT, (torch.float8_e5m2, torch.bfloat16): E5M2_BF16OUT,
+             (torch.float32, torch.float32): TF32_F32OUT, (torch.float32, torch.bfloat16): TF32_BF16OUT}
     try:
         return table[(in_dtype, out_dtype)]
     except KeyError:
@@ -107,8 +109,8 @@ def dtype_code(in_dtype: torch.dtype, out_dtype: torch.dtype) -> int:
 
 
 def vector_dtype(in_dtype: torch.dtype) -> torch.dtype:
-    """dtype of the bias and scale vectors for an input dtype (bf16 for fp8 inputs)."""
-    return torch.bfloat16 if in_dtype in FP8_DTYPES else in_dtype
+    """dtype of the bias and scale vectors for an input dtype (bf16 for fp8 and fp32 / tf32 inputs)."""
+    return torch.bfloat16 if in_dtype in FP8_DTYPES or in_dtype == torch.float32 else in_dtype
 
 
 def _ld(t: torch.Tensor) -> int:
@@ -126,15 +128,20 @@ def _stream_handle(stream) -> int:
 
 class Plan:
     """Owner of a ``gemm_plan_t``.  ``b_layout`` is "kn" (B is K x N) or "nk"
-    (B is a Linear weight W, N x K)."""
+    (B is a Linear weight W, N x K); ``a_layout`` is "mk" (A is M x K) or "km"
+    (A is stored K x M, the transposed operand)."""
 
     def __init__(self, device: int | torch.device = 0, b_layout: str = "kn", b_const: bool = False,
-                 multicast: bool = False):
+                 multicast: bool = False, a_layout: str = "mk"):
         if isinstance(device, torch.device):
             device = device.index if device.index is not None else torch.cuda.current_device()
         self.device = int(device)
+        if b_layout not in ("kn", "nk") or a_layout not in ("mk", "km"):
+            raise ValueError("b_layout is 'kn' or 'nk', a_layout 'mk' or 'km'")
         self.b_nk = b_layout == "nk"
-        flags = (B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0) | (TC_MULTICAST if multicast else 0)
+        self.a_km = a_layout == "km"
+        flags = ((B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0) | (TC_MULTICAST if multicast else 0)
+                 | (A_KM if self.a_km else 0))
         h = _vp()
         _check(lib().gemm_plan_create(ctypes.byref(h), self.device, flags), "gemm_plan_create")
         self._h = h
@@ -199,7 +206,7 @@ class Plan:
             scale: torch.Tensor | None = None):
         """C = relu?(alpha * (A . B) * scale + bias + beta * C), written into the
         caller's C (gemm_run, or gemm_run_ex when alpha, beta or scale is set)."""
-        M, K = A.shape
+        M, K = (A.shape[1], A.shape[0]) if self.a_km else (A.shape[0], A.shape[1])
         N = B.shape[0] if self.b_nk else B.shape[1]
         if (B.shape[1] if self.b_nk else B.shape[0]) != K or tuple(C.shape) != (M, N):
             raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} C {tuple(C.shape)}")

@@ -63,7 +63,11 @@ typedef enum {
  * section 2.7: fewer bytes per operand, fp32 accumulation) take bf16 bias and
  * scale vectors, need B stored N x K (plan flag GEMM_B_NK: both operands
  * K-major) and always run on the large-M kernels; per-tensor scale factors go
- * in gemm_run_ex's alpha. */
+ * in gemm_run_ex's alpha.  The tf32 types take fp32 A and B in memory, which
+ * the tensor cores multiply at tf32 precision (8-bit exponent, 10-bit
+ * mantissa; CMU 15-418 notes, section 2.7), with fp32 accumulation; like fp8
+ * they take bf16 bias and scale vectors, need GEMM_B_NK and run on the
+ * large-M kernels. */
 typedef enum {
     GEMM_BF16_F32OUT = 0,
     GEMM_BF16_BF16OUT = 1,
@@ -72,7 +76,9 @@ typedef enum {
     GEMM_E4M3_F32OUT = 4,
     GEMM_E4M3_BF16OUT = 5,
     GEMM_E5M2_F32OUT = 6,
-    GEMM_E5M2_BF16OUT = 7
+    GEMM_E5M2_BF16OUT = 7,
+    GEMM_TF32_F32OUT = 8,
+    GEMM_TF32_BF16OUT = 9
 } gemm_dtype_t;
 
 /* Plan flags. */
@@ -88,6 +94,11 @@ typedef enum {
  * reads from L2; on GB300 it lowers power but was not faster at the sizes
  * measured, so it is off by default). */
 #define GEMM_TC_MULTICAST 4u
+/* A is stored K x M (the transpose of the M x K operand, BLAS "transa"):
+ * A(i, k) = A[k * lda + i], lda >= M.  Runs on the tensor-core kernels (also for
+ * M <= 128); 16-bit inputs only (fp8 operands must be K-major: refused with
+ * GEMM_ERR_UNSUPPORTED); not taken by gemm_run_noalloc. */
+#define GEMM_A_KM 8u
 
 /* Kernel selection (gemm_plan_set_kernel / gemm_plan_last_kernel). */
 #define GEMM_KERNEL_AUTO 0
@@ -125,7 +136,7 @@ typedef struct {
 } gemm_epilogue_args_t;
 
 /* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK,
- * optionally | GEMM_B_CONST and | GEMM_TC_MULTICAST.
+ * optionally | GEMM_A_KM, | GEMM_B_CONST and | GEMM_TC_MULTICAST.
  * Allocates the plan and its device status word; restores the caller's
  * current device before returning.  *plan is set only on success. */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);

@@ -61,9 +61,14 @@ def test_validate_rejects_bad_arguments(lib):
     assert val(M=-1) == G.ERR_INVALID_ARG
     assert val(K=-5) == G.ERR_INVALID_ARG
     assert val(epi=4) == G.ERR_INVALID_ARG
-    assert val(dtype=9) == G.ERR_INVALID_ARG
-    assert val(flags=8) == G.ERR_INVALID_ARG
+    assert val(dtype=10) == G.ERR_INVALID_ARG
+    assert val(dtype=G.TF32_F32OUT) == G.OK and val(dtype=G.TF32_BF16OUT) == G.OK
+    assert val(flags=16) == G.ERR_INVALID_ARG
     assert val(flags=G.TC_MULTICAST) == G.OK
+    # A stored K x M: lda counts M
+    assert val(flags=G.A_KM, M=96, K=32, lda=96, ldc=64) == G.OK
+    assert val(flags=G.A_KM, M=96, K=32, lda=95, ldc=64) == G.ERR_INVALID_ARG    # lda < M
+    assert val(flags=G.A_KM, M=32, K=96, lda=32, ldc=64) == G.OK                 # lda < K is fine here
     assert val(flags=G.B_NK | G.B_CONST, N=32, ldb=64, ldc=32) == G.OK
     assert val(lda=63) == G.ERR_INVALID_ARG               # lda < K
     assert val(ldb=63) == G.ERR_INVALID_ARG               # ldb < N (K x N layout)
