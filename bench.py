@@ -58,6 +58,10 @@ WORKLOADS = {
     # fp8 operands (both K-major: B stored N x K), bf16 output
     "square8192_e4m3": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
     "square8192_e5m2": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
+    # fp32 operands multiplied at tf32 precision (B stored N x K), bf16 output
+    "square8192_tf32": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
+    # A stored K x M (the transposed operand, plan flag GEMM_A_KM)
+    "square8192_transa_bf16": (8192, 8192, 8192, "kn", (False, False), "bf16", 1.0, 1.0),
     "odd_4095": (4095, 4095, 4095, "kn", (False, False), "bf16", 1.0, 1.0),
     "odd_1000": (1000, 1000, 1000, "kn", (False, False), "bf16", 1.0, 1.0),
     # decode-like Linear layers: W stored out x in, bias, M tokens
@@ -182,8 +186,14 @@ class ClockSampler:
 
 
 def fp8_dtype(name):
+    """torch dtype of a workload's operands when they are not 16-bit (fp8, or fp32 read as tf32)."""
     import torch
-    return {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}.get(name.rsplit("_", 1)[-1])
+    return {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2,
+            "tf32": torch.float32}.get(name.rsplit("_", 1)[-1])
+
+
+# nominal dense tensor rate of each operand type relative to bf16 (fp8 4.5 / 2.25, tf32 1.1 / 2.25)
+PEAK_RATIO = {"e4m3": 2.0, "e5m2": 2.0, "tf32": 1.1 / 2.25}
 
 
 ATTN_SHAPE = (4, 32, 4096, 128)   # B, H, S, D
@@ -207,9 +217,17 @@ def make_inputs(name, device, seed=0):
         kv = torch.stack([normal_bf16((B, H, S, D), 3 * seed + 1), normal_bf16((B, H, S, D), 3 * seed + 2)])
         return q, kv, None
     f8 = fp8_dtype(name)
+    if f8 is not None and name.endswith("_tf32"):   # N(0,1) fp32
+        A = normal_bf16((M, K), 3 * seed, a_std, dtype=torch.float32)
+        B = normal_bf16((N, K), 3 * seed + 1, b_std, dtype=torch.float32)
+        return A, B, None
     if f8 is not None:   # N(0,1) drawn as bf16, then rounded to the fp8 format
         A = normal_bf16((M, K), 3 * seed, a_std).to(f8)
         B = normal_bf16((N, K), 3 * seed + 1, b_std).to(f8)
+        return A, B, None
+    if "_transa_" in name:   # A as stored: K x M
+        A = normal_bf16((K, M), 3 * seed, a_std)
+        B = normal_bf16((N, K) if lay == "nk" else (K, N), 3 * seed + 1, b_std)
         return A, B, None
     if name.startswith(("conv_implicit", "conv_pool")):
         # x (NHWC 32x56x56x256, ReLU(N(0,1))) and w[f][r][s][c] as they are
@@ -255,7 +273,7 @@ def run_ours(args):
     C = (torch.empty(tuple(A.shape), dtype=torch.bfloat16, device=dev) if attn else
          torch.empty((M // 4 if pool else M, N), dtype=torch.bfloat16, device=dev))
     # Linear-layer weights are constant model parameters: say so to the plan
-    plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"))
+    plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"), a_layout="km" if "_transa_" in name else "mk")
     if args.kernel != "auto":
         plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
@@ -267,7 +285,7 @@ def run_ours(args):
     elif conv:   # activations, weights and output once each (no im2col matrix exists)
         nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2 + (N * 2 if has_bias else 0))
     else:
-        es = 1 if f8 is not None else 2
+        es = A.element_size()
         nbytes_step = R.gemm_bytes(M, N, K, es, es, 2, 2 if has_bias else 0)
     # Workloads smaller than twice the L2 rotate through enough copies of their
     # operands that each step reads HBM, not the previous step's L2 lines.
@@ -392,14 +410,15 @@ def run_ours(args):
 
     peaks, src = R.load_peaks()
     nbytes = nbytes_step
-    # an fp8 contraction takes the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
-    t_peak = peaks["bf16_tflops"] * (2.0 if f8 is not None else 1.0)
+    # an fp8 or tf32 contraction takes the measured bf16 peak times the nominal ratio of the two rates
+    kind = name.rsplit("_", 1)[-1]
+    t_peak = peaks["bf16_tflops"] * (PEAK_RATIO[kind] if f8 is not None else 1.0)
     t_roof = R.roofline_time(flops, nbytes, t_peak * 1e12, peaks["hbm_gbs"] * 1e9)
     tensor_bound = flops / (t_peak * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9)
     if tensor_bound:
         achieved, peak, r_unit = flops / (kernel_ms * 1e-3) / 1e12, t_peak, "TFLOP/s"
-        peak_src = ("MEASURED_PEAKS.json bf16_tflops (burst) x 2, the nominal fp8 / bf16 ratio" if f8 is not None
-                    else "MEASURED_PEAKS.json bf16_tflops (burst)")
+        peak_src = (f"MEASURED_PEAKS.json bf16_tflops (burst) x {PEAK_RATIO[kind]:.4g}, the nominal {kind} / bf16 "
+                    "ratio" if f8 is not None else "MEASURED_PEAKS.json bf16_tflops (burst)")
     else:
         achieved, peak, r_unit = nbytes / (kernel_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_src = "MEASURED_PEAKS.json hbm_gbs"
@@ -412,13 +431,14 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": name.rsplit("_", 1)[-1] if f8 is not None else "bf16",
-            "data": ("synthetic: N(0,1) drawn as bf16 (torch CPU generator, fixed seeds), rounded to "
-                     f"{name.rsplit('_', 1)[-1]}, resident in HBM" if f8 is not None else
+            "data": ("synthetic: N(0,1) fp32 (torch CPU generator, fixed seeds), resident in HBM" if kind == "tf32"
+                     else "synthetic: N(0,1) drawn as bf16 (torch CPU generator, fixed seeds), rounded to "
+                     f"{kind}, resident in HBM" if f8 is not None else
                      "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM"),
             "config": {"workload": name,
                        **({"B": ATTN_SHAPE[0], "H": ATTN_SHAPE[1], "Sq": ATTN_SHAPE[2], "Sk": ATTN_SHAPE[2],
                            "D": ATTN_SHAPE[3], "causal": "causal" in name, "scale": "1/sqrt(D)"} if attn else
-                          {"M": M, "N": N, "K": K, "b_layout": lay,
+                          {"M": M, "N": N, "K": K, "b_layout": lay, "a_layout": "km" if "_transa_" in name else "mk",
                            "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none"}),
                        "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
                        "l2": (f"inputs larger than L2 ({nbytes / 1e6:.1f} MB > {l2 / 1e6:.0f} MB), no flush"
@@ -484,6 +504,8 @@ def _oracle_rows_timer(name, A, B, bias):
 
         return run_conv, 1
     Af = oracle._f64(A); Bf = oracle._f64(B)   # fp8 bytes decoded by the oracle's own decoders
+    if "_transa_" in name:                      # A is stored K x M
+        Af = np.ascontiguousarray(Af.T)
     bf = bias.double().numpy() if bias is not None else None
     rng = np.random.default_rng(0)
 
