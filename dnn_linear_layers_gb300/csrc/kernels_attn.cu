@@ -18,13 +18,14 @@
 //     instruction is accepted only as the tensor pipe drains, so one thread
 //     issuing both products would leave the pipe idle while it waited for the
 //     other's operands; two threads keep it fed from whichever is ready;
-//   * warps 3..10: softmax, two threads per query row (TMEM lane), one per
-//     half of the 128 keys (and of the D accumulator columns), so two warps
-//     share each SM sub-partition and hide each other's latency; the halves
-//     swap their block maxima through shared memory behind a (bounded)
-//     mbarrier and keep partial row sums until the end.  Each thread reads its
-//     64 scores from TMEM once (the score buffer is handed back at once),
-//     P = 2^(s - m) is written
+//   * warps 3..10: softmax in two groups of four warps that take the key blocks
+//     in turn (group 0 the even ones, group 1 the odd ones), one thread per
+//     query row (TMEM lane) in each, so the two warps that share an SM
+//     sub-partition work on different blocks and hide each other's latency.
+//     A row's reference max passes from group to group once per block through
+//     shared memory behind a (bounded) mbarrier; each group keeps a partial
+//     row sum until the end.  Each thread reads its 128 scores from TMEM once
+//     (the score buffer is handed back at once), P = 2^(s - m) is written
 //     as bf16 / fp16 into one of two 128-byte-swizzled shared-memory tiles
 //     (the A operand of the PV product; two, so P_j is written while P_{j-1} V
 //     runs).  The reference max m of a row moves only when the block max
@@ -58,7 +59,7 @@ struct AttnCfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffP = kOffV + kStages * kKVBytes;   // two P tiles
     static constexpr int kOffMisc = kOffP + 2 * kPBytes;
-    static constexpr int kOffXch = 256;   // in misc: float [2 slots][2 halves][128 rows]
+    static constexpr int kOffXch = 256;   // in misc: float hand-off [2 groups][128 rows], sums [2][128]
     static constexpr int kMiscBytes = kOffXch + 2 * 2 * kBQ * 4;
     // the tiles want 1024-byte alignment; a window starting at a multiple of
     // 256 bytes fits (the kernel checks, and stops with a status bit if not)
@@ -67,8 +68,9 @@ struct AttnCfg {
     // barriers (8 bytes each) in the misc region; pairs are indexed by buffer
     static constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarSFull = 9,
                          kBarSFree = 11, kBarPFull = 13, kBarODone = 15, kBarDone = 17,
-                         kBarXch = 18,   // [4 lane quarters][2 slots]
-                         kAbort = 26 * 8, kTmemPtr = kAbort + 4;
+                         kBarHand = 18,  // [4 lane quarters][2 groups]: a group published its max
+                         kBarFin = 26,   // [4 lane quarters]: both groups wrote their row sums
+                         kAbort = 30 * 8, kTmemPtr = kAbort + 4;
     static constexpr int kTmemS = 0;      // two score buffers: columns 0..127 and 128..255
     static constexpr int kTmemO = 256;    // accumulator: columns 256 .. 256 + D - 1
     static_assert(kTmemPtr + 4 <= kOffXch, "misc layout");
@@ -191,11 +193,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(Cfg::kBarKEmpty + s), 1);
             mbar_init(bar(Cfg::kBarVEmpty + s), 1);
             mbar_init(bar(Cfg::kBarSFull + s), 1);
-            mbar_init(bar(Cfg::kBarSFree + s), 8);   // the eight softmax warps
-            mbar_init(bar(Cfg::kBarPFull + s), 8);
+            mbar_init(bar(Cfg::kBarSFree + s), 4);   // the four warps of the group that owns buffer s
+            mbar_init(bar(Cfg::kBarPFull + s), 4);
             mbar_init(bar(Cfg::kBarODone + s), 1);
         }
-        for (int x = 0; x < 8; ++x) mbar_init(bar(Cfg::kBarXch + x), 64);   // both warps of a quarter
+        for (int x = 0; x < 8; ++x) mbar_init(bar(Cfg::kBarHand + x), 32);   // one warp
+        for (int x = 0; x < 4; ++x) mbar_init(bar(Cfg::kBarFin + x), 64);    // both groups' warps of a quarter
         mbar_init(bar(Cfg::kBarDone), 2);   // the two MMA issuers
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
@@ -300,65 +303,76 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_commit_1(bar(Cfg::kBarDone));
         }
     } else {
-        // ---- softmax warps: thread = query row r (TMEM lane 32 q + lane), key half h
+        // ---- softmax warps: thread = query row r (TMEM lane 32 q + lane); group g
+        // takes key blocks j = g, g + 2, .. into score buffer and P tile g
         const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const uint32_t q = warp & 3u;
-        const uint32_t h = (warp - 3u) >> 2;
+        const int g = (int)((warp - 3u) >> 2);
         const int r = 32 * (int)q + (int)lane;
         const int i = q0 + r;                              // query index
         const int lim = p.causal ? i + (p.Sk - p.Sq) : p.Sk - 1;   // last visible key
         const uint32_t lrow = (32u * q) << 16;             // TMEM lane offset of this warp
-        volatile float* const xch = reinterpret_cast<volatile float*>(base_ptr + Cfg::kOffMisc + Cfg::kOffXch);
+        volatile float* const hand = reinterpret_cast<volatile float*>(base_ptr + Cfg::kOffMisc + Cfg::kOffXch);
+        volatile float* const sums = hand + 2 * kBQ;
         const float c2 = p.scale_log2;
-        float m = -INFINITY, l = 0.0f;                     // reference max (base 2), this half's row sum
+        // m: the row's reference max (base 2) as last known here; l: this group's
+        // share of the row sum, relative to m
+        float m = -INFINITY, l = 0.0f;
+        // the factor that moves sums from reference m_old to m_new (1 when equal)
+        auto factor = [](float m_old, float m_new) { return m_new == m_old ? 1.0f : ex2_approx(m_old - m_new); };
         bool ok = true;
-        for (int j = 0; j < nkb && ok; ++j) {
-            const int sb = j & 1;
+        for (int j = g; j < nkb && ok; j += 2) {
+            const int sb = g;
             const uint32_t ph = ((uint32_t)j >> 1) & 1u;
             ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ph));
             if (!ok) break;
             tc_fence_after();
-            uint32_t v[2][32];
-            const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u + h * 64u;
-            tmem_ld_32x32b_x32(tS, v[0]);
-            tmem_ld_32x32b_x32(tS + 32u, v[1]);
+            uint32_t v[4][32];
+            const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v[c]);
             tmem_ld_wait();
             // the scores are in registers: the buffer is free for S_{j+2}
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
-            const int k0 = j * kBKey + 64 * (int)h;
-            if (!__all_sync(0xffffffffu, k0 + 63 <= lim)) {   // a block on the mask's edge
+            const int k0 = j * kBKey;
+            if (!__all_sync(0xffffffffu, k0 + kBKey - 1 <= lim)) {   // a block on the mask's edge
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
                         if (k0 + 32 * c + t > lim) v[c][t] = __float_as_uint(-INFINITY);
             }
-            // max of this half's raw scores, scaled once (the scale is positive)
+            // block max of the raw scores, scaled once (the scale is positive)
             float mp[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) mp[t] = __uint_as_float(v[0][t]);
 #pragma unroll
-            for (int x = 8; x < 64; x += 16)
+            for (int x = 8; x < 128; x += 16)
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
                     mp[t] = fmax3(mp[t], __uint_as_float(v[(x + t) >> 5][(x + t) & 31]),
                                   __uint_as_float(v[(x + 8 + t) >> 5][(x + 8 + t) & 31]));
-            const float mh = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7])) * c2;
-            // the block max of the row: both halves take the max of the same two values
-            const uint32_t xb = bar(Cfg::kBarXch + 2 * (int)q + sb);
-            xch[(sb * 2 + (int)h) * kBQ + r] = mh;
-            mbar_arrive_local(xb);
-            ok = __all_sync(0xffffffffu, w(xb, ph));
-            if (!ok) break;
-            const float mx = fmaxf(mh, xch[(sb * 2 + (int)(h ^ 1u)) * kBQ + r]);
+            const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7])) * c2;
+            // the reference max after block j - 1, from the other group
+            if (j >= 1) {
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarHand + 2 * (int)q + (g ^ 1)), ((uint32_t)(j - 1) >> 1) & 1u));
+                if (!ok) break;
+                const float mh = hand[(g ^ 1) * kBQ + r];
+                l *= factor(m, mh);
+                m = mh;
+            }
             const bool grow = mx > m + 8.0f;      // false while nothing is visible
             float alpha = 1.0f;
             if (grow) {
                 alpha = ex2_approx(m - mx);       // 0 on the row's first visible block
                 m = mx;
+                l *= alpha;
             }
+            // pass the reference on to block j + 1
+            hand[g * kBQ + r] = m;
+            mbar_arrive_local(bar(Cfg::kBarHand + 2 * (int)q + g));
             const float mu = (m == -INFINITY) ? 0.0f : m;
             // P_j goes into the tile that P_{j-2} V_{j-2} read
             if (j >= 2) {
@@ -366,14 +380,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!ok) break;
                 tc_fence_after();
             }
-            // P = 2^(s - m) as 16-bit into this half's box of the swizzled A tile
-            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + h * (uint32_t)kBox + (uint32_t)r * 128u;
+            // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
+            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
             const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
             uint64_t sp[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) sp[t] = f2_pack(0.0f, 0.0f);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 float e[32];
 #pragma unroll
                 for (int t = 0; t < 32; t += 2) {   // s * scale - m for two keys at once
@@ -383,27 +397,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     e[t + 1] = ex2_approx(x1);
                     sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(e[t], e[t + 1]));
                 }
-                // keys 32 c .. 32 c + 31 of the half: 16-byte pieces 4 c .. 4 c + 3
+                // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
+                const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t piece = (uint32_t)(4 * c + t) ^ ((uint32_t)r & 7u);
-                    st_shared_v4u(prow + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
+                    const uint32_t piece = (uint32_t)(4 * (c & 1) + t) ^ ((uint32_t)r & 7u);
+                    st_shared_v4u(box + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
                                   pack2<InT>(e[8 * t + 2], e[8 * t + 3]), pack2<InT>(e[8 * t + 4], e[8 * t + 5]),
                                   pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
                 }
             }
             float s0, s1;
             f2_unpack(f2_add(f2_add(sp[0], sp[1]), f2_add(sp[2], sp[3])), s0, s1);
-            l = l * alpha + (s0 + s1);
-            // a row whose reference max moved rescales its half of the accumulator
-            // row, once P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
+            l += s0 + s1;
+            // a row whose reference max moved rescales its accumulator row, once
+            // P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
             if (j >= 1 && __any_sync(0xffffffffu, grow)) {
                 ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (sb ^ 1)), (((uint32_t)j - 1) >> 1) & 1u));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tO = tmem + lrow + Cfg::kTmemO + h * (uint32_t)(D / 2);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
+                const uint32_t tO = tmem + lrow + Cfg::kTmemO;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, o);
                     tmem_ld_wait();
@@ -419,7 +434,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
         }
-        // ---- O / l, stored by row, each half its D / 2 columns.  The TMEM loads
+        // ---- the row sum: the group that did not take the last block brings its
+        // share to the final reference, then the two shares are added
+        if (ok && nkb > 0) {
+            const int g_last = (nkb - 1) & 1;
+            if (g != g_last && nkb >= 2) {
+                ok = __all_sync(0xffffffffu,
+                                w(bar(Cfg::kBarHand + 2 * (int)q + g_last), ((uint32_t)(nkb - 1) >> 1) & 1u));
+                if (ok) l *= factor(m, hand[g_last * kBQ + r]);
+            }
+        }
+        if (ok && nkb > 0) {
+            sums[g * kBQ + r] = l;
+            mbar_arrive_local(bar(Cfg::kBarFin + (int)q));
+            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarFin + (int)q), 0u));
+            if (ok) l = sums[r] + sums[kBQ + r];
+        }
+        // ---- O / l, stored by row, each group its D / 2 columns.  The TMEM loads
         // are warp-collective: the whole warp loads (conditions below are
         // warp-uniform); only the stores depend on the row being a real query.
         if (ok && nkb > 0) {
@@ -427,18 +458,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                             w(bar(Cfg::kBarODone + ((nkb - 1) & 1)), (((uint32_t)nkb - 1) >> 1) & 1u));
             if (ok) tc_fence_after();
         }
-        if (ok) {   // the row sum is the two halves' sums (the slot after the last block's)
-            const int sb = nkb & 1;
-            const uint32_t xb = bar(Cfg::kBarXch + 2 * (int)q + sb);
-            xch[(sb * 2 + (int)h) * kBQ + r] = l;
-            mbar_arrive_local(xb);
-            ok = __all_sync(0xffffffffu, w(xb, ((uint32_t)nkb >> 1) & 1u));
-            if (ok) l += xch[(sb * 2 + (int)(h ^ 1u)) * kBQ + r];
-        }
         const bool store = i < p.Sq;
-        OutT* orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)bh * p.Sq + (store ? i : 0)) * D + h * (D / 2);
+        OutT* orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)bh * p.Sq + (store ? i : 0)) * D + g * (D / 2);
         const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-        const uint32_t tO = tmem + lrow + Cfg::kTmemO + h * (uint32_t)(D / 2);
+        const uint32_t tO = tmem + lrow + Cfg::kTmemO + (uint32_t)g * (uint32_t)(D / 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             uint32_t v[32];
