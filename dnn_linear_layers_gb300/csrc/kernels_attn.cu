@@ -59,21 +59,24 @@ struct AttnCfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffP = kOffV + kStages * kKVBytes;   // two P tiles
     static constexpr int kOffMisc = kOffP + 2 * kPBytes;
-    static constexpr int kOffXch = 256;   // in misc: float hand-off [2 groups][128 rows], sums [2][128]
-    static constexpr int kMiscBytes = kOffXch + 2 * 2 * kBQ * 4;
+    // misc: 32 barriers (8 bytes each), then float hand-off [2 groups][128 rows],
+    // the abort flag and the TMEM address
+    static constexpr int kOffHand = 256;
+    static constexpr int kAbort = kOffHand + 2 * kBQ * 4, kTmemPtr = kAbort + 4;
+    static constexpr int kMiscBytes = kTmemPtr + 12;
     // the tiles want 1024-byte alignment; a window starting at a multiple of
     // 256 bytes fits (the kernel checks, and stops with a status bit if not)
     static constexpr int kSlack = 768;
     static constexpr int kSmem = kOffMisc + kMiscBytes + kSlack;
-    // barriers (8 bytes each) in the misc region; pairs are indexed by buffer
-    static constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarSFull = 9,
-                         kBarSFree = 11, kBarPFull = 13, kBarODone = 15, kBarDone = 17,
-                         kBarHand = 18,  // [4 lane quarters][2 groups]: a group published its max
-                         kBarFin = 26,   // [4 lane quarters]: both groups wrote their row sums
-                         kAbort = 30 * 8, kTmemPtr = kAbort + 4;
+    // barriers; pairs are indexed by buffer (global block index & 1)
+    static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarK = 2, kBarV = 4, kBarKEmpty = 6, kBarVEmpty = 8,
+                         kBarSFull = 10, kBarSFree = 12, kBarPFull = 14, kBarODone = 16, kBarDone = 18,
+                         kBarOFree = 19,   // the item's O has been read out of TMEM
+                         kBarHand = 20,    // [4 lane quarters][2 groups]: a group published a row max
+                         kBarFin = 28;     // [4 lane quarters]: the other group's share of the row sums is in
     static constexpr int kTmemS = 0;      // two score buffers: columns 0..127 and 128..255
     static constexpr int kTmemO = 256;    // accumulator: columns 256 .. 256 + D - 1
-    static_assert(kTmemPtr + 4 <= kOffXch, "misc layout");
+    static_assert(32 * 8 <= kOffHand, "misc layout");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -162,6 +165,26 @@ __device__ __forceinline__ int key_blocks(const AttnParams& p, int q0) {
     return min(all, j_last / kBKey + 1);
 }
 
+// Work items of the persistent CTAs: 128 queries of one head each.  The query
+// blocks of a head are consecutive items (CTAs working at the same time share
+// that head's K and V in L2), taken in the order Q-1, 0, Q-2, 1, ... (Q blocks
+// per head).  Under a causal mask block qb sees qb + 1 key blocks, so a CTA
+// takes items in pairs: a pair costs about Q + 1 whatever it is, and the CTAs
+// get even shares; otherwise every item costs the same and CTAs take them one
+// by one.  Step `step` of CTA `cta` among `ctas`:
+__device__ __forceinline__ int attn_item_index(bool paired, int cta, int ctas, int step) {
+    return paired ? 2 * (cta + (step >> 1) * ctas) + (step & 1) : cta + step * ctas;
+}
+struct AttnItem {
+    int bh, q0, nkb;
+};
+__device__ __forceinline__ AttnItem attn_item(const AttnParams& p, int qblocks, int item) {
+    const int bh = item / qblocks;
+    const int k = item - bh * qblocks;
+    const int qb = (k & 1) ? (k >> 1) : qblocks - 1 - (k >> 1);
+    return {bh, qb * kBQ, key_blocks(p, qb * kBQ)};
+}
+
 template <int D, typename InT, typename OutT>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -181,12 +204,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_LAYOUT);
         return;
     }
-    const int bh = (int)blockIdx.y;
-    const int q0 = (int)blockIdx.x * kBQ;
-    const int nkb = key_blocks(p, q0);
+    const int qblocks = (p.Sq + kBQ - 1) / kBQ;
+    const int items = p.BH * qblocks;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(Cfg::kBarQ), 1);
+        mbar_init(bar(Cfg::kBarQFull), 1);
+        mbar_init(bar(Cfg::kBarQEmpty), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(Cfg::kBarK + s), 1);
             mbar_init(bar(Cfg::kBarV + s), 1);
@@ -197,9 +220,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(Cfg::kBarPFull + s), 4);
             mbar_init(bar(Cfg::kBarODone + s), 1);
         }
+        mbar_init(bar(Cfg::kBarDone), 2);    // the two MMA issuers
+        mbar_init(bar(Cfg::kBarOFree), 4);   // the four warps of the group that writes O out
         for (int x = 0; x < 8; ++x) mbar_init(bar(Cfg::kBarHand + x), 32);   // one warp
-        for (int x = 0; x < 4; ++x) mbar_init(bar(Cfg::kBarFin + x), 64);    // both groups' warps of a quarter
-        mbar_init(bar(Cfg::kBarDone), 2);   // the two MMA issuers
+        for (int x = 0; x < 4; ++x) mbar_init(bar(Cfg::kBarFin + x), 32);    // one warp
         *abort_flag = 0;
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmQ);
@@ -215,60 +239,90 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Every role walks the same items in the same order.  Barrier phases follow
+    // global counters: gb numbers the key blocks of all items this CTA has
+    // taken (buffer gb & 1), qi / oi the items that have key blocks.
     if (warp == 0) {
-        if (lane == 0 && nkb > 0) {
+        // ---- TMA producer
+        if (lane == 0) {
             const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_PRODUCER};
             const uint64_t pol_q = l2_policy_evict_normal();
             const uint64_t pol_kv = l2_policy_evict_last();   // read by every query block of the head
-            mbar_arrive_expect_tx(bar(Cfg::kBarQ), Cfg::kQBytes);
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b)
-                tma_load_3d(base + Cfg::kOffQ + b * kBox, &tmQ, bar(Cfg::kBarQ), 64 * b, q0, bh, pol_q);
-            // block j of K or V: one 128-key box per 64 columns
-            auto load_kv = [&](const CUtensorMap* map, int off, int barid, int j) {
-                const int s = j & 1;
-                mbar_arrive_expect_tx(bar(barid + s), Cfg::kKVBytes);
+            uint32_t qi = 0;
+            int gb0 = 0;
+            bool ok = true;
+            for (int step = 0, item; ok && (item = attn_item_index(p.causal != 0u, (int)blockIdx.x, (int)gridDim.x, step)) < items; ++step) {
+                const AttnItem it = attn_item(p, qblocks, item);
+                if (it.nkb == 0) continue;
+                // Q: its tile frees once the previous item's last score product is done
+                ok = w(bar(Cfg::kBarQEmpty), (qi & 1u) ^ 1u);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(Cfg::kBarQFull), Cfg::kQBytes);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(base + off + s * Cfg::kKVBytes + b * kBox, map, bar(barid + s), 64 * b, j * kBKey, bh,
-                                pol_kv);
-            };
-            // order K_0, K_1, V_0, K_2, V_1, ...: slot j & 1 of K frees when S_{j-2}
-            // is done, that of V when P_{j-2} V_{j-2} is
-            if (w(bar(Cfg::kBarKEmpty), 1u)) {
-                load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, 0);
-                for (int j = 0; j < nkb; ++j) {
-                    if (j + 1 < nkb) {
-                        const int jn = j + 1;
-                        if (!w(bar(Cfg::kBarKEmpty + (jn & 1)), (((uint32_t)jn >> 1) & 1u) ^ 1u)) break;
-                        load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, jn);
+                    tma_load_3d(base + Cfg::kOffQ + b * kBox, &tmQ, bar(Cfg::kBarQFull), 64 * b, it.q0, it.bh, pol_q);
+                ++qi;
+                // block j (global gb) of K or V: one 128-key box per 64 columns
+                auto load_kv = [&](const CUtensorMap* map, int off, int barid, int gb, int j) {
+                    const int s = gb & 1;
+                    mbar_arrive_expect_tx(bar(barid + s), Cfg::kKVBytes);
+#pragma unroll
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(base + off + s * Cfg::kKVBytes + b * kBox, map, bar(barid + s), 64 * b,
+                                    j * kBKey, it.bh, pol_kv);
+                };
+                // order K_0, K_1, V_0, K_2, V_1, ...: a K slot frees when the score
+                // product two blocks back is done, a V slot when that PV product is
+                ok = w(bar(Cfg::kBarKEmpty + (gb0 & 1)), (((uint32_t)gb0 >> 1) & 1u) ^ 1u);
+                if (!ok) break;
+                load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gb0, 0);
+                for (int j = 0; j < it.nkb && ok; ++j) {
+                    if (j + 1 < it.nkb) {
+                        const int gn = gb0 + j + 1;
+                        ok = w(bar(Cfg::kBarKEmpty + (gn & 1)), (((uint32_t)gn >> 1) & 1u) ^ 1u);
+                        if (!ok) break;
+                        load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gn, j + 1);
                     }
-                    if (!w(bar(Cfg::kBarVEmpty + (j & 1)), (((uint32_t)j >> 1) & 1u) ^ 1u)) break;
-                    load_kv(&tmV, Cfg::kOffV, Cfg::kBarV, j);
+                    const int gb = gb0 + j;
+                    ok = w(bar(Cfg::kBarVEmpty + (gb & 1)), (((uint32_t)gb >> 1) & 1u) ^ 1u);
+                    if (!ok) break;
+                    load_kv(&tmV, Cfg::kOffV, Cfg::kBarV, gb, j);
                 }
+                gb0 += it.nkb;
             }
         }
     } else if (warp == 1) {
-        // ---- S issuer: S_j = Q K_j^T into score buffer j & 1
-        if (lane == 0 && nkb > 0) {
+        // ---- S issuer: S_j = Q K_j^T into score buffer gb & 1
+        if (lane == 0) {
             const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
-            bool ok = w(bar(Cfg::kBarQ), 0);
-            const uint32_t tS = tmem + Cfg::kTmemS;
-            for (int j = 0; j < nkb && ok; ++j) {
-                const int s = j & 1;
-                ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)j >> 1) & 1u) ^ 1u) &&
-                     w(bar(Cfg::kBarK + s), ((uint32_t)j >> 1) & 1u);
+            uint32_t qi = 0;
+            int gb0 = 0;
+            bool ok = true;
+            for (int step = 0, item; ok && (item = attn_item_index(p.causal != 0u, (int)blockIdx.x, (int)gridDim.x, step)) < items; ++step) {
+                const AttnItem it = attn_item(p, qblocks, item);
+                if (it.nkb == 0) continue;
+                ok = w(bar(Cfg::kBarQFull), qi & 1u);
                 if (!ok) break;
-                tc_fence_after();
-                const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + s * Cfg::kKVBytes;
+                for (int j = 0; j < it.nkb && ok; ++j) {
+                    const int gb = gb0 + j, s = gb & 1;
+                    ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)gb >> 1) & 1u) ^ 1u) &&
+                         w(bar(Cfg::kBarK + s), ((uint32_t)gb >> 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + s * Cfg::kKVBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                    tc_mma<1>(tS + (uint32_t)s * 128u, smem_desc_sw128(kq + off, 16, 1024),
-                              smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
+                        tc_mma<1>(tmem + Cfg::kTmemS + (uint32_t)s * 128u, smem_desc_sw128(kq + off, 16, 1024),
+                                  smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
+                    }
+                    tc_commit_1(bar(Cfg::kBarSFull + s));
+                    tc_commit_1(bar(Cfg::kBarKEmpty + s));
                 }
-                tc_commit_1(bar(Cfg::kBarSFull + s));
-                tc_commit_1(bar(Cfg::kBarKEmpty + s));
+                if (!ok) break;
+                tc_commit_1(bar(Cfg::kBarQEmpty));   // Q is free once these products are done
+                ++qi;
+                gb0 += it.nkb;
             }
             tc_commit_1(bar(Cfg::kBarDone));
             // every MMA of both issuers has finished before TMEM is released
@@ -277,210 +331,238 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp == 2) {
         // ---- PV issuer: O += P_j V_j once the softmax has written P_j
-        if (lane == 0 && nkb > 0) {
+        if (lane == 0) {
             const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
+            uint32_t oi = 0;
+            int gb0 = 0;
             bool ok = true;
             const uint32_t tO = tmem + Cfg::kTmemO;
-            for (int j = 0; j < nkb && ok; ++j) {
-                const int s = j & 1;
-                ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)j >> 1) & 1u) &&
-                     w(bar(Cfg::kBarV + s), ((uint32_t)j >> 1) & 1u);
+            for (int step = 0, item; ok && (item = attn_item_index(p.causal != 0u, (int)blockIdx.x, (int)gridDim.x, step)) < items; ++step) {
+                const AttnItem it = attn_item(p, qblocks, item);
+                if (it.nkb == 0) continue;
+                // the accumulator holds the previous item's O until it has been read out
+                ok = w(bar(Cfg::kBarOFree), (oi & 1u) ^ 1u);
                 if (!ok) break;
-                tc_fence_after();
-                const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
+                for (int j = 0; j < it.nkb && ok; ++j) {
+                    const int gb = gb0 + j, s = gb & 1;
+                    ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)gb >> 1) & 1u) &&
+                         w(bar(Cfg::kBarV + s), ((uint32_t)gb >> 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBKey / 16; ++kk) {
-                    const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                    // V is K x N = keys x D with D contiguous: MN-major, 64-column
-                    // chunks one box apart, 16 key rows per step
-                    tc_mma<1>(tO, smem_desc_sw128(pp + aoff, 16, 1024),
-                              smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
-                              (j | kk) ? 1u : 0u);
+                    for (int kk = 0; kk < kBKey / 16; ++kk) {
+                        const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
+                        // V is K x N = keys x D with D contiguous: MN-major, 64-column
+                        // chunks one box apart, 16 key rows per step
+                        tc_mma<1>(tO, smem_desc_sw128(pp + aoff, 16, 1024),
+                                  smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
+                                  (j | kk) ? 1u : 0u);
+                    }
+                    tc_commit_1(bar(Cfg::kBarODone + s));
+                    tc_commit_1(bar(Cfg::kBarVEmpty + s));
                 }
-                tc_commit_1(bar(Cfg::kBarODone + s));
-                tc_commit_1(bar(Cfg::kBarVEmpty + s));
+                ++oi;
+                gb0 += it.nkb;
             }
             tc_commit_1(bar(Cfg::kBarDone));
         }
     } else {
         // ---- softmax warps: thread = query row r (TMEM lane 32 q + lane); group g
-        // takes key blocks j = g, g + 2, .. into score buffer and P tile g
+        // takes the key blocks whose global index gb has parity g, into score
+        // buffer and P tile g
         const AWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const uint32_t q = warp & 3u;
         const int g = (int)((warp - 3u) >> 2);
         const int r = 32 * (int)q + (int)lane;
-        const int i = q0 + r;                              // query index
-        const int lim = p.causal ? i + (p.Sk - p.Sq) : p.Sk - 1;   // last visible key
         const uint32_t lrow = (32u * q) << 16;             // TMEM lane offset of this warp
-        volatile float* const hand = reinterpret_cast<volatile float*>(base_ptr + Cfg::kOffMisc + Cfg::kOffXch);
-        volatile float* const sums = hand + 2 * kBQ;
+        volatile float* const hand = reinterpret_cast<volatile float*>(base_ptr + Cfg::kOffMisc + Cfg::kOffHand);
         const float c2 = p.scale_log2;
-        // m: the row's reference max (base 2) as last known here; l: this group's
-        // share of the row sum, relative to m
-        float m = -INFINITY, l = 0.0f;
         // the factor that moves sums from reference m_old to m_new (1 when equal)
         auto factor = [](float m_old, float m_new) { return m_new == m_old ? 1.0f : ex2_approx(m_old - m_new); };
+        uint32_t oi = 0;
+        int gb0 = 0;
         bool ok = true;
-        for (int j = g; j < nkb && ok; j += 2) {
-            const int sb = g;
-            const uint32_t ph = ((uint32_t)j >> 1) & 1u;
-            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ph));
+        for (int step = 0, item; ok && (item = attn_item_index(p.causal != 0u, (int)blockIdx.x, (int)gridDim.x, step)) < items; ++step) {
+            const AttnItem it = attn_item(p, qblocks, item);
+            const int i = it.q0 + r;                       // query index
+            const int lim = p.causal ? i + (p.Sk - p.Sq) : p.Sk - 1;   // last visible key
+            const bool store = i < p.Sq;
+            OutT* const orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)it.bh * p.Sq + (store ? i : 0)) * D;
+            if (it.nkb == 0) {   // no key is visible to any query of the item: zeros, from group 0
+                if (g == 0 && store) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int t = 0; t < D * (int)sizeof(OutT) / 16; ++t) reinterpret_cast<uint4*>(orow)[t] = z;
+                }
+                continue;
+            }
+            const int nkb = it.nkb;
+            const int gl = (gb0 + nkb - 1) & 1;            // the group that takes the item's last block
+            // m: the row's reference max (base 2) as last known here; l: this
+            // group's share of the row sum, relative to m
+            float m = -INFINITY, l = 0.0f;
+            for (int j = (g - gb0) & 1; j < nkb && ok; j += 2) {
+                const int gb = gb0 + j, sb = g;
+                const uint32_t ph = ((uint32_t)gb >> 1) & 1u;
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarSFull + sb), ph));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t v[4][32];
+                const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v[c]);
+                tmem_ld_wait();
+                // the scores are in registers: the buffer is free for the block after next
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
+                const int k0 = j * kBKey;
+                if (!__all_sync(0xffffffffu, k0 + kBKey - 1 <= lim)) {   // a block on the mask's edge
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (k0 + 32 * c + t > lim) v[c][t] = __float_as_uint(-INFINITY);
+                }
+                // block max of the raw scores, scaled once (the scale is positive)
+                float mp[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) mp[t] = __uint_as_float(v[0][t]);
+#pragma unroll
+                for (int x = 8; x < 128; x += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t)
+                        mp[t] = fmax3(mp[t], __uint_as_float(v[(x + t) >> 5][(x + t) & 31]),
+                                      __uint_as_float(v[(x + 8 + t) >> 5][(x + 8 + t) & 31]));
+                const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7])) * c2;
+                // the reference max after block j - 1, from the other group
+                if (j >= 1) {
+                    ok = __all_sync(0xffffffffu,
+                                    w(bar(Cfg::kBarHand + 2 * (int)q + (g ^ 1)), ((uint32_t)(gb - 1) >> 1) & 1u));
+                    if (!ok) break;
+                    const float mh = hand[(g ^ 1) * kBQ + r];
+                    l *= factor(m, mh);
+                    m = mh;
+                }
+                const bool grow = mx > m + 8.0f;      // false while nothing is visible
+                float alpha = 1.0f;
+                if (grow) {
+                    alpha = ex2_approx(m - mx);       // 0 on the row's first visible block
+                    m = mx;
+                    l *= alpha;
+                }
+                // pass the reference on to block j + 1
+                hand[g * kBQ + r] = m;
+                mbar_arrive_local(bar(Cfg::kBarHand + 2 * (int)q + g));
+                const float mu = (m == -INFINITY) ? 0.0f : m;
+                // P goes into the tile that the product of block gb - 2 read
+                if (gb >= 2) {
+                    ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + sb), (((uint32_t)gb - 2) >> 1) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
+                const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
+                const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
+                uint64_t sp[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) sp[t] = f2_pack(0.0f, 0.0f);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float e[32];
+#pragma unroll
+                    for (int t = 0; t < 32; t += 2) {   // s * scale - m for two keys at once
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c][t]), __uint_as_float(v[c][t + 1])), c2x2, nmu2),
+                                  x0, x1);
+                        e[t] = ex2_approx(x0);
+                        e[t + 1] = ex2_approx(x1);
+                        sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(e[t], e[t + 1]));
+                    }
+                    // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
+                    const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t piece = (uint32_t)(4 * (c & 1) + t) ^ ((uint32_t)r & 7u);
+                        st_shared_v4u(box + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
+                                      pack2<InT>(e[8 * t + 2], e[8 * t + 3]), pack2<InT>(e[8 * t + 4], e[8 * t + 5]),
+                                      pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
+                    }
+                }
+                float s0, s1;
+                f2_unpack(f2_add(f2_add(sp[0], sp[1]), f2_add(sp[2], sp[3])), s0, s1);
+                l += s0 + s1;
+                // a row whose reference max moved rescales its accumulator row, once
+                // the product of block j - 1 is in it (block 0 has nothing to rescale)
+                if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+                    ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (sb ^ 1)), (((uint32_t)gb - 1) >> 1) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t tO = tmem + lrow + Cfg::kTmemO;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        tmem_st_32x32b_x32(tO + (uint32_t)c * 32u, o);
+                    }
+                    tmem_st_wait();
+                }
+                // P (generic-proxy stores) and the rescaled O are ready for the MMA
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
+            }
             if (!ok) break;
-            tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t tS = tmem + lrow + Cfg::kTmemS + (uint32_t)sb * 128u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + (uint32_t)c * 32u, v[c]);
-            tmem_ld_wait();
-            // the scores are in registers: the buffer is free for S_{j+2}
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarSFree + sb));
-            const int k0 = j * kBKey;
-            if (!__all_sync(0xffffffffu, k0 + kBKey - 1 <= lim)) {   // a block on the mask's edge
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        if (k0 + 32 * c + t > lim) v[c][t] = __float_as_uint(-INFINITY);
-            }
-            // block max of the raw scores, scaled once (the scale is positive)
-            float mp[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) mp[t] = __uint_as_float(v[0][t]);
-#pragma unroll
-            for (int x = 8; x < 128; x += 16)
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    mp[t] = fmax3(mp[t], __uint_as_float(v[(x + t) >> 5][(x + t) & 31]),
-                                  __uint_as_float(v[(x + 8 + t) >> 5][(x + 8 + t) & 31]));
-            const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7])) * c2;
-            // the reference max after block j - 1, from the other group
-            if (j >= 1) {
-                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarHand + 2 * (int)q + (g ^ 1)), ((uint32_t)(j - 1) >> 1) & 1u));
+            if (g != gl) {
+                // this group's share of the row sum, at the final reference, goes to
+                // the group of the last block through that group's hand-off slot
+                // (its max has just been read from there); then on to the next item
+                ok = __all_sync(0xffffffffu,
+                                w(bar(Cfg::kBarHand + 2 * (int)q + gl), ((uint32_t)(gb0 + nkb - 1) >> 1) & 1u));
                 if (!ok) break;
-                const float mh = hand[(g ^ 1) * kBQ + r];
-                l *= factor(m, mh);
-                m = mh;
-            }
-            const bool grow = mx > m + 8.0f;      // false while nothing is visible
-            float alpha = 1.0f;
-            if (grow) {
-                alpha = ex2_approx(m - mx);       // 0 on the row's first visible block
-                m = mx;
-                l *= alpha;
-            }
-            // pass the reference on to block j + 1
-            hand[g * kBQ + r] = m;
-            mbar_arrive_local(bar(Cfg::kBarHand + 2 * (int)q + g));
-            const float mu = (m == -INFINITY) ? 0.0f : m;
-            // P_j goes into the tile that P_{j-2} V_{j-2} read
-            if (j >= 2) {
-                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + sb), (((uint32_t)j - 2) >> 1) & 1u));
+                l *= factor(m, hand[gl * kBQ + r]);   // l = 0 if this group took no block of the item
+                hand[gl * kBQ + r] = l;
+                mbar_arrive_local(bar(Cfg::kBarFin + (int)q));
+            } else {
+                // the group of the last block adds the other share, writes O / l out
+                // (the whole row) and frees the accumulator for the next item.  The
+                // TMEM loads are warp-collective: the whole warp loads; only the
+                // stores depend on the row being a real query.
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarFin + (int)q), oi & 1u));
+                if (!ok) break;
+                l += hand[gl * kBQ + r];
+                const int gbl = gb0 + nkb - 1;
+                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (gbl & 1)), ((uint32_t)gbl >> 1) & 1u));
                 if (!ok) break;
                 tc_fence_after();
-            }
-            // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
-            const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
-            const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
-            uint64_t sp[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) sp[t] = f2_pack(0.0f, 0.0f);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float e[32];
-#pragma unroll
-                for (int t = 0; t < 32; t += 2) {   // s * scale - m for two keys at once
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c][t]), __uint_as_float(v[c][t + 1])), c2x2, nmu2), x0, x1);
-                    e[t] = ex2_approx(x0);
-                    e[t + 1] = ex2_approx(x1);
-                    sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(e[t], e[t + 1]));
-                }
-                // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
-                const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t piece = (uint32_t)(4 * (c & 1) + t) ^ ((uint32_t)r & 7u);
-                    st_shared_v4u(box + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
-                                  pack2<InT>(e[8 * t + 2], e[8 * t + 3]), pack2<InT>(e[8 * t + 4], e[8 * t + 5]),
-                                  pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
-                }
-            }
-            float s0, s1;
-            f2_unpack(f2_add(f2_add(sp[0], sp[1]), f2_add(sp[2], sp[3])), s0, s1);
-            l += s0 + s1;
-            // a row whose reference max moved rescales its accumulator row, once
-            // P_{j-1} V_{j-1} is in it (block 0 has nothing to rescale)
-            if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-                ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + (sb ^ 1)), (((uint32_t)j - 1) >> 1) & 1u));
-                if (!ok) break;
-                tc_fence_after();
+                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
                 const uint32_t tO = tmem + lrow + Cfg::kTmemO;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, o);
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, v);
                     tmem_ld_wait();
+                    if (store) {
+                        OutT o[32];
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                    tmem_st_32x32b_x32(tO + (uint32_t)c * 32u, o);
+                        for (int t = 0; t < 32; ++t) o[t] = cvt_out(__uint_as_float(v[t]) * inv, (OutT*)nullptr);
+                        constexpr int kVec = 32 * (int)sizeof(OutT) / 16;
+#pragma unroll
+                        for (int t = 0; t < kVec; ++t)
+                            reinterpret_cast<uint4*>(orow + 32 * c)[t] = reinterpret_cast<const uint4*>(o)[t];
+                    }
                 }
-                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(bar(Cfg::kBarOFree));
             }
-            // P_j (generic-proxy stores) and the rescaled O are ready for the MMA
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
-        }
-        // ---- the row sum: the group that did not take the last block brings its
-        // share to the final reference, then the two shares are added
-        if (ok && nkb > 0) {
-            const int g_last = (nkb - 1) & 1;
-            if (g != g_last && nkb >= 2) {
-                ok = __all_sync(0xffffffffu,
-                                w(bar(Cfg::kBarHand + 2 * (int)q + g_last), ((uint32_t)(nkb - 1) >> 1) & 1u));
-                if (ok) l *= factor(m, hand[g_last * kBQ + r]);
-            }
-        }
-        if (ok && nkb > 0) {
-            sums[g * kBQ + r] = l;
-            mbar_arrive_local(bar(Cfg::kBarFin + (int)q));
-            ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarFin + (int)q), 0u));
-            if (ok) l = sums[r] + sums[kBQ + r];
-        }
-        // ---- O / l, stored by row, each group its D / 2 columns.  The TMEM loads
-        // are warp-collective: the whole warp loads (conditions below are
-        // warp-uniform); only the stores depend on the row being a real query.
-        if (ok && nkb > 0) {
-            ok = __all_sync(0xffffffffu,
-                            w(bar(Cfg::kBarODone + ((nkb - 1) & 1)), (((uint32_t)nkb - 1) >> 1) & 1u));
-            if (ok) tc_fence_after();
-        }
-        const bool store = i < p.Sq;
-        OutT* orow = reinterpret_cast<OutT*>(p.O) + ((int64_t)bh * p.Sq + (store ? i : 0)) * D + g * (D / 2);
-        const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-        const uint32_t tO = tmem + lrow + Cfg::kTmemO + (uint32_t)g * (uint32_t)(D / 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            uint32_t v[32];
-            if (ok && nkb > 0) {
-                tmem_ld_32x32b_x32(tO + (uint32_t)c * 32u, v);
-                tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = 0u;
-            }
-            if (store) {
-                OutT o[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t) o[t] = cvt_out(__uint_as_float(v[t]) * inv, (OutT*)nullptr);
-                constexpr int kVec = 32 * (int)sizeof(OutT) / 16;
-#pragma unroll
-                for (int t = 0; t < kVec; ++t)
-                    reinterpret_cast<uint4*>(orow + 32 * c)[t] = reinterpret_cast<const uint4*>(o)[t];
-            }
+            ++oi;
+            gb0 += nkb;
         }
     }
     tc_fence_before();
@@ -494,7 +576,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 template <int D, typename InT, typename OutT>
 cudaError_t launch_impl(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                         cudaStream_t stream) {
-    dim3 grid((unsigned)((p.Sq + kBQ - 1) / kBQ), (unsigned)p.BH, 1);
+    // persistent: one CTA per SM (at most one per item, or per pair of items
+    // under a causal mask)
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t items = (int64_t)p.BH * ((p.Sq + kBQ - 1) / kBQ);
+    const int64_t units = p.causal ? (items + 1) / 2 : items;
+    const unsigned grid = (unsigned)(units < sms[dev] ? units : sms[dev]);
     attn_fwd_kernel<D, InT, OutT><<<grid, kAttnThreads, AttnCfg<D>::kSmem, stream>>>(tmQ, tmK, tmV, p);
     return cudaGetLastError();
 }
