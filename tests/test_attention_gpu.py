@@ -88,3 +88,20 @@ def test_attention_rejects_bad_head_dim(plan):
     with pytest.raises(G.GemmError) as e:
         plan.attention(q, q, q, torch.zeros(1, 1, 8, 96, device="cuda"))
     assert e.value.code == G.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_persistent_many_items_per_cta(plan, causal):
+    # 160 heads x 3 query blocks = 480 items: every CTA walks several items (in
+    # pairs under the causal mask), so barrier phases carry across items
+    run(plan, 2, 80, 300, 260, 64, causal, seed=40 + causal)
+
+
+def test_attention_persistent_with_empty_items(plan):
+    # causal with twice as many queries as keys: the first query blocks of every
+    # head see no key (items with no key block) between items that do
+    run(plan, 1, 160, 600, 300, 64, True, seed=42)
+
+
+def test_attention_persistent_d128_bf16_out(plan):
+    run(plan, 1, 64, 640, 512, 128, True, out_dtype=torch.bfloat16, seed=43)
