@@ -794,6 +794,7 @@ int gemm_attention(gemm_plan_t p, int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     ap.O = O;
     ap.status = p->status_dev;
     ap.timeout_ns = p->timeout_ns;
+    ap.debug = p->debug;
     e = launch_attention(dtype, (int)D, tmQ, tmK, tmV, ap, stream);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;

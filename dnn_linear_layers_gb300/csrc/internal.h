@@ -43,7 +43,7 @@ enum StatusBits : int {
 
 // Fault-injection flags (tests only): make one wait run out on purpose.
 enum DebugFlags : uint32_t {
-    DBG_SKIP_FIRST_ACC_COMMIT = 1u,   // MMA warp never signals the first accumulator
+    DBG_SKIP_FIRST_ACC_COMMIT = 1u,   // MMA warp never signals the first accumulator (attention: the first PV product)
 };
 
 // Tile shape of the tensor-core kernels: each CTA owns 128 rows of C, the
@@ -157,6 +157,7 @@ struct AttnParams {
     void* O;
     int* status;
     uint64_t timeout_ns;
+    uint32_t debug;        // DebugFlags (tests only)
 };
 cudaError_t attention_prepare(int dtype);
 cudaError_t launch_attention(int dtype, int D, const CUtensorMap& tmQ, const CUtensorMap& tmK,

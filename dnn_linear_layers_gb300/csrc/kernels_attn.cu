@@ -290,6 +290,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 gb0 += it.nkb;
             }
+            if (!ok) {
+                // let copies already issued land before shared memory is released
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 100000ull) { }
+            }
         }
     } else if (warp == 1) {
         // ---- S issuer: S_j = Q K_j^T into score buffer gb & 1
@@ -325,9 +330,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 gb0 += it.nkb;
             }
             tc_commit_1(bar(Cfg::kBarDone));
-            // every MMA of both issuers has finished before TMEM is released
-            const AWait wd{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
-            wd(bar(Cfg::kBarDone), 0);
+            // every MMA of both issuers has finished before TMEM is released; this
+            // wait ignores the abort flag (only its time budget ends it), so an
+            // aborted run still lets the products in flight drain
+            if (!mbar_try_wait(bar(Cfg::kBarDone), 0)) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar(Cfg::kBarDone), 0) && globaltimer_ns() - t0 < p.timeout_ns) { }
+            }
         }
     } else if (warp == 2) {
         // ---- PV issuer: O += P_j V_j once the softmax has written P_j
@@ -359,7 +368,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                   smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
                                   (j | kk) ? 1u : 0u);
                     }
-                    tc_commit_1(bar(Cfg::kBarODone + s));
+                    if (!((p.debug & DBG_SKIP_FIRST_ACC_COMMIT) && gb == 0)) tc_commit_1(bar(Cfg::kBarODone + s));
                     tc_commit_1(bar(Cfg::kBarVEmpty + s));
                 }
                 ++oi;

@@ -258,8 +258,9 @@ int gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns);
 int gemm_plan_set_packing(gemm_plan_t plan, int enabled);
 
 /* Test hook: fault-injection flags.  Bit 0 makes the MMA warp skip the first
- * "accumulator ready" signal so the epilogue's bounded wait runs out and the
- * run reports GEMM_ERR_DEVICE_TIMEOUT; the GPU context stays usable. */
+ * "accumulator ready" signal (gemm_attention: the first "PV product done"
+ * signal) so a bounded wait runs out and the run reports
+ * GEMM_ERR_DEVICE_TIMEOUT; the GPU context stays usable. */
 int gemm_plan_set_debug(gemm_plan_t plan, unsigned flags);
 
 /* Bytes of workspace the plan currently holds. */

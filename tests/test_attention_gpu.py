@@ -105,3 +105,28 @@ def test_attention_persistent_with_empty_items(plan):
 
 def test_attention_persistent_d128_bf16_out(plan):
     run(plan, 1, 64, 640, 512, 128, True, out_dtype=torch.bfloat16, seed=43)
+
+
+def test_attention_bounded_wait_reports_timeout_and_context_survives():
+    """Fault injection on the host's request: the PV issuer withholds the first
+    'product done' signal, a softmax wait runs out, every role leaves through
+    its bounded waits, the run reports GEMM_ERR_DEVICE_TIMEOUT, and the next
+    run on the same context matches the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    with G.Plan(0, "nk") as p:
+        p.set_timeout_ns(20_000_000)          # 20 ms
+        g = torch.Generator().manual_seed(50)
+        q = torch.randn(1, 2, 512, 64, generator=g).bfloat16()
+        k = torch.randn(1, 2, 512, 64, generator=g).bfloat16()
+        v = torch.randn(1, 2, 512, 64, generator=g).bfloat16()
+        o = torch.zeros(1, 2, 512, 64, device="cuda")
+        p.set_debug(1)
+        p.attention(q.cuda(), k.cuda(), v.cuda(), o)
+        assert p.status() == G.ERR_DEVICE_TIMEOUT
+        p.set_debug(0)
+        p.attention(q.cuda(), k.cuda(), v.cuda(), o)
+        assert p.status() == 0
+        ref = oracle.attention(q, k, v)
+        vmax = np.abs(oracle._f64(v)).max(axis=-2, keepdims=True)
+        assert np.all(np.abs(o.double().cpu().numpy() - ref) <= 2 * 2.0 ** -9 * vmax + 1e-5)

@@ -140,3 +140,18 @@ def test_tf32_refusals():
         p.set_kernel(G.KERNEL_SKINNY)
         with pytest.raises(G.GemmError):
             p.run(A, torch.zeros(16, 32, device="cuda"), C)
+
+
+def test_tf32_extended_epilogue_integer_exact(plan):
+    # alpha * acc * scale + bias + beta * C_old, ReLU; bf16 scale and bias vectors
+    A, W, _ = inputs(260, 300, 64, "int", 7)
+    g = torch.Generator().manual_seed(8)
+    scale = torch.randint(-4, 5, (300,), generator=g).to(torch.bfloat16)
+    bias = torch.randint(-4, 5, (300,), generator=g).to(torch.bfloat16)
+    C0 = torch.randint(-4, 5, (260, 300), generator=g).float()
+    C = C0.cuda().clone()
+    plan.set_kernel(G.KERNEL_AUTO)
+    plan.run(A.cuda(), W.cuda(), C, bias.cuda(), relu=True, alpha=2.0, beta=-1.0, scale=scale.cuda())
+    assert plan.status() == 0
+    ref, _ = oracle.gemm_ex(A, W, alpha=2.0, beta=-1.0, C0=C0, scale=scale, bias=bias, relu=True, b_nk=True)
+    assert (C.double().cpu().numpy() == ref).all()

@@ -105,3 +105,24 @@ def test_transposed_a_refusals(plans):
     B8 = torch.zeros(16, 64, device="cuda").to(torch.float8_e4m3fn)
     with pytest.raises(G.GemmError):
         p.run(A8, B8, C)
+
+
+@pytest.mark.parametrize("kernel", [G.KERNEL_TC_SINGLE, G.KERNEL_TC_PAIR])
+def test_transposed_a_extended_epilogue_integer_exact(plans, kernel):
+    # t = alpha * acc * scale + bias + beta * C_old, ReLU, with every step exact in
+    # fp32 (alpha a power of two, integers well under 2^24)
+    import oracle
+    from dnn_linear_layers_gb300.inputs import int_bf16
+    M, N, K = 300, 520, 64
+    A = int_bf16((M, K), 60)
+    B = int_bf16((N, K), 61)
+    scale = int_bf16((N,), 62)
+    bias = int_bf16((N,), 63)
+    C0 = int_bf16((M, N), 64).float()
+    p = plans["nk"]
+    p.set_kernel(kernel)
+    C = C0.cuda().clone()
+    p.run(A.t().contiguous().cuda(), B.cuda(), C, bias.cuda(), relu=True, alpha=0.5, beta=2.0, scale=scale.cuda())
+    assert p.status() == 0
+    ref, _ = oracle.gemm_ex(A, B, alpha=0.5, beta=2.0, C0=C0, scale=scale, bias=bias, relu=True, b_nk=True)
+    assert (C.double().cpu().numpy() == ref).all()
