@@ -52,31 +52,31 @@ template <int D>
 struct AttnCfg {
     static constexpr int kQBytes = kBQ * D * 2;   // D / 64 boxes
     static constexpr int kKVBytes = kBKey * D * 2;
-    static constexpr int kPBytes = kBQ * kBKey * 2;   // two boxes of 64 keys
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 3;             // K and V ring slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffP = kOffV + kStages * kKVBytes;   // two P tiles
-    static constexpr int kOffMisc = kOffP + 2 * kPBytes;
-    // misc: 32 barriers (8 bytes each), then float hand-off [2 groups][128 rows],
+    static constexpr int kOffMisc = kOffV + kStages * kKVBytes;
+    // misc: 36 barriers (8 bytes each), then float hand-off [2 groups][128 rows],
     // the abort flag and the TMEM address
-    static constexpr int kOffHand = 256;
+    static constexpr int kOffHand = 320;
     static constexpr int kAbort = kOffHand + 2 * kBQ * 4, kTmemPtr = kAbort + 4;
     static constexpr int kMiscBytes = kTmemPtr + 12;
     // the tiles want 1024-byte alignment; a window starting at a multiple of
     // 256 bytes fits (the kernel checks, and stops with a status bit if not)
     static constexpr int kSlack = 768;
     static constexpr int kSmem = kOffMisc + kMiscBytes + kSlack;
-    // barriers; pairs are indexed by buffer (global block index & 1)
-    static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarK = 2, kBarV = 4, kBarKEmpty = 6, kBarVEmpty = 8,
-                         kBarSFull = 10, kBarSFree = 12, kBarPFull = 14, kBarODone = 16, kBarDone = 18,
-                         kBarOFree = 19,   // the item's O has been read out of TMEM
-                         kBarHand = 20,    // [4 lane quarters][2 groups]: a group published a row max
-                         kBarFin = 28;     // [4 lane quarters]: the other group's share of the row sums is in
+    // barriers: K / V ring slots indexed by global block index % 3, score and P
+    // buffers by global block index & 1
+    static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarK = 2, kBarV = 5, kBarKEmpty = 8, kBarVEmpty = 11,
+                         kBarSFull = 14, kBarSFree = 16, kBarPFull = 18, kBarODone = 20, kBarDone = 22,
+                         kBarOFree = 23,   // the item's O has been read out of TMEM
+                         kBarHand = 24,    // [4 lane quarters][2 groups]: a group published a row max
+                         kBarFin = 32;     // [4 lane quarters]: the other group's share of the row sums is in
     static constexpr int kTmemS = 0;      // two score buffers: columns 0..127 and 128..255
     static constexpr int kTmemO = 256;    // accumulator: columns 256 .. 256 + D - 1
-    static_assert(32 * 8 <= kOffHand, "misc layout");
+    static constexpr int kTmemP = 384;    // two P tiles, 64 columns each (two 16-bit values per column)
+    static_assert(36 * 8 <= kOffHand, "misc layout");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -116,9 +116,6 @@ __device__ __forceinline__ float cvt_out(float v, float*) { return v; }
 __device__ __forceinline__ __nv_bfloat16 cvt_out(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
 __device__ __forceinline__ __half cvt_out(float v, __half*) { return __float2half_rn(v); }
 
-__device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 // 2^x on the special-function unit (ex2.approx: relative error about 2^-22,
 // subnormal results flushed to zero, 2^-inf = +0)
@@ -210,11 +207,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (threadIdx.x == 0) {
         mbar_init(bar(Cfg::kBarQFull), 1);
         mbar_init(bar(Cfg::kBarQEmpty), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(bar(Cfg::kBarK + s), 1);
             mbar_init(bar(Cfg::kBarV + s), 1);
             mbar_init(bar(Cfg::kBarKEmpty + s), 1);
             mbar_init(bar(Cfg::kBarVEmpty + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(bar(Cfg::kBarSFull + s), 1);
             mbar_init(bar(Cfg::kBarSFree + s), 4);   // the four warps of the group that owns buffer s
             mbar_init(bar(Cfg::kBarPFull + s), 4);
@@ -262,9 +261,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(base + Cfg::kOffQ + b * kBox, &tmQ, bar(Cfg::kBarQFull), 64 * b, it.q0, it.bh, pol_q);
                 ++qi;
-                // block j (global gb) of K or V: one 128-key box per 64 columns
+                // block j (global gb) of K or V, into ring slot gb % 3: one 128-key box
+                // per 64 columns
                 auto load_kv = [&](const CUtensorMap* map, int off, int barid, int gb, int j) {
-                    const int s = gb & 1;
+                    const int s = gb % Cfg::kStages;
                     mbar_arrive_expect_tx(bar(barid + s), Cfg::kKVBytes);
 #pragma unroll
                     for (int b = 0; b < D / 64; ++b)
@@ -272,19 +272,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                     j * kBKey, it.bh, pol_kv);
                 };
                 // order K_0, K_1, V_0, K_2, V_1, ...: a K slot frees when the score
-                // product two blocks back is done, a V slot when that PV product is
-                ok = w(bar(Cfg::kBarKEmpty + (gb0 & 1)), (((uint32_t)gb0 >> 1) & 1u) ^ 1u);
+                // product three blocks back is done, a V slot when that PV product is
+                auto ring_phase = [](int gb) { return ((uint32_t)(gb / Cfg::kStages) & 1u) ^ 1u; };
+                ok = w(bar(Cfg::kBarKEmpty + gb0 % Cfg::kStages), ring_phase(gb0));
                 if (!ok) break;
                 load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gb0, 0);
                 for (int j = 0; j < it.nkb && ok; ++j) {
                     if (j + 1 < it.nkb) {
                         const int gn = gb0 + j + 1;
-                        ok = w(bar(Cfg::kBarKEmpty + (gn & 1)), (((uint32_t)gn >> 1) & 1u) ^ 1u);
+                        ok = w(bar(Cfg::kBarKEmpty + gn % Cfg::kStages), ring_phase(gn));
                         if (!ok) break;
                         load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gn, j + 1);
                     }
                     const int gb = gb0 + j;
-                    ok = w(bar(Cfg::kBarVEmpty + (gb & 1)), (((uint32_t)gb >> 1) & 1u) ^ 1u);
+                    ok = w(bar(Cfg::kBarVEmpty + gb % Cfg::kStages), ring_phase(gb));
                     if (!ok) break;
                     load_kv(&tmV, Cfg::kOffV, Cfg::kBarV, gb, j);
                 }
@@ -309,12 +310,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ok = w(bar(Cfg::kBarQFull), qi & 1u);
                 if (!ok) break;
                 for (int j = 0; j < it.nkb && ok; ++j) {
-                    const int gb = gb0 + j, s = gb & 1;
+                    const int gb = gb0 + j, s = gb & 1, r3 = gb % Cfg::kStages;
                     ok = w(bar(Cfg::kBarSFree + s), (((uint32_t)gb >> 1) & 1u) ^ 1u) &&
-                         w(bar(Cfg::kBarK + s), ((uint32_t)gb >> 1) & 1u);
+                         w(bar(Cfg::kBarK + r3), (uint32_t)(gb / Cfg::kStages) & 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + s * Cfg::kKVBytes;
+                    const uint32_t kq = base + Cfg::kOffQ, kk0 = base + Cfg::kOffK + r3 * Cfg::kKVBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
@@ -322,7 +323,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                   smem_desc_sw128(kk0 + off, 16, 1024), p.idesc_s, kk ? 1u : 0u);
                     }
                     tc_commit_1(bar(Cfg::kBarSFull + s));
-                    tc_commit_1(bar(Cfg::kBarKEmpty + s));
+                    tc_commit_1(bar(Cfg::kBarKEmpty + r3));
                 }
                 if (!ok) break;
                 tc_commit_1(bar(Cfg::kBarQEmpty));   // Q is free once these products are done
@@ -353,23 +354,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ok = w(bar(Cfg::kBarOFree), (oi & 1u) ^ 1u);
                 if (!ok) break;
                 for (int j = 0; j < it.nkb && ok; ++j) {
-                    const int gb = gb0 + j, s = gb & 1;
+                    const int gb = gb0 + j, s = gb & 1, r3 = gb % Cfg::kStages;
                     ok = w(bar(Cfg::kBarPFull + s), ((uint32_t)gb >> 1) & 1u) &&
-                         w(bar(Cfg::kBarV + s), ((uint32_t)gb >> 1) & 1u);
+                         w(bar(Cfg::kBarV + r3), (uint32_t)(gb / Cfg::kStages) & 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t pp = base + Cfg::kOffP + s * Cfg::kPBytes, vv = base + Cfg::kOffV + s * Cfg::kKVBytes;
+                    const uint32_t pt = tmem + Cfg::kTmemP + (uint32_t)s * 64u;
+                    const uint32_t vv = base + Cfg::kOffV + r3 * Cfg::kKVBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBKey / 16; ++kk) {
-                        const uint32_t aoff = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
-                        // V is K x N = keys x D with D contiguous: MN-major, 64-column
-                        // chunks one box apart, 16 key rows per step
-                        tc_mma<1>(tO, smem_desc_sw128(pp + aoff, 16, 1024),
-                                  smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024), p.idesc_o,
-                                  (j | kk) ? 1u : 0u);
+                        // P from TMEM: 16 keys = 8 columns per step.  V is K x N = keys
+                        // x D with D contiguous: MN-major, 64-column chunks one box
+                        // apart, 16 key rows per step
+                        tc_mma_ts(tO, pt + (uint32_t)kk * 8u, smem_desc_sw128(vv + (uint32_t)kk * 2048u, kBox, 1024),
+                                  p.idesc_o, (j | kk) ? 1u : 0u);
                     }
                     if (!((p.debug & DBG_SKIP_FIRST_ACC_COMMIT) && gb == 0)) tc_commit_1(bar(Cfg::kBarODone + s));
-                    tc_commit_1(bar(Cfg::kBarVEmpty + s));
+                    tc_commit_1(bar(Cfg::kBarVEmpty + r3));
                 }
                 ++oi;
                 gb0 += it.nkb;
@@ -465,40 +466,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 hand[g * kBQ + r] = m;
                 mbar_arrive_local(bar(Cfg::kBarHand + 2 * (int)q + g));
                 const float mu = (m == -INFINITY) ? 0.0f : m;
-                // P goes into the tile that the product of block gb - 2 read
+                // P goes into the TMEM tile that the product of block gb - 2 read
                 if (gb >= 2) {
                     ok = __all_sync(0xffffffffu, w(bar(Cfg::kBarODone + sb), (((uint32_t)gb - 2) >> 1) & 1u));
                     if (!ok) break;
                     tc_fence_after();
                 }
-                // P = 2^(s - m) as 16-bit into the swizzled A tile, and its row sum
-                const uint32_t prow = base + Cfg::kOffP + (uint32_t)sb * Cfg::kPBytes + (uint32_t)r * 128u;
+                // P = 2^(s - m) as 16-bit values into the group's TMEM tile (two
+                // per column, keys 2c and 2c + 1 in column c), and its row sum
+                const uint32_t tP = tmem + lrow + Cfg::kTmemP + (uint32_t)sb * 64u;
                 const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
                 uint64_t sp[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) sp[t] = f2_pack(0.0f, 0.0f);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float e[32];
+                for (int c = 0; c < 4; ++c) {    // keys 32 c .. 32 c + 31 -> columns 16 c .. 16 c + 15
+                    // the packed pairs go into v[c] in place: entry t / 2 has been
+                    // read by the time it is written
 #pragma unroll
                     for (int t = 0; t < 32; t += 2) {   // s * scale - m for two keys at once
                         float x0, x1;
                         f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c][t]), __uint_as_float(v[c][t + 1])), c2x2, nmu2),
                                   x0, x1);
-                        e[t] = ex2_approx(x0);
-                        e[t + 1] = ex2_approx(x1);
-                        sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(e[t], e[t + 1]));
+                        x0 = ex2_approx(x0);
+                        x1 = ex2_approx(x1);
+                        sp[(t >> 1) & 3] = f2_add(sp[(t >> 1) & 3], f2_pack(x0, x1));
+                        v[c][t >> 1] = pack2<InT>(x0, x1);
                     }
-                    // keys 32 c .. 32 c + 31: box c / 2, 16-byte pieces 4 (c & 1) .. + 3
-                    const uint32_t box = prow + (uint32_t)(c >> 1) * (uint32_t)kBox;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t piece = (uint32_t)(4 * (c & 1) + t) ^ ((uint32_t)r & 7u);
-                        st_shared_v4u(box + (piece << 4), pack2<InT>(e[8 * t], e[8 * t + 1]),
-                                      pack2<InT>(e[8 * t + 2], e[8 * t + 3]), pack2<InT>(e[8 * t + 4], e[8 * t + 5]),
-                                      pack2<InT>(e[8 * t + 6], e[8 * t + 7]));
-                    }
+                    tmem_st_32x32b_x16(tP + 16u * (uint32_t)c, v[c]);
                 }
+                tmem_st_wait();
                 float s0, s1;
                 f2_unpack(f2_add(f2_add(sp[0], sp[1]), f2_add(sp[2], sp[3])), s0, s1);
                 l += s0 + s1;
@@ -520,8 +517,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     tmem_st_wait();
                 }
-                // P (generic-proxy stores) and the rescaled O are ready for the MMA
-                fence_proxy_async_smem();
+                // P and the rescaled O are in TMEM, ready for the MMA
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_local(bar(Cfg::kBarPFull + sb));
