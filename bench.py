@@ -71,6 +71,10 @@ WORKLOADS = {
     "linear_m1_4096x4096": (1, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m16_4096x4096": (16, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m128_4096x4096": (128, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
+    # the same decode layers with e4m3 weights and activations (per-tensor scales belong in alpha)
+    "linear_m1_4096x14336_e4m3": (1, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
+    "linear_m16_4096x14336_e4m3": (16, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
+    "linear_m128_4096x14336_e4m3": (128, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
 }
 DEFAULT_WORKLOAD = "square8192_bf16"
 KERNEL_NAME = "gemm_tc_kernel"
@@ -221,10 +225,11 @@ def make_inputs(name, device, seed=0):
         A = normal_bf16((M, K), 3 * seed, a_std, dtype=torch.float32)
         B = normal_bf16((N, K), 3 * seed + 1, b_std, dtype=torch.float32)
         return A, B, None
-    if f8 is not None:   # N(0,1) drawn as bf16, then rounded to the fp8 format
+    if f8 is not None:   # N(0,1) drawn as bf16, then rounded to the fp8 format; bf16 bias
         A = normal_bf16((M, K), 3 * seed, a_std).to(f8)
         B = normal_bf16((N, K), 3 * seed + 1, b_std).to(f8)
-        return A, B, None
+        bias = normal_bf16((N,), 3 * seed + 2, 0.02) if has_bias else None
+        return A, B, bias
     if "_transa_" in name:   # A as stored: K x M
         A = normal_bf16((K, M), 3 * seed, a_std)
         B = normal_bf16((N, K) if lay == "nk" else (K, N), 3 * seed + 1, b_std)

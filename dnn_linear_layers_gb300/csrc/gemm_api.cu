@@ -239,7 +239,9 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     const int mpad = (int)round_up(M, 16);
     const int tmem_cols = mpad <= 32 ? 32 : (mpad <= 64 ? 64 : 128);
     const int64_t n_tiles = (N + 127) / 128;
-    const int64_t nkb = (K + 63) / 64;
+    const int es = in_bytes(dtype);                   // 2, or 1 for fp8 (N x K W only)
+    const int kbk = 128 / es;                         // elements per 128-byte k-block row
+    const int64_t nkb = (K + kbk - 1) / kbk;
     if (n_tiles > INT32_MAX / 8) return GEMM_ERR_UNSUPPORTED;
     // Weight bytes in flight decide the bandwidth, and only resident CTAs have
     // loads in flight: take the largest split count S whose grid (n_tiles * S
@@ -280,10 +282,10 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
         stages = p->skinny_stages ? p->skinny_stages : 3;
     }
     CUtensorMap tmW, tmX;
-    const bool okw = w_nk ? make_map(&tmW, in_dt, W, (uint64_t)K, (uint64_t)N, (uint64_t)ldw * 2, 64, 128)
+    const bool okw = w_nk ? make_map(&tmW, in_dt, W, (uint64_t)K, (uint64_t)N, (uint64_t)ldw * es, kbk, 128)
                           : make_map(&tmW, in_dt, W, (uint64_t)N, (uint64_t)K, (uint64_t)ldw * 2, 64, 64);
     if (!okw) return GEMM_ERR_CUDA;
-    if (!make_map(&tmX, in_dt, X, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, 64, (uint32_t)mpad))
+    if (!make_map(&tmX, in_dt, X, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * es, kbk, (uint32_t)mpad))
         return GEMM_ERR_CUDA;
     SkinnyParams sp;
     std::memset(&sp, 0, sizeof(sp));
@@ -292,13 +294,12 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     sp.w_prefetch = (p->pdl && (p->flags & GEMM_B_CONST)) ? 1u : 0u;
     // X by TMA; the cp.async loader in the epilogue warps measured equal for
     // M <= 16 and slower for M = 128 on GB300, so it is only a sweep option
-    sp.x_lsu = p->skinny_x_lsu ? 1u : 0u;
+    sp.x_lsu = (p->skinny_x_lsu && es == 2) ? 1u : 0u;
     sp.X = X; sp.ldx = ldx; sp.pdl = p->pdl; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
     sp.epi = epi;
     sp.ex = ex;
-    const uint32_t ab = in_is_bf16(dtype) ? 1u : 0u;
-    sp.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((w_nk ? 0u : 1u) << 15) | ((uint32_t)(mpad >> 3) << 17) |
-               ((uint32_t)(128 >> 4) << 24);
+    // A = W (128 features; MN-major when stored K x N), B = X (mpad tokens, K-major)
+    sp.idesc = make_idesc(dtype, false, 128, mpad, !w_nk);
     sp.w_mn_major = w_nk ? 0u : 1u;
     sp.bias = bias;
     sp.Y = Y; sp.ldy = ldy;
@@ -369,6 +370,8 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     for (int dt = 0; dt < 4; ++dt) {
         e = attention_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+    }
+    for (int dt = 0; dt <= DT_E5M2_BF16; ++dt) {
         e = skinny_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
     }
@@ -542,10 +545,12 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const bool fp8 = dtype_is_fp8(dtype) || dtype_is_tf32(dtype);
     if (fp8 && (!b_nk || conv || a_km)) return GEMM_ERR_UNSUPPORTED;
     if (a_km && conv) return GEMM_ERR_UNSUPPORTED;
+    // the small-M kernel takes 16-bit and fp8 operands with an M x K A
+    const bool tf32 = dtype_is_tf32(dtype);
     int kernel = p->forced_kernel;
     if (kernel == GEMM_KERNEL_AUTO)
-        kernel = (M <= 128 && !conv && !fp8 && !a_km) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
-    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || fp8 || a_km)) return GEMM_ERR_UNSUPPORTED;
+        kernel = (M <= 128 && !conv && !tf32 && !a_km) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || tf32 || a_km)) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
         return GEMM_ERR_UNSUPPORTED;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;

@@ -23,7 +23,11 @@
 //     accumulate-then-combine is the warp-shuffle reduction idea of the CMU
 //     15-418 notes, section 3.3, lifted to CTAs.
 //   * W may be N x K (a Linear weight, K contiguous) or K x N (N contiguous);
-//     the MMA reads either from 128-byte-swizzled shared memory.
+//     the MMA reads either from 128-byte-swizzled shared memory;
+//   * fp8 weights and activations (e4m3 / e5m2, N x K W): kind::f8f6f4 MMAs,
+//     a k-block is still one 128-byte row per feature, now 128 elements, so the
+//     ring and its descriptors are those of the 16-bit kernel with half the
+//     weight bytes per output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,7 +40,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
-constexpr int kWStage = 128 * 64 * 2;      // 128 features x 64 k, 16 KB
+constexpr int kWStage = 128 * 128;         // 128 features x one 128-byte k-block row, 16 KB
 constexpr int kMiscBytes = 2048;          // barriers, then bias and scale staging
 
 __device__ __forceinline__ void cluster_arrive_wait() {
@@ -106,8 +110,10 @@ __device__ __forceinline__ float out_float(__nv_bfloat16 v) { return __bfloat162
 __device__ __forceinline__ float out_float(__half v) { return __half2float(v); }
 
 // Grid: num_n_tiles * S CTAs, clusters of S along x.  CTA rank r of a cluster
-// owns k-blocks [r*nkb/S, (r+1)*nkb/S) of feature tile blockIdx.x / S.
-template <typename InT, typename OutT>
+// owns k-blocks [r*nkb/S, (r+1)*nkb/S) of feature tile blockIdx.x / S.  KIND 0:
+// 16-bit operands (64 elements per k-block); KIND 1: fp8 (128 elements); InT is
+// the type of the bias and scale vectors.
+template <typename InT, typename OutT, int KIND>
 __global__ void __launch_bounds__(kThreads, kSkinnyMaxCtasPerSm)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const SkinnyParams p) {
@@ -118,6 +124,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int mpad = p.mpad;                          // 16..128, multiple of 16
     const int kStages = p.stages;                     // 2..kMaxStages
+    constexpr int kKb = KIND ? 128 : 64;              // elements per k-block
     const uint32_t x_stage = (uint32_t)mpad * 128u;   // mpad tokens x 64 k x 2 B
     const uint32_t off_x = kStages * kWStage;
     const uint32_t off_misc = off_x + kStages * x_stage;   // multiple of 1024
@@ -194,19 +201,19 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const uint32_t tx = kWStage + (p.x_lsu ? 0u : x_stage);
             for (int it = 0; it < pre; ++it) {
                 mbar_arrive_expect_tx(bar_full(it), tx);
-                load_w(it, (kb_begin + it) * 64);
+                load_w(it, (kb_begin + it) * kKb);
             }
             grid_dependency_wait();
             if (!p.x_lsu)
                 for (int it = 0; it < pre; ++it)
-                    tma_load_2d(base + off_x + it * x_stage, &tmX, bar_full(it), (kb_begin + it) * 64, 0, pol_x);
+                    tma_load_2d(base + off_x + it * x_stage, &tmX, bar_full(it), (kb_begin + it) * kKb, 0, pol_x);
             bool ok = true;
             for (int it = pre; it < nk; ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                 if (!w(bar_empty(s), ph ^ 1u)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar_full(s), tx);
-                const int k0 = (kb_begin + it) * 64;
+                const int k0 = (kb_begin + it) * kKb;
                 load_w(s, k0);
                 if (!p.x_lsu) tma_load_2d(base + off_x + s * x_stage, &tmX, bar_full(s), k0, 0, pol_x);
             }
@@ -229,7 +236,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint64_t adesc = p.w_mn_major ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
                                                         : smem_desc_sw128(sw + kk * 32, 16, 1024);
                     const uint64_t bdesc = smem_desc_sw128(sx + kk * 32, 16, 1024);
-                    tc_mma<1>(tmem, adesc, bdesc, p.idesc, (it | kk) != 0 ? 1u : 0u);
+                    tc_mma<1, KIND>(tmem, adesc, bdesc, p.idesc, (it | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit_1(bar_empty(s));
             }
@@ -246,7 +253,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // per warp) once its copies are complete, up to stages-1 stages behind the
     // issue (the producer of a stage needs the MMA to have drained the stage
     // issued `stages` earlier, which this lag guarantees has been handed over).
-    if (warp >= 2 && p.x_lsu) {
+    if (KIND == 0 && warp >= 2 && p.x_lsu) {   // 16-bit X only
         const int lag = kStages - 1;
         const BoundedWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
         const int et = (int)threadIdx.x - 64;          // 0..127
@@ -435,7 +442,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // shared memory past barrier (2).
 }
 
-template <typename InT, typename OutT>
+template <typename InT, typename OutT, int KIND = 0>
 cudaError_t launch_skinny_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p, int grid,
                                cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -452,18 +459,18 @@ cudaError_t launch_skinny_impl(const CUtensorMap& tmW, const CUtensorMap& tmX, c
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<InT, OutT>, tmW, tmX, p);
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<InT, OutT, KIND>, tmW, tmX, p);
 }
 
-template <typename InT, typename OutT>
+template <typename InT, typename OutT, int KIND = 0>
 cudaError_t prepare_skinny_impl() {
     const int most = 227 * 1024;   // rings are sized on the host; this is the per-CTA ceiling
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         most);
+    auto fn = gemm_skinny_kernel<InT, OutT, KIND>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_skinny_kernel<InT, OutT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 }  // namespace
@@ -479,6 +486,11 @@ cudaError_t skinny_prepare(int dtype) {
         case DT_BF16_BF16: return prepare_skinny_impl<__nv_bfloat16, __nv_bfloat16>();
         case DT_F16_F32: return prepare_skinny_impl<__half, float>();
         case DT_F16_F16: return prepare_skinny_impl<__half, __half>();
+        // fp8 operands (the format is in the instruction descriptor); bf16 bias / scale
+        case DT_E4M3_F32:
+        case DT_E5M2_F32: return prepare_skinny_impl<__nv_bfloat16, float, 1>();
+        case DT_E4M3_BF16:
+        case DT_E5M2_BF16: return prepare_skinny_impl<__nv_bfloat16, __nv_bfloat16, 1>();
     }
     return cudaErrorInvalidValue;
 }
@@ -492,6 +504,10 @@ cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& 
         case DT_BF16_BF16: return launch_skinny_impl<__nv_bfloat16, __nv_bfloat16>(tmW, tmX, p, grid, stream);
         case DT_F16_F32: return launch_skinny_impl<__half, float>(tmW, tmX, p, grid, stream);
         case DT_F16_F16: return launch_skinny_impl<__half, __half>(tmW, tmX, p, grid, stream);
+        case DT_E4M3_F32:
+        case DT_E5M2_F32: return launch_skinny_impl<__nv_bfloat16, float, 1>(tmW, tmX, p, grid, stream);
+        case DT_E4M3_BF16:
+        case DT_E5M2_BF16: return launch_skinny_impl<__nv_bfloat16, __nv_bfloat16, 1>(tmW, tmX, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -62,8 +62,9 @@ typedef enum {
  * (OCP e4m3 / e5m2 bytes, both operands in one format; CMU 15-418 notes,
  * section 2.7: fewer bytes per operand, fp32 accumulation) take bf16 bias and
  * scale vectors, need B stored N x K (plan flag GEMM_B_NK: both operands
- * K-major) and always run on the large-M kernels; per-tensor scale factors go
- * in gemm_run_ex's alpha.  The tf32 types take fp32 A and B in memory, which
+ * K-major) and run on the small-M kernel for M <= 128, on the large-M
+ * kernels otherwise; per-tensor scale factors go in gemm_run_ex's alpha.  The
+ * tf32 types take fp32 A and B in memory, which
  * the tensor cores multiply at tf32 precision (8-bit exponent, 10-bit
  * mantissa; CMU 15-418 notes, section 2.7), with fp32 accumulation; like fp8
  * they take bf16 bias and scale vectors, need GEMM_B_NK and run on the

@@ -47,7 +47,10 @@ def test_fp8_exact_integers(fmt, out, shape, kernel):
         p.set_kernel(kernel)
         p.run(A.cuda(), B.cuda(), C, bias.cuda(), True)
         assert p.status() == 0
-        assert p.last_kernel in (G.KERNEL_TC_PAIR, G.KERNEL_TC_SINGLE)
+        if kernel == G.KERNEL_AUTO and M <= 128:
+            assert p.last_kernel == G.KERNEL_SKINNY          # small M: the weight-streaming kernel
+        else:
+            assert p.last_kernel in (G.KERNEL_TC_PAIR, G.KERNEL_TC_SINGLE)
     ref = oracle.gemm(A, B, bias=bias, relu=True, b_nk=True)
     want = oracle.bf16_round(ref) if out == "bf16" else ref
     got = C.double().cpu().numpy()
@@ -93,10 +96,10 @@ def test_fp8_unsupported_combinations_are_refused():
         with pytest.raises(G.GemmError) as e:
             p.run(A, int_fp8((128, 256), 5, "e4m3").cuda(), C)
         assert e.value.code == G.ERR_UNSUPPORTED
-    with G.Plan(0, "nk") as p:
+    with G.Plan(0, "kn") as p:                  # nor on the small-M kernel
         p.set_kernel(G.KERNEL_SKINNY)
         with pytest.raises(G.GemmError) as e:
-            p.run(A[:16], int_fp8((256, 128), 6, "e4m3").cuda(), C[:16])
+            p.run(A[:16], int_fp8((128, 256), 6, "e4m3").cuda(), C[:16])
         assert e.value.code == G.ERR_UNSUPPORTED
 
 
@@ -116,3 +119,63 @@ def test_fp8_4096_whole_matrix_exact_freivalds():
     rows = np.array([0, 1, 127, 128, 255, 256, 2047, 4095])
     ref = oracle.gemm_rows(A, B, rows, b_nk=True)
     assert np.array_equal(Cc[torch.from_numpy(rows)].double().numpy(), ref)
+
+
+# ---- small M: the weight-streaming kernel with fp8 weights and activations
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 128, 128), (16, 4096, 640), (100, 300, 1000), (128, 1000, 2048), (33, 136, 200)])
+def test_fp8_small_m_exact_integers(fmt, out, shape):
+    M, N, K = shape
+    A = int_fp8((M, K), 7 * M + K, fmt)
+    B = int_fp8((N, K), N + 3 * K, fmt)
+    bias = torch.randint(-8, 9, (N,), generator=torch.Generator().manual_seed(N + 1)).to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), dtype=OUT[out], device="cuda")
+    with G.Plan(0, "nk", b_const=True) as p:
+        p.set_kernel(G.KERNEL_SKINNY)
+        p.run(A.cuda(), B.cuda(), C, bias.cuda(), True)
+        assert p.status() == 0
+        assert p.last_kernel == G.KERNEL_SKINNY
+    ref = oracle.gemm(A, B, bias=bias, relu=True, b_nk=True)
+    want = oracle.bf16_round(ref) if out == "bf16" else ref
+    got = C.double().cpu().numpy()
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[0]}: {got[tuple(bad[0])]} vs {want[tuple(bad[0])]}"
+
+
+def test_fp8_small_m_extended_epilogue_and_packing():
+    M, N, K = 16, 520, 384
+    A = int_fp8((M, K), 21, "e4m3")
+    B = int_fp8((N, K), 22, "e4m3")
+    g = torch.Generator().manual_seed(23)
+    scale = torch.randint(-4, 5, (N,), generator=g).to(torch.bfloat16)
+    bias = torch.randint(-4, 5, (N,), generator=g).to(torch.bfloat16)
+    C0 = torch.randint(-4, 5, (M, N), generator=g).float()
+    # activations with a row pitch of K + 3 bytes: packed first
+    abuf = torch.zeros(M, K + 3, dtype=torch.uint8, device="cuda")
+    abuf[:, :K] = A.view(torch.uint8).cuda()
+    Ad = abuf.view(torch.float8_e4m3fn)[:, :K]
+    C = C0.cuda().clone()
+    with G.Plan(0, "nk") as p:
+        p.run(Ad, B.cuda(), C, bias.cuda(), relu=True, alpha=0.5, beta=2.0, scale=scale.cuda())
+        assert p.status() == 0
+        assert p.last_kernel == G.KERNEL_SKINNY
+    ref, _ = oracle.gemm_ex(A, B, alpha=0.5, beta=2.0, C0=C0, scale=scale, bias=bias, relu=True, b_nk=True)
+    assert np.array_equal(C.double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_small_m_float_inputs_with_scales(fmt):
+    M, N, K = 64, 2048, 4096
+    g = torch.Generator().manual_seed(31)
+    a_scale, b_scale = 0.25, 0.0625
+    A = (torch.randn(M, K, generator=g) / a_scale).to(FMT[fmt])
+    B = (torch.randn(N, K, generator=g) / b_scale).to(FMT[fmt])
+    C = torch.empty(M, N, device="cuda")
+    with G.Plan(0, "nk") as p:
+        p.run(A.cuda(), B.cuda(), C, alpha=a_scale * b_scale)
+        assert p.status() == 0
+        assert p.last_kernel == G.KERNEL_SKINNY
+    C_ref, S = oracle.gemm_ex(A, B, alpha=a_scale * b_scale, b_nk=True)
+    ok, worst, _ = oracle.check_close(C.double().cpu().numpy(), C_ref, S)
+    assert ok, f"worst err/bound {worst:.3f}"
