@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -55,6 +56,7 @@ WORKLOADS = {
     # fused attention forward, B 4 x H 32 x S 4096 x D 128 (M = B*H*S query rows, N = D, K = S keys)
     "attention_b4h32s4096d128": (4 * 32 * 4096, 128, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
     "attention_causal_b4h32s4096d128": (4 * 32 * 4096, 128, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
+    "attention_b4h32s4096d64": (4 * 32 * 4096, 64, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
     # fp8 operands (both K-major: B stored N x K), bf16 output
     "square8192_e4m3": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
     "square8192_e5m2": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
@@ -200,12 +202,16 @@ def fp8_dtype(name):
 PEAK_RATIO = {"e4m3": 2.0, "e5m2": 2.0, "tf32": 1.1 / 2.25}
 
 
-ATTN_SHAPE = (4, 32, 4096, 128)   # B, H, S, D
+def attn_shape(name):
+    """(B, H, S, D) of an attention workload, from its name (..._b4h32s4096d128)."""
+    m = re.search(r"_b(\d+)h(\d+)s(\d+)d(\d+)$", name)
+    return tuple(int(x) for x in m.groups())
 
 
-def attention_flops(causal: bool) -> float:
+def attention_flops(name: str) -> float:
     """4 D FLOPs per visible (query, key) pair: 2 D for the score, 2 D for P V."""
-    B, H, S, D = ATTN_SHAPE
+    causal = "causal" in name
+    B, H, S, D = attn_shape(name)
     pairs = S * (S + 1) / 2 if causal else S * S
     return 4.0 * B * H * D * pairs
 
@@ -216,7 +222,7 @@ def make_inputs(name, device, seed=0):
     M, N, K, lay, (has_bias, relu), out, a_std, b_std = WORKLOADS[name]
     if name.startswith(("attention_",)):
         # q (B, H, S, D) and k, v stacked: (2, B, H, S, D); N(0, 1) bf16
-        B, H, S, D = ATTN_SHAPE
+        B, H, S, D = attn_shape(name)
         q = normal_bf16((B, H, S, D), 3 * seed)
         kv = torch.stack([normal_bf16((B, H, S, D), 3 * seed + 1), normal_bf16((B, H, S, D), 3 * seed + 2)])
         return q, kv, None
@@ -282,7 +288,7 @@ def run_ours(args):
     if args.kernel != "auto":
         plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
     stream = torch.cuda.current_stream(dev)
-    flops = attention_flops(causal) if attn else 2.0 * M * N * K
+    flops = attention_flops(name) if attn else 2.0 * M * N * K
     conv = name.startswith(("conv_implicit", "conv_pool"))
     f8 = fp8_dtype(name)
     if attn:   # q, k, v read once, o written once
@@ -441,8 +447,9 @@ def run_ours(args):
                      f"{kind}, resident in HBM" if f8 is not None else
                      "synthetic: N(0,1) bf16 (torch CPU generator, fixed seeds), resident in HBM"),
             "config": {"workload": name,
-                       **({"B": ATTN_SHAPE[0], "H": ATTN_SHAPE[1], "Sq": ATTN_SHAPE[2], "Sk": ATTN_SHAPE[2],
-                           "D": ATTN_SHAPE[3], "causal": "causal" in name, "scale": "1/sqrt(D)"} if attn else
+                       **({"B": attn_shape(name)[0], "H": attn_shape(name)[1], "Sq": attn_shape(name)[2],
+                           "Sk": attn_shape(name)[2], "D": attn_shape(name)[3], "causal": "causal" in name,
+                           "scale": "1/sqrt(D)"} if attn else
                           {"M": M, "N": N, "K": K, "b_layout": lay, "a_layout": "km" if "_transa_" in name else "mk",
                            "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none"}),
                        "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
@@ -482,7 +489,7 @@ def _oracle_rows_timer(name, A, B, bias):
     threads = len(os.sched_getaffinity(0))
     if name.startswith("attention_"):
         # float64 attention of n seeded heads (numpy); each head is a unit of work
-        Bb, Hh, S, D = ATTN_SHAPE
+        Bb, Hh, S, D = attn_shape(name)
         causal = "causal" in name
         rng = np.random.default_rng(0)
 
@@ -527,8 +534,8 @@ def oracle_unit(name):
     """(FLOPs per unit of oracle work, units in the workload, unit description)."""
     M, N, K, *_ = WORKLOADS[name]
     if name.startswith("attention_"):
-        Bb, Hh, S, D = ATTN_SHAPE
-        return attention_flops("causal" in name) / (Bb * Hh), Bb * Hh, f"heads ({S} x {S} scores, D {D})"
+        Bb, Hh, S, D = attn_shape(name)
+        return attention_flops(name) / (Bb * Hh), Bb * Hh, f"heads ({S} x {S} scores, D {D})"
     return 2.0 * N * K, M, f"rows of C (each {N} x {K} MACs)"
 
 
