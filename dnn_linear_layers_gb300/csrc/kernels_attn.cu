@@ -6,32 +6,35 @@
 // to FlashAttention" and the devpress.csdn.net notes, section 4 (Q, K, V in
 // blocks that stay on chip).
 //
-// Design for sm_103a, one CTA per 128 queries of one head:
-//   * warp 0: TMA producer -- Q once, K_j and V_j (128 keys each) into
-//     2-stage rings (3-D tensor maps: keys past Sk read as zero).  K runs one
+// Design for sm_103a: persistent CTAs, one per SM, each walking work items of
+// 128 queries of one head (see attn_item below); per CTA:
+//   * warp 0: TMA producer -- Q of each item, K_j and V_j (128 keys each) into
+//     3-slot rings (3-D tensor maps: keys past Sk read as zero).  K runs one
 //     block ahead of V (a K slot frees when its score product is done, a V
-//     slot only when its PV product is), so the next K block is on chip before
-//     the tensor core wants it;
+//     slot only when its PV product is), and the next item's Q and first K
+//     blocks load while the current item's last blocks run;
 //   * warps 1 and 2: MMA issuers -- warp 1 S_j = Q K_j^T into one of two TMEM
 //     score buffers (S_{j+1} is computed while the softmax works on S_j), warp
-//     2 O += P_j V_j into the TMEM accumulator once P_j is ready.  An MMA
-//     instruction is accepted only as the tensor pipe drains, so one thread
-//     issuing both products would leave the pipe idle while it waited for the
-//     other's operands; two threads keep it fed from whichever is ready;
+//     2 O += P_j V_j into the TMEM accumulator once P_j is ready, with P read
+//     from TMEM as the A operand.  An MMA instruction is accepted only as the
+//     tensor pipe drains, so one thread issuing both products would leave the
+//     pipe idle while it waited for the other's operands; two threads keep it
+//     fed from whichever is ready;
 //   * warps 3..10: softmax in two groups of four warps that take the key blocks
-//     in turn (group 0 the even ones, group 1 the odd ones), one thread per
-//     query row (TMEM lane) in each, so the two warps that share an SM
-//     sub-partition work on different blocks and hide each other's latency.
-//     A row's reference max passes from group to group once per block through
-//     shared memory behind a (bounded) mbarrier; each group keeps a partial
-//     row sum until the end.  Each thread reads its 128 scores from TMEM once
-//     (the score buffer is handed back at once), P = 2^(s - m) is written
-//     as bf16 / fp16 into one of two 128-byte-swizzled shared-memory tiles
-//     (the A operand of the PV product; two, so P_j is written while P_{j-1} V
-//     runs).  The reference max m of a row moves only when the block max
-//     exceeds it by more than 8 (a factor 2^8): O = sum_j 2^(s_j - m) v_j /
-//     sum_j 2^(s_j - m) holds for any m, so a stale m changes nothing but the
-//     rounding, and the accumulator row is rescaled in TMEM only then.
+//     in turn, one thread per query row (TMEM lane) in each, so the two warps
+//     that share an SM sub-partition work on different blocks and hide each
+//     other's latency.  A row's reference max passes from group to group once
+//     per block through shared memory behind a (bounded) mbarrier; each group
+//     keeps its share of the row sum until the end of the item, when the group
+//     of the last block adds the other's share and writes O / l out while the
+//     other group starts the next item.  Each thread reads its 128 scores from
+//     TMEM once (the score buffer is handed back at once) and writes
+//     P = 2^(s - m) as bf16 / fp16, two per column, into its group's 64-column
+//     TMEM tile (two tiles, so P_j is written while P_{j-1} V runs).  The
+//     reference max m of a row moves only when the block max exceeds it by more
+//     than 8 (a factor 2^8): O = sum_j 2^(s_j - m) v_j / sum_j 2^(s_j - m) holds
+//     for any m, so a stale m changes nothing but the rounding, and the
+//     accumulator row is rescaled in TMEM only then.
 // Scores are taken in base 2 (scale * log2 e folded into one factor).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

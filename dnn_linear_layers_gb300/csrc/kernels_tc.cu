@@ -12,11 +12,17 @@
 //   * one CTA owns 128 rows x 256 columns of the output; with cta_group::2 a
 //     pair of CTAs (a 2-CTA cluster) issues 256 x 256 x 16 MMAs, each CTA
 //     holding half of A's rows and half of B's columns in its own smem;
-//   * k-blocks of 64 elements = one 128-byte swizzle row; a ring of stages
-//     (6 for a pair, 4 for a single CTA) keeps TMA loads ahead of the MMAs;
+//   * a k-block is one 128-byte swizzle row: 64 16-bit elements (kind::f16),
+//     128 fp8 (kind::f8f6f4) or 32 tf32 (kind::tf32), four MMAs of 32 bytes
+//     each; a ring of stages (6 for a pair, 4 for a single CTA) keeps TMA loads
+//     ahead of the MMAs.  A (M x K, or K x M read MN-major) and B (N x K, or
+//     K x N read MN-major) come from 2-D tensor maps; for an implicit-GEMM
+//     convolution A comes through an im2col map of the NHWC activations (two
+//     maps, top and bottom rows of each row pair, for the fused max-pool);
 //   * warp 0 issues TMA loads, warp 1 issues MMAs (leader CTA only) and owns
 //     the TMEM allocation, warps 2-5 run the epilogue: TMEM -> registers ->
-//     (+bias, ReLU, cast) -> swizzled smem -> TMA store;
+//     (alpha, per-column scale, +bias, +beta C, ReLU, cast) -> swizzled smem ->
+//     TMA store, or for the fused max-pool the 2 x 2 maximum of each window;
 //   * the accumulator is double buffered in TMEM (2 x 256 fp32 columns), so
 //     the epilogue of one tile overlaps the main loop of the next;
 //   * the grid is persistent (one CTA per SM) and walks the output tiles in
