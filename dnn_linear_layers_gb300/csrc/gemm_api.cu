@@ -1,8 +1,11 @@
 // C-ABI layer: plans, argument validation, TMA tensor maps, operand packing
 // and kernel dispatch.  The interface mirrors the BLAS GEMM call of
-// youngju.dev "GEMM to FlashAttention" ("GEMM interface": m, n, k, lda, ldb,
-// ldc, transb) and the handle create/use/destroy pattern of its cuBLAS
-// example, for row-major operands and alpha = 1, beta = 0.
+// youngju.dev "GEMM to FlashAttention" ("GEMM interface": m, n, k, alpha, lda,
+// ldb, beta, ldc, transa / transb) and the handle create/use/destroy pattern of
+// its cuBLAS example, for row-major operands: gemm_run is the alpha = 1,
+// beta = 0 form, gemm_run_ex the general one; plan flags give transa
+// (GEMM_A_KM) and transb (GEMM_B_NK).  The convolution and attention entry
+// points build their tensor maps here too.
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
