@@ -112,3 +112,30 @@ def test_odd_shapes(plans, idx):
     A, B, bias, C = run_full(plans, case)
     check_sampled(case, A, B, bias, C, n_random=16)
     freivalds(case, A, B, bias, C, trials=1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_full_size_sampled_heads(plans, causal):
+    """The benchmark's attention workload (B 4, H 32, S 4096, D 128, bf16 in and
+    out, seeded N(0, 1) inputs) in its launch configuration; eight seeded heads
+    are checked against the float64 oracle, every output of each, with the
+    bound of the attention parity tests (2 u max_j |V_jd| + 1e-5 plus one bf16
+    ulp of the output, u = 2^-9)."""
+    from dnn_linear_layers_gb300.inputs import normal_bf16
+    B, H, S, D = 4, 32, 4096, 128
+    q = normal_bf16((B, H, S, D), 0)
+    k = normal_bf16((B, H, S, D), 1)
+    v = normal_bf16((B, H, S, D), 2)
+    o = torch.empty(B, H, S, D, dtype=torch.bfloat16, device="cuda")
+    p = plans["nk"]
+    p.attention(q.cuda(), k.cuda(), v.cuda(), o, causal=causal)
+    assert p.status() == 0
+    got = o.view(B * H, S, D).double().cpu().numpy()
+    qf, kf, vf = (t.view(B * H, S, D) for t in (q, k, v))
+    heads = np.random.default_rng(5 + causal).choice(B * H, size=8, replace=False)
+    for hd in heads:
+        ref = oracle.attention(qf[hd], kf[hd], vf[hd], causal=causal)
+        vmax = np.abs(oracle._f64(vf[hd])).max(axis=0, keepdims=True)
+        bound = 2 * 2.0 ** -9 * vmax + 1e-5 + oracle.ulp_bf16(ref)
+        err = np.abs(got[hd] - ref)
+        assert np.all(err <= bound), f"head {hd}: worst err/bound {(err / bound).max():.3f}"

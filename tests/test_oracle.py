@@ -437,3 +437,32 @@ def test_attention_closed_forms():
     # a query that sees no key gets zeros (causal, more queries than keys)
     Oz = oracle.attention(rng.standard_normal((6, D)), K[:3], V[:3], causal=True)
     assert np.array_equal(Oz[:3], np.zeros((3, D))) and np.all(Oz[3:] != 0)
+
+
+def test_attention_matches_the_tiled_online_softmax_recurrence():
+    """The oracle materialises the softmax; the FlashAttention recurrence of the
+    pages (keys in tiles, a running row max m, a running sum l and the
+    accumulator rescaled by e^(m_old - m_new) whenever m grows) reaches the same
+    result without it.  Written out here with tiles of three keys, it must agree
+    with the oracle to rounding, with and without the causal mask."""
+    rng = np.random.default_rng(61)
+    for Sq, Sk, D, causal in [(5, 7, 4, False), (6, 9, 3, True), (4, 4, 2, True), (8, 3, 5, True)]:
+        Q = rng.standard_normal((Sq, D)); K = rng.standard_normal((Sk, D)); V = rng.standard_normal((Sk, D))
+        s = 1.0 / np.sqrt(D)
+        out = np.zeros((Sq, D))
+        for i in range(Sq):
+            m, l, acc = -np.inf, 0.0, np.zeros(D)
+            for t0 in range(0, Sk, 3):
+                keys = [j for j in range(t0, min(t0 + 3, Sk)) if not causal or j <= i + (Sk - Sq)]
+                if not keys:
+                    continue
+                sc = np.array([s * float(Q[i] @ K[j]) for j in keys])
+                m_new = max(m, float(sc.max()))
+                f = np.exp(m - m_new) if np.isfinite(m) else 0.0
+                p = np.exp(sc - m_new)
+                l = l * f + float(p.sum())
+                acc = acc * f + p @ V[keys]
+                m = m_new
+            out[i] = acc / l if l > 0 else 0.0
+        assert np.allclose(oracle.attention(Q, K, V, causal=causal), out, rtol=0, atol=1e-13)
+
