@@ -246,15 +246,12 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     const int kbk = 128 / es;                         // elements per 128-byte k-block row
     const int64_t nkb = (K + kbk - 1) / kbk;
     if (n_tiles > INT32_MAX / 8) return GEMM_ERR_UNSUPPORTED;
-    // Weight bytes in flight decide the bandwidth, and only resident CTAs have
-    // loads in flight: take the largest split count S whose grid (n_tiles * S
-    // CTAs) fits on the SMs at once with a ring of at least 3 stages.
     // Bandwidth follows the weight bytes in flight, and only resident CTAs have
-    // loads in flight.  Candidates (splits S <= 8, ring depth >= 3) are kept
-    // when the whole grid fits on the SMs with 20% headroom for placing
-    // clusters inside GPCs; the one with the most weight bytes in flight
-    // (counting at most four stages per CTA) wins, ties going to more CTAs.  (Measured on GB300: grids at the residency
-    // limit fall into a second wave, and 16-CTA clusters were slower.)
+    // loads in flight.  Candidates (splits S <= 8, ring depth 3..4, or 2 for an
+    // unsplit K) are kept when the whole grid fits on the SMs with 20% headroom
+    // for placing clusters inside GPCs; the one with the most weight bytes in
+    // flight wins, ties going to more CTAs.  (Measured on GB300: grids at the
+    // residency limit fall into a second wave, and 16-CTA clusters were slower.)
     const int64_t stage_bytes = 16384 + (int64_t)mpad * 128;
     int S = 1, stages = 2;
     int64_t best = -1;
@@ -263,7 +260,10 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
         if (p->skinny_splits && cand != p->skinny_splits) continue;
         const int64_t ctas = n_tiles * cand;
         const int64_t kb_per_slice = nkb / cand;
-        for (int st = 8; st >= 2; --st) {
+        // rings deeper than four stages earn nothing (below) and measured slower
+        // (M = 1 and 16 at 4096 -> 14336: 2 x 4 beats 2 x 6 by 2%): the search
+        // starts at four unless a depth is forced
+        for (int st = p->skinny_stages ? 8 : 4; st >= 2; --st) {
             if (p->skinny_stages && st != p->skinny_stages) continue;
             if (st < 3 && !p->skinny_stages && cand > 1) continue;
             const int64_t smem = skinny_smem_bytes(mpad, st);
