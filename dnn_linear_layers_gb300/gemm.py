@@ -349,6 +349,16 @@ def conv2d(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None, r
     return _plan_for(x.device, "nk").conv2d(x, w, out, bias, relu, pad)
 
 
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+              scale: float | None = None, out_dtype: torch.dtype | None = None, out: torch.Tensor | None = None):
+    """Attention forward o = softmax(scale * q k^T) v per (batch, head): q is
+    [B, H, Sq, D], k and v [B, H, Sk, D] (D 64 or 128, bf16 or fp16); scale None
+    means 1 / sqrt(D); causal: key j visible to query i iff j <= i + (Sk - Sq)."""
+    if out is None:
+        out = torch.empty(tuple(q.shape), device=q.device, dtype=out_dtype or q.dtype)
+    return _plan_for(q.device, "nk").attention(q, k, v, out, scale=0.0 if scale is None else scale, causal=causal)
+
+
 def im2col(x: torch.Tensor, R: int, S: int, pad: int = 0, stride: int = 1, out: torch.Tensor | None = None):
     """Explicit-GEMM matrix of an R x S convolution of the NHWC tensor ``x``."""
     if x.dim() != 4 or not x.is_contiguous() or x.device.type != "cuda":

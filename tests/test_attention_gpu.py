@@ -130,3 +130,19 @@ def test_attention_bounded_wait_reports_timeout_and_context_survives():
         ref = oracle.attention(q, k, v)
         vmax = np.abs(oracle._f64(v)).max(axis=-2, keepdims=True)
         assert np.all(np.abs(o.double().cpu().numpy() - ref) <= 2 * 2.0 ** -9 * vmax + 1e-5)
+
+
+def test_attention_module_function():
+    # gemm.attention allocates the output (the input dtype unless told otherwise)
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    g = torch.Generator().manual_seed(70)
+    q = torch.randn(2, 3, 200, 64, generator=g).bfloat16()
+    k = torch.randn(2, 3, 260, 64, generator=g).bfloat16()
+    v = torch.randn(2, 3, 260, 64, generator=g).bfloat16()
+    o = G.attention(q.cuda(), k.cuda(), v.cuda(), causal=True, out_dtype=torch.float32)
+    assert o.dtype == torch.float32 and tuple(o.shape) == (2, 3, 200, 64)
+    ref = oracle.attention(q, k, v, causal=True)
+    vmax = np.abs(oracle._f64(v)).max(axis=-2, keepdims=True)
+    assert np.all(np.abs(o.double().cpu().numpy() - ref) <= 2 * 2.0 ** -9 * vmax + 1e-5)
+
