@@ -68,3 +68,32 @@ def test_reference_arm_non_zero_rank_does_nothing(monkeypatch):
         workload, steps, warmup, cpu_seconds = "square8192_bf16", 1, 3, 1.0
 
     assert bench.run_reference(Args()) is None
+
+
+def test_attention_workload_shapes_and_flops():
+    assert bench.attn_shape("attention_b4h32s4096d128") == (4, 32, 4096, 128)
+    assert bench.attn_shape("attention_causal_b4h32s4096d128") == (4, 32, 4096, 128)
+    assert bench.attn_shape("attention_b4h32s4096d64") == (4, 32, 4096, 64)
+    B, H, S, D = 4, 32, 4096, 128
+    # two products of 2 D FLOPs per (query, key) pair: every pair, or the
+    # S (S + 1) / 2 pairs on and below the diagonal under the causal mask
+    assert bench.attention_flops("attention_b4h32s4096d128") == 4.0 * B * H * S * S * D
+    assert bench.attention_flops("attention_causal_b4h32s4096d128") == 4.0 * B * H * D * S * (S + 1) / 2
+    # the oracle's unit of work is one head, and the heads add up to the workload
+    per, total, _ = bench.oracle_unit("attention_causal_b4h32s4096d128")
+    assert total == B * H and per * total == bench.attention_flops("attention_causal_b4h32s4096d128")
+
+
+def test_gemm_oracle_unit_and_operand_types():
+    import torch
+    per, total, _ = bench.oracle_unit("square8192_bf16")
+    assert total == 8192 and per == 2.0 * 8192 * 8192          # one row of C
+    assert bench.fp8_dtype("square8192_e4m3") == torch.float8_e4m3fn
+    assert bench.fp8_dtype("square8192_e5m2") == torch.float8_e5m2
+    assert bench.fp8_dtype("square8192_tf32") == torch.float32
+    assert bench.fp8_dtype("square8192_bf16") is None
+    # nominal dense rates relative to bf16: fp8 2x, tf32 1.1 / 2.25
+    assert bench.PEAK_RATIO["e4m3"] == bench.PEAK_RATIO["e5m2"] == 2.0
+    assert abs(bench.PEAK_RATIO["tf32"] - 1.1 / 2.25) < 1e-12
+    for name, (M, N, K, lay, *_rest) in bench.WORKLOADS.items():
+        assert M > 0 and N > 0 and K > 0 and lay in ("kn", "nk"), name
