@@ -120,3 +120,23 @@ def test_conv2d_rejects_null_plan(lib):
 def test_run_ex_rejects_null_plan_and_args(lib):
     ea = G.EpilogueArgs(1.0, 0.0, None, None, 0)
     assert G.lib().gemm_run_ex(None, 8, 8, 8, P, 8, P, 8, P, 8, ctypes.byref(ea), 1, None) == G.ERR_INVALID_ARG
+
+
+def test_noalloc_refuses_the_operand_forms_it_does_not_take(lib):
+    # checked after argument validation and before any CUDA call
+    args = dict(M=64, N=64, K=64, lda=64, ldb=64, ldc=64)
+    def call(dtype, flags):
+        return lib.gemm_run_noalloc(args["M"], args["N"], args["K"], P, args["lda"], P, args["ldb"], None, P,
+                                    args["ldc"], 0, dtype, flags, None, None)
+    for dtype in (G.E4M3_F32OUT, G.E5M2_BF16OUT, G.TF32_F32OUT, G.TF32_BF16OUT):
+        assert call(dtype, G.B_NK) == G.ERR_UNSUPPORTED
+    assert call(G.BF16_F32OUT, G.A_KM) == G.ERR_UNSUPPORTED
+
+
+def test_attention_rejects_null_plan_and_bad_arguments(lib):
+    assert lib.gemm_attention(None, 1, 1, 8, 8, 64, P, P, P, P, 0.0, 0, G.BF16_F32OUT, None) == G.ERR_INVALID_ARG
+
+
+def test_conv2d_maxpool_rejects_null_plan(lib):
+    assert lib.gemm_conv2d_maxpool(None, 1, 4, 4, 64, 64, 3, 3, 1, P, P, P, 64, None, G.BF16_BF16OUT,
+                                   None) == G.ERR_INVALID_ARG
