@@ -21,10 +21,8 @@ struct gemm_plan {
     int device = 0;
     unsigned flags = 0;
     int sm_count = 0;
-    int max_pairs = 0;        // co-resident 2-CTA clusters
-    int max_singles = 0;      // co-resident single CTAs
-    int max_quads = 0;        // co-resident clusters of two CTA pairs
-    int multicast = 0;        // share B between two pairs by TMA multicast when M > 256
+    int max_pairs[kNumDtypes] = {};     // co-resident 2-CTA clusters, per operand type
+    int max_singles[kNumDtypes] = {};   // co-resident single CTAs, per operand type
     int* status_dev = nullptr;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
@@ -38,7 +36,7 @@ struct gemm_plan {
     int group_m = 8;
     unsigned l2_policy = 0;
     unsigned pdl = 1;             // programmatic dependent launch of the GEMM kernels
-    int debug_log = 0;            // GB300_GEMM_DEBUG=1: one line per launch on stderr
+    int debug_log = 0;            // GEMM_OPT_LOG: one line per launch on stderr
     int tail_split = 1;           // split the last wave's tiles into N-halves
     int k_snake = 1;              // serpentine k order across a worker's tiles (measured: -30% DRAM reads)
     int skinny_splits = 0;        // 0: automatic; otherwise forced split count (sweeps)
@@ -327,7 +325,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_RELU) return GEMM_ERR_INVALID_ARG;
     if (dtype < GEMM_BF16_F32OUT || dtype > GEMM_TF32_BF16OUT) return GEMM_ERR_INVALID_ARG;
-    if (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST | GEMM_A_KM)) return GEMM_ERR_INVALID_ARG;
+    if (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_A_KM)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
     if ((epilogue & GEMM_EPI_BIAS) && bias == nullptr) return GEMM_ERR_INVALID_ARG;
@@ -341,7 +339,7 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
 }
 
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
-    if (plan == nullptr || device < 0 || (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_TC_MULTICAST | GEMM_A_KM)))
+    if (plan == nullptr || device < 0 || (flags & ~(GEMM_B_NK | GEMM_B_CONST | GEMM_A_KM)))
         return GEMM_ERR_INVALID_ARG;
     int ndev = 0;
     cudaError_t e = cudaGetDeviceCount(&ndev);
@@ -352,24 +350,23 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     if (!p) return GEMM_ERR_NO_MEMORY;
     p->device = device;
     p->flags = flags;
-    p->multicast = (flags & GEMM_TC_MULTICAST) ? 1 : 0;
     DeviceGuard g(device);
     cudaDeviceProp prop;
     e = cudaGetDeviceProperties(&prop, device);
     if (e != cudaSuccess) { delete p; return GEMM_ERR_CUDA; }
     if (prop.major * 10 + prop.minor < 100) { delete p; return GEMM_ERR_UNSUPPORTED; }
     p->sm_count = prop.multiProcessorCount;
+    // co-residency of the tensor-core kernels, kept per operand type (each type
+    // is its own instantiation, with its own register count)
     for (int dt = 0; dt < kNumDtypes; ++dt) {
         int n2 = 0, n1 = 0;
-        int n4 = 0, unused = 0;
-        e = tc_prepare(2, dt, &n2, &n4);
-        if (e == cudaSuccess) e = tc_prepare(1, dt, &n1, &unused);
-        p->max_quads = n4;
+        e = tc_prepare(2, dt, &n2);
+        if (e == cudaSuccess) e = tc_prepare(1, dt, &n1);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
-        p->max_pairs = n2;
-        p->max_singles = n1;
+        if (n2 < 1 || n1 < 1) { delete p; return GEMM_ERR_UNSUPPORTED; }
+        p->max_pairs[dt] = n2;
+        p->max_singles[dt] = n1;
     }
-    if (p->max_pairs < 1 || p->max_singles < 1) { delete p; return GEMM_ERR_UNSUPPORTED; }
     for (int dt = 0; dt < 4; ++dt) {
         e = attention_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
@@ -384,31 +381,6 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     if (e != cudaSuccess) { delete p; return GEMM_ERR_NO_MEMORY; }
     e = cudaMemset(p->status_dev, 0, sizeof(int));
     if (e != cudaSuccess) { cudaFree(p->status_dev); delete p; return GEMM_ERR_CUDA; }
-    // tuning overrides for benchmarking sweeps only
-    if (const char* s = std::getenv("GB300_GEMM_GROUP_M")) {
-        int v = std::atoi(s);
-        if (v >= 1 && v <= 1024) p->group_m = v;
-    }
-    if (const char* s = std::getenv("GB300_GEMM_DEBUG")) p->debug_log = std::atoi(s) != 0;
-    if (const char* s = std::getenv("GB300_GEMM_NO_TAIL_SPLIT")) p->tail_split = std::atoi(s) == 0;
-    if (const char* s = std::getenv("GB300_GEMM_K_SNAKE")) p->k_snake = std::atoi(s) != 0;
-    if (const char* s = std::getenv("GB300_GEMM_MC")) p->multicast = std::atoi(s) != 0;
-    if (const char* s = std::getenv("GB300_GEMM_SKINNY_X_LSU")) p->skinny_x_lsu = std::atoi(s) != 0;
-    if (const char* s = std::getenv("GB300_GEMM_SKINNY_SPLITS")) {
-        int v = std::atoi(s);
-        if (v == 1 || v == 2 || v == 4 || v == 8) p->skinny_splits = v;
-    }
-    if (const char* s = std::getenv("GB300_GEMM_SKINNY_STAGES")) {
-        int v = std::atoi(s);
-        if (v >= 2 && v <= 8) p->skinny_stages = v;
-    }
-    if (const char* s = std::getenv("GB300_GEMM_NO_PDL")) {
-        if (std::atoi(s) != 0) p->pdl = 0;
-    }
-    if (const char* s = std::getenv("GB300_GEMM_L2_POLICY")) {
-        int v = std::atoi(s);
-        if (v >= 0 && v <= 2) p->l2_policy = (unsigned)v;
-    }
     *plan = p;
     return GEMM_OK;
 }
@@ -450,6 +422,57 @@ int gemm_plan_set_debug(gemm_plan_t p, unsigned flags) {
     if (!p) return GEMM_ERR_INVALID_ARG;
     p->debug = flags;
     return GEMM_OK;
+}
+
+int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    const bool b01 = v == 0 || v == 1;
+    switch (option) {
+        case GEMM_OPT_GROUP_M:
+            if (v < 1 || v > 1024) return GEMM_ERR_INVALID_ARG;
+            p->group_m = (int)v; return GEMM_OK;
+        case GEMM_OPT_TAIL_SPLIT:
+            if (!b01) return GEMM_ERR_INVALID_ARG;
+            p->tail_split = (int)v; return GEMM_OK;
+        case GEMM_OPT_K_SNAKE:
+            if (!b01) return GEMM_ERR_INVALID_ARG;
+            p->k_snake = (int)v; return GEMM_OK;
+        case GEMM_OPT_PDL:
+            if (!b01) return GEMM_ERR_INVALID_ARG;
+            p->pdl = (unsigned)v; return GEMM_OK;
+        case GEMM_OPT_L2_POLICY:
+            if (v < 0 || v > 2) return GEMM_ERR_INVALID_ARG;
+            p->l2_policy = (unsigned)v; return GEMM_OK;
+        case GEMM_OPT_SKINNY_SPLITS:
+            if (v != 0 && v != 1 && v != 2 && v != 4 && v != 8) return GEMM_ERR_INVALID_ARG;
+            p->skinny_splits = (int)v; return GEMM_OK;
+        case GEMM_OPT_SKINNY_STAGES:
+            if (v != 0 && (v < 2 || v > 8)) return GEMM_ERR_INVALID_ARG;
+            p->skinny_stages = (int)v; return GEMM_OK;
+        case GEMM_OPT_SKINNY_X_LSU:
+            if (!b01) return GEMM_ERR_INVALID_ARG;
+            p->skinny_x_lsu = (int)v; return GEMM_OK;
+        case GEMM_OPT_LOG:
+            if (!b01) return GEMM_ERR_INVALID_ARG;
+            p->debug_log = (int)v; return GEMM_OK;
+    }
+    return GEMM_ERR_INVALID_ARG;
+}
+
+int gemm_plan_get_option(gemm_plan_t p, int option, int64_t* v) {
+    if (!p || !v) return GEMM_ERR_INVALID_ARG;
+    switch (option) {
+        case GEMM_OPT_GROUP_M: *v = p->group_m; return GEMM_OK;
+        case GEMM_OPT_TAIL_SPLIT: *v = p->tail_split; return GEMM_OK;
+        case GEMM_OPT_K_SNAKE: *v = p->k_snake; return GEMM_OK;
+        case GEMM_OPT_PDL: *v = p->pdl; return GEMM_OK;
+        case GEMM_OPT_L2_POLICY: *v = p->l2_policy; return GEMM_OK;
+        case GEMM_OPT_SKINNY_SPLITS: *v = p->skinny_splits; return GEMM_OK;
+        case GEMM_OPT_SKINNY_STAGES: *v = p->skinny_stages; return GEMM_OK;
+        case GEMM_OPT_SKINNY_X_LSU: *v = p->skinny_x_lsu; return GEMM_OK;
+        case GEMM_OPT_LOG: *v = p->debug_log; return GEMM_OK;
+    }
+    return GEMM_ERR_INVALID_ARG;
 }
 
 int gemm_plan_status(gemm_plan_t p) {
@@ -558,8 +581,6 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         return GEMM_ERR_UNSUPPORTED;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
     const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
-    // two pairs per cluster sharing B: only when there are rows for both
-    const int mc = (cg == 2 && p->multicast && p->max_quads > 0 && M > TC_BM * 2) ? 2 : 1;
 
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
     const int ob = out_bytes(dtype);
@@ -620,9 +641,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * es, kbk, TC_BM)) {
         return GEMM_ERR_CUDA;
     }
-    bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * es, kbk,
-                               mc == 2 ? 64 : TC_BN / cg)
-                    : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * 2, 64, TC_BK);
+    // N x K B: one box of the CTA's columns per k-block row; K x N B (16-bit
+    // only, checked above): 64-column boxes, TC_BK k-rows each
+    bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * es, kbk, TC_BN / cg)
+                    : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * es, 64, TC_BK);
     if (!okb) return GEMM_ERR_CUDA;
     if (!make_map(&tmC, out_dt, C_use, (uint64_t)N, (uint64_t)M, (uint64_t)ldc_use * ob, 128 / ob, 32))
         return GEMM_ERR_CUDA;
@@ -630,7 +652,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
     prm.M = (int32_t)M; prm.N = (int32_t)N; prm.K = (int32_t)K;
-    prm.num_m_tiles = (int32_t)((M + TC_BM * cg * mc - 1) / (TC_BM * cg * mc));
+    prm.num_m_tiles = (int32_t)((M + TC_BM * cg - 1) / (TC_BM * cg));
     prm.num_n_tiles = (int32_t)((N + TC_BN - 1) / TC_BN);
     prm.num_k_blocks = (int32_t)((K + kbk - 1) / kbk);
     prm.group_m = p->group_m;
@@ -665,16 +687,15 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     }
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
-    const int64_t cap = mc == 2 ? p->max_quads : (cg == 2 ? p->max_pairs : p->max_singles);
+    const int64_t cap = cg == 2 ? p->max_pairs[dtype] : p->max_singles[dtype];
     const int64_t units = tiles < cap ? tiles : cap;
-    prm.multicast = mc == 2 ? 1u : 0u;
     prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
     prm.idesc_half = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN / 2, a_km);
     if (p->debug_log)
-        std::fprintf(stderr, "[gemm] tc cta_group=%d mc=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
-                     cg, mc, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
-                     (long long)(units * cg * mc), A_use != A, B_use != B, C_use != C);
-    e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg * mc), stream,
+        std::fprintf(stderr, "[gemm] tc cta_group=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
+                     cg, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
+                     (long long)(units * cg), A_use != A, B_use != B, C_use != C);
+    e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream,
                        (conv && conv->pool) ? &tmA2 : nullptr);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;

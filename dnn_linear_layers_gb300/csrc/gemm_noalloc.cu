@@ -41,8 +41,8 @@ constexpr int kMaxDevices = 64;
 struct DeviceSetup {
     bool ready = false;
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
-    int max_pairs = 0;
-    int max_singles = 0;
+    int max_pairs[4] = {};     // co-resident CTA pairs, per 16-bit operand type
+    int max_singles[4] = {};   // co-resident single CTAs, per 16-bit operand type
 };
 
 DeviceSetup g_setup[kMaxDevices];
@@ -63,14 +63,13 @@ int setup_device(int dev, DeviceSetup** out) {
         void* addr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
         if (e != cudaSuccess || addr == nullptr) { cudaGetLastError(); return GEMM_ERR_CUDA; }
-        int n2 = 0, n1 = 0;
+        int n2[4] = {}, n1[4] = {};
         for (int dt = 0; dt < 4; ++dt) {
-            int n4 = 0;
-            e = gb300::tc_prepare(2, dt, &n2, &n4);
-            if (e == cudaSuccess) e = gb300::tc_prepare(1, dt, &n1, &n4);
+            e = gb300::tc_prepare(2, dt, &n2[dt]);
+            if (e == cudaSuccess) e = gb300::tc_prepare(1, dt, &n1[dt]);
             if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+            if (n2[dt] < 1 || n1[dt] < 1) return GEMM_ERR_UNSUPPORTED;
         }
-        if (n2 < 1 || n1 < 1) return GEMM_ERR_UNSUPPORTED;
         if (!g_encode_na) {
             void* fn = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -80,8 +79,10 @@ int setup_device(int dev, DeviceSetup** out) {
             g_encode_na = reinterpret_cast<EncodeTiledFn>(fn);
         }
         s.scratch = static_cast<unsigned char*>(addr);
-        s.max_pairs = n2;
-        s.max_singles = n1;
+        for (int dt = 0; dt < 4; ++dt) {
+            s.max_pairs[dt] = n2[dt];
+            s.max_singles[dt] = n1[dt];
+        }
         s.ready = true;
     }
     *out = &s;
@@ -107,10 +108,12 @@ int64_t rup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                                 int64_t ldb, const void* bias, void* C, int64_t ldc, int epilogue, int dtype,
                                 unsigned flags, int* dev_status, void* stream_v) {
+    // only the B-layout flag applies here: no plan to hold constant weights
+    // or a transposed A
+    if (flags & ~GEMM_B_NK) return GEMM_ERR_INVALID_ARG;
     int rc = gemm_validate(flags, M, N, K, A, lda, B, ldb, bias, C, ldc, epilogue, dtype);
     if (rc == GEMM_OK && (gb300::dtype_is_fp8(dtype) || gb300::dtype_is_tf32(dtype)))
         rc = GEMM_ERR_UNSUPPORTED;   // 16-bit inputs only
-    if (rc == GEMM_OK && (flags & GEMM_A_KM)) rc = GEMM_ERR_UNSUPPORTED;           // M x K A only
     if (rc != GEMM_OK) return rc;
     if (M == 0 || N == 0) return GEMM_OK;
     const bool b_nk = (flags & GEMM_B_NK) != 0;
@@ -201,7 +204,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     prm.num_full = prm.num_m_tiles * prm.num_n_tiles;   // whole tiles only
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
-    const int64_t cap = (cg == 2) ? s->max_pairs : s->max_singles;
+    const int64_t cap = (cg == 2) ? s->max_pairs[dtype] : s->max_singles[dtype];
     const int64_t units = tiles < cap ? tiles : cap;
     e = gb300::launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;

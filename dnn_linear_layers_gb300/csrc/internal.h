@@ -72,7 +72,6 @@ struct TcParams {
     uint32_t l2_policy;    // 0: A evict_last, B evict_normal; 1: A normal, B last; 2: both normal
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
-    uint32_t multicast;    // 1: clusters of two CTA pairs share B by TMA multicast (cta_group 2)
     EpiArgs ex;            // alpha / scale / beta operands of the epilogue
     // Implicit-GEMM convolution (conv != 0): A is not a matrix but an NHWC
     // activation tensor read through an im2col tensor map; row m of A is
@@ -108,9 +107,9 @@ cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, con
 int tc_smem_bytes(int cta_group);
 
 // Configure kernel attributes (dynamic smem) and report the largest number of
-// co-resident clusters (cta_group 2: pairs, and clusters of two pairs in
-// *max_quads) or CTAs (cta_group 1) on this device.
-cudaError_t tc_prepare(int cta_group, int dtype, int* max_units, int* max_quads);
+// co-resident clusters (cta_group 2: CTA pairs) or CTAs (cta_group 1) on this
+// device.
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units);
 
 // Skinny-M (M <= 128) Linear layer: weight-streaming tcgen05 kernel ------
 struct SkinnyParams {

@@ -174,12 +174,9 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
     return v;
 }
 
-// MC = number of CTA pairs in a cluster (1 or 2, CG = 2 only).  With MC = 2
-// the two pairs work on vertically adjacent 256-row tiles of the same 256
-// columns, so their B tiles are identical: each pair fetches half of it and
-// multicasts it to both, halving the B reads out of L2.  A stage may then be
-// refilled only when both pairs' MMAs are done with it.
-template <int CG, int MC, typename InT, typename OutT, int KIND>
+// CG = CTAs per cluster (1, or 2 for a CTA pair issuing cta_group::2 MMAs).
+// Each CTA fetches its own operand tiles: no copy is shared across CTAs.
+template <int CG, typename InT, typename OutT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                const __grid_constant__ CUtensorMap tmB,
@@ -193,12 +190,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const uint32_t pair = rank >> 1;              // which CTA pair of the cluster
-    const uint32_t lead = rank & ~1u;             // rank of this pair's leader
-    const uint32_t crank = rank & 1u;             // rank within the pair
-    const int unit = (int)(blockIdx.x / (CG * MC));
-    const int num_units = (int)(gridDim.x / (CG * MC));
+    const uint32_t crank = (CG == 2) ? cluster_ctarank() : 0u;   // rank within the pair
+    const int unit = (int)(blockIdx.x / CG);
+    const int num_units = (int)(gridDim.x / CG);
 
     const uint32_t misc = base + Cfg::kOffMisc;
     auto bar_full = [&](int s) { return misc + Cfg::kBarFull + 8u * s; };
@@ -215,7 +209,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), MC);
+            mbar_init(bar_empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull(a), 1);
@@ -268,7 +262,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // serpentine k order: a tile starts on the k-slabs the previous one
                 // ended on, which are the ones most likely still in L2
                 const bool rev = p.k_snake && (tcount & 1u);
-                const int m0 = (tm * MC + (int)pair) * TC_BM * CG + (int)crank * TC_BM;
+                const int m0 = tm * TC_BM * CG + (int)crank * TC_BM;
                 const int nb = n0 + (int)crank * (nw / CG);
                 // implicit GEMM: base pixel (top-left of the filter window) of row m0
                 int px_n = 0, px_h = 0, px_w = 0;
@@ -324,9 +318,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 };
                 // K x N operand: one 64-column box per 64 columns this CTA holds;
-                // N x K operand: one full-height box (a half tile uses its top rows),
-                // or 64-row boxes when the two pairs share B
-                const bool boxes64 = p.b_mn_major || MC == 2;
+                // N x K operand: one full-height box (a half tile uses its top rows)
+                const bool boxes64 = p.b_mn_major != 0;
                 const int b_boxes = boxes64 ? nw / CG / 64 : 1;
                 const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBStage;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -336,23 +329,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
                     const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
                     const int k0 = (rev ? nkb - 1 - kb : kb) * kBk;
-                    if constexpr (CG == 2 && MC == 2) {
-                        const uint32_t fb = mapa_shared(bar_full(s), lead);
-                        if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
-                        load_a(sa, fb, k0, true);
-                        // B box c goes to this CTA and its counterpart in the other pair;
-                        // pair c issues it (pair 0 issues the only box of a half tile)
-                        const uint16_t mask = (uint16_t)((1u << crank) | (1u << (crank + 2)));
-                        for (int c = 0; c < b_boxes; ++c) {
-                            if ((b_boxes == 2 ? c : 0) != (int)pair) continue;
-                            if (p.b_mn_major)
-                                tma_load_2d_pair_mc(sb + c * 8192, &tmB, fb, nb + 64 * c, k0, mask, pol_b);
-                            else
-                                tma_load_2d_pair_mc(sb + c * 8192, &tmB, fb, k0, nb + 64 * c, mask, pol_b);
-                        }
-                    } else if constexpr (CG == 2) {
+                    if constexpr (CG == 2) {
                         const uint32_t fb = mapa_shared(bar_full(s), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
+                        if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
                         load_a(sa, fb, k0, true);
                         if (boxes64) {
                             for (int c = 0; c < b_boxes; ++c) {
@@ -385,9 +364,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------------------------- MMA issuer ----
         if (crank == 0 && lane == 0) {
             const Waiter w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
-            // stage release reaches every CTA whose smem this pair's loads fill
-            const uint16_t empty_mask = (uint16_t)(MC == 2 ? 0xF : 0x3);
-            const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pair));
+            // stage release and accumulator hand-over reach both CTAs of the pair
+            const uint16_t pair_mask = 0x3u;
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int item = unit; item < num_items && ok; item += num_units, ++tcount) {
@@ -420,7 +398,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
                         tc_mma<CG, KIND>(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if constexpr (CG == 2) tc_commit_2(bar_empty(s), empty_mask); else tc_commit_1(bar_empty(s));
+                    if constexpr (CG == 2) tc_commit_2(bar_empty(s), pair_mask); else tc_commit_1(bar_empty(s));
                 }
                 if (!ok) break;
                 if (!((p.debug & DBG_SKIP_FIRST_ACC_COMMIT) && tcount == 0)) {
@@ -428,7 +406,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
             // Every MMA this thread issued has finished before TMEM can be released.
-            if constexpr (CG == 2) tc_commit_2(bar_done, (uint16_t)(1u << rank)); else tc_commit_1(bar_done);
+            if constexpr (CG == 2) tc_commit_2(bar_done, (uint16_t)(1u << crank)); else tc_commit_1(bar_done);
             const Waiter wd{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_MMA};
             if (!mbar_try_wait(bar_done, 0)) {
                 const uint64_t t0 = globaltimer_ns();
@@ -445,14 +423,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const bool has_bias = (p.epi & EPI_BIAS) != 0;
         const bool relu = (p.epi & EPI_RELU) != 0;
         const InT* bias = reinterpret_cast<const InT*>(p.bias);
-        const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), lead) : bar_tempty(0);
-        const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), lead) : bar_tempty(1);
+        const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), 0) : bar_tempty(0);
+        const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), 0) : bar_tempty(1);
         uint32_t tcount = 0, cstore = 0;
         for (int item = unit; item < num_items; item += num_units, ++tcount) {
             int tm, n0, nw;
             work_item(item, p, tm, n0, nw);
             const int kChunks = nw / kCols;
-            const int m0 = (tm * MC + (int)pair) * TC_BM * CG + (int)crank * TC_BM;
+            const int m0 = tm * TC_BM * CG + (int)crank * TC_BM;
             const int row0 = m0 + 32 * (int)q;
             const uint32_t a = tcount & 1u;
             const uint32_t aph = (tcount >> 1) & 1u;
@@ -699,7 +677,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (CG == 2) cluster_sync_all();
 }
 
-template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
+template <int CG, typename InT, typename OutT, int KIND = 0>
 cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const TcParams& p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -709,28 +687,28 @@ cudaError_t launch_impl(const CUtensorMap& tmA, const CUtensorMap& tmA2, const C
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG * MC;
+    attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, MC, InT, OutT, KIND>, tmA, tmA2, tmB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CG, InT, OutT, KIND>, tmA, tmA2, tmB, tmC, p);
 }
 
-template <int CG, int MC, typename InT, typename OutT, int KIND = 0>
+template <int CG, typename InT, typename OutT, int KIND = 0>
 cudaError_t prepare_impl(int* max_units) {
-    auto fn = gemm_tc_kernel<CG, MC, InT, OutT, KIND>;
+    auto fn = gemm_tc_kernel<CG, InT, OutT, KIND>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<CG>::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CG * MC, 1, 1);
+    cfg.gridDim = dim3(CG, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = TcCfg<CG>::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG * MC;
+    attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -742,39 +720,39 @@ cudaError_t prepare_impl(int* max_units) {
     return cudaSuccess;
 }
 
-template <int CG, int MC>
+template <int CG>
 cudaError_t launch_dt(int dtype, const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB, const CUtensorMap& tmC,
                       const TcParams& p, int grid, cudaStream_t stream) {
     switch (dtype) {
-        case DT_BF16_F32: return launch_impl<CG, MC, __nv_bfloat16, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
-        case DT_BF16_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(tmA, tmA2, tmB, tmC, p, grid, stream);
-        case DT_F16_F32: return launch_impl<CG, MC, __half, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
-        case DT_F16_F16: return launch_impl<CG, MC, __half, __half>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_BF16_F32: return launch_impl<CG, __nv_bfloat16, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_BF16_BF16: return launch_impl<CG, __nv_bfloat16, __nv_bfloat16>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_F16_F32: return launch_impl<CG, __half, float>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_F16_F16: return launch_impl<CG, __half, __half>(tmA, tmA2, tmB, tmC, p, grid, stream);
         // fp8 operands (the format is in the instruction descriptor); bf16 bias / scale
         case DT_E4M3_F32:
-        case DT_E5M2_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_E5M2_F32: return launch_impl<CG, __nv_bfloat16, float, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
         case DT_E4M3_BF16:
-        case DT_E5M2_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_E5M2_BF16: return launch_impl<CG, __nv_bfloat16, __nv_bfloat16, 1>(tmA, tmA2, tmB, tmC, p, grid, stream);
         // fp32 operands multiplied as tf32; bf16 bias / scale
-        case DT_TF32_F32: return launch_impl<CG, MC, __nv_bfloat16, float, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
-        case DT_TF32_BF16: return launch_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_TF32_F32: return launch_impl<CG, __nv_bfloat16, float, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
+        case DT_TF32_BF16: return launch_impl<CG, __nv_bfloat16, __nv_bfloat16, 2>(tmA, tmA2, tmB, tmC, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
 
-template <int CG, int MC>
+template <int CG>
 cudaError_t prepare_dt(int dtype, int* max_units) {
     switch (dtype) {
-        case DT_BF16_F32: return prepare_impl<CG, MC, __nv_bfloat16, float>(max_units);
-        case DT_BF16_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16>(max_units);
-        case DT_F16_F32: return prepare_impl<CG, MC, __half, float>(max_units);
-        case DT_F16_F16: return prepare_impl<CG, MC, __half, __half>(max_units);
+        case DT_BF16_F32: return prepare_impl<CG, __nv_bfloat16, float>(max_units);
+        case DT_BF16_BF16: return prepare_impl<CG, __nv_bfloat16, __nv_bfloat16>(max_units);
+        case DT_F16_F32: return prepare_impl<CG, __half, float>(max_units);
+        case DT_F16_F16: return prepare_impl<CG, __half, __half>(max_units);
         case DT_E4M3_F32:
-        case DT_E5M2_F32: return prepare_impl<CG, MC, __nv_bfloat16, float, 1>(max_units);
+        case DT_E5M2_F32: return prepare_impl<CG, __nv_bfloat16, float, 1>(max_units);
         case DT_E4M3_BF16:
-        case DT_E5M2_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 1>(max_units);
-        case DT_TF32_F32: return prepare_impl<CG, MC, __nv_bfloat16, float, 2>(max_units);
-        case DT_TF32_BF16: return prepare_impl<CG, MC, __nv_bfloat16, __nv_bfloat16, 2>(max_units);
+        case DT_E5M2_BF16: return prepare_impl<CG, __nv_bfloat16, __nv_bfloat16, 1>(max_units);
+        case DT_TF32_F32: return prepare_impl<CG, __nv_bfloat16, float, 2>(max_units);
+        case DT_TF32_BF16: return prepare_impl<CG, __nv_bfloat16, __nv_bfloat16, 2>(max_units);
     }
     return cudaErrorInvalidValue;
 }
@@ -789,19 +767,14 @@ cudaError_t launch_tc_gemm(int cta_group, int dtype, const CUtensorMap& tmA, con
                            const CUtensorMap& tmC, const TcParams& p, int grid, cudaStream_t stream,
                            const CUtensorMap* tmA2) {
     const CUtensorMap& a2 = tmA2 ? *tmA2 : tmA;
-    if (cta_group == 2)
-        return p.multicast ? launch_dt<2, 2>(dtype, tmA, a2, tmB, tmC, p, grid, stream)
-                           : launch_dt<2, 1>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
-    if (cta_group == 1) return launch_dt<1, 1>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
+    if (cta_group == 2) return launch_dt<2>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
+    if (cta_group == 1) return launch_dt<1>(dtype, tmA, a2, tmB, tmC, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_prepare(int cta_group, int dtype, int* max_units, int* max_quads) {
-    if (cta_group == 2) {
-        cudaError_t e = prepare_dt<2, 2>(dtype, max_quads);
-        return e != cudaSuccess ? e : prepare_dt<2, 1>(dtype, max_units);
-    }
-    if (cta_group == 1) { *max_quads = 0; return prepare_dt<1, 1>(dtype, max_units); }
+cudaError_t tc_prepare(int cta_group, int dtype, int* max_units) {
+    if (cta_group == 2) return prepare_dt<2>(dtype, max_units);
+    if (cta_group == 1) return prepare_dt<1>(dtype, max_units);
     return cudaErrorInvalidValue;
 }
 

@@ -157,19 +157,6 @@ __device__ __forceinline__ void tma_load_im2col_pair(uint32_t dst, const CUtenso
         : "memory");
 }
 
-// As tma_load_2d_pair, multicast: the tile lands at the same offset in every
-// CTA of `mask`, and each destination's pair leader barrier (at the offset of
-// `cluster_bar`, which names a pair leader) counts its bytes.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar,
-                                                    int32_t c0, int32_t c1, uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "h"(mask),
-           "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
                  :: "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1) : "memory");

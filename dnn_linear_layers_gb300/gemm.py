@@ -20,7 +20,9 @@ BF16_F32OUT, BF16_BF16OUT, F16_F32OUT, F16_F16OUT = 0, 1, 2, 3
 E4M3_F32OUT, E4M3_BF16OUT, E5M2_F32OUT, E5M2_BF16OUT = 4, 5, 6, 7
 TF32_F32OUT, TF32_BF16OUT = 8, 9   # fp32 A and B, multiplied at tf32 precision
 FP8_DTYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
-B_KN, B_NK, B_CONST, TC_MULTICAST, A_KM = 0, 1, 2, 4, 8
+B_KN, B_NK, B_CONST, A_KM = 0, 1, 2, 8
+(OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY, OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES,
+ OPT_SKINNY_X_LSU, OPT_LOG) = range(1, 10)
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY = 0, 1, 2, 3, 4
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
     0, -1, -2, -3, -4, -5, -6)
@@ -51,6 +53,8 @@ SIGNATURES = {
     "gemm_plan_set_packing": (_int, [_vp, _int]),
     "gemm_plan_set_debug": (_int, [_vp, _uint]),
     "gemm_plan_workspace_bytes": (_i64, [_vp]),
+    "gemm_plan_set_option": (_int, [_vp, _int, _i64]),
+    "gemm_plan_get_option": (_int, [_vp, _int, ctypes.POINTER(_i64)]),
     "gemm_validate": (_int, [_uint, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int]),
     "gemm_im2col": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _vp, _i64, _int, _vp]),
     "gemm_run_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _int, _int, _uint, _vp, _vp]),
@@ -132,7 +136,7 @@ class Plan:
     (A is stored K x M, the transposed operand)."""
 
     def __init__(self, device: int | torch.device = 0, b_layout: str = "kn", b_const: bool = False,
-                 multicast: bool = False, a_layout: str = "mk"):
+                 a_layout: str = "mk"):
         if isinstance(device, torch.device):
             device = device.index if device.index is not None else torch.cuda.current_device()
         self.device = int(device)
@@ -140,8 +144,7 @@ class Plan:
             raise ValueError("b_layout is 'kn' or 'nk', a_layout 'mk' or 'km'")
         self.b_nk = b_layout == "nk"
         self.a_km = a_layout == "km"
-        flags = ((B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0) | (TC_MULTICAST if multicast else 0)
-                 | (A_KM if self.a_km else 0))
+        flags = (B_NK if self.b_nk else B_KN) | (B_CONST if b_const else 0) | (A_KM if self.a_km else 0)
         h = _vp()
         _check(lib().gemm_plan_create(ctypes.byref(h), self.device, flags), "gemm_plan_create")
         self._h = h
@@ -179,6 +182,15 @@ class Plan:
 
     def set_debug(self, flags: int):
         _check(lib().gemm_plan_set_debug(self._h, int(flags)), "gemm_plan_set_debug")
+
+    def set_option(self, option: int, value: int):
+        """Set a GEMM_OPT_* scheduling option (sweeps and tests)."""
+        _check(lib().gemm_plan_set_option(self._h, int(option), int(value)), "gemm_plan_set_option")
+
+    def get_option(self, option: int) -> int:
+        v = ctypes.c_int64()
+        _check(lib().gemm_plan_get_option(self._h, int(option), ctypes.byref(v)), "gemm_plan_get_option")
+        return v.value
 
     @property
     def last_kernel(self) -> int:

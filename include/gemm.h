@@ -90,11 +90,6 @@ typedef enum {
  * while the previous kernel of the stream is still finishing; A, bias and C
  * are still touched only after that kernel is done. */
 #define GEMM_B_CONST 2u
-/* Large-M kernel: clusters of two CTA pairs on vertically adjacent tiles
- * fetch each shared B tile once and multicast it to both pairs (halves the B
- * reads from L2; on GB300 it lowers power but was not faster at the sizes
- * measured, so it is off by default). */
-#define GEMM_TC_MULTICAST 4u
 /* A is stored K x M (the transpose of the M x K operand, BLAS "transa"):
  * A(i, k) = A[k * lda + i], lda >= M.  Runs on the tensor-core kernels (also for
  * M <= 128); 16-bit inputs only (fp8 operands must be K-major: refused with
@@ -136,8 +131,11 @@ typedef struct {
     int relu;             /* nonzero: ReLU before the cast                    */
 } gemm_epilogue_args_t;
 
-/* Create a plan for `device` (a CUDA ordinal).  flags: GEMM_B_KN or GEMM_B_NK,
- * optionally | GEMM_A_KM, | GEMM_B_CONST and | GEMM_TC_MULTICAST.
+/* Create a plan for `device` (a CUDA ordinal): the handle of the
+ * create / use / destroy pattern of the cuBLAS example on youngju.dev "GEMM to
+ * FlashAttention" (BLAS/cuBLAS interface listing), which gemm_run then takes
+ * as its first argument.  flags: GEMM_B_KN or GEMM_B_NK, optionally
+ * | GEMM_A_KM and | GEMM_B_CONST; any other bit is GEMM_ERR_INVALID_ARG.
  * Allocates the plan and its device status word; restores the caller's
  * current device before returning.  *plan is set only on success. */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
@@ -159,13 +157,21 @@ int gemm_run_ex(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
 
 /* Synchronise the stream of the last gemm_run and report device-side errors:
  * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last call (the
- * status word is then cleared), GEMM_ERR_CUDA if the stream reports an error. */
+ * status word is then cleared), GEMM_ERR_CUDA if the stream reports an error.
+ * The pages have no counterpart: it is this library's design, the host end of
+ * the bounded device-side waits (a wait that runs out reports here instead of
+ * hanging the GPU). */
 int gemm_plan_status(gemm_plan_t plan);
 
-/* Release the plan, its status word and its workspace.  NULL is accepted. */
+/* Release the plan, its status word and its workspace (the destroy step of
+ * the cuBLAS handle pattern, youngju.dev "GEMM to FlashAttention",
+ * BLAS/cuBLAS interface listing).  Waits for the plan's last stream first.
+ * NULL is accepted. */
 int gemm_plan_destroy(gemm_plan_t plan);
 
-/* Static description of a return code. */
+/* Static description of a return code (never NULL; "unknown error" for a
+ * code not listed above).  The pages have no counterpart: it is this
+ * library's design, so that callers across the C ABI can print an error. */
 const char* gemm_strerror(int code);
 
 /* Explicit-GEMM (im2col) matrix of a convolution (CMU 15-418 "DNNs and ML
@@ -267,6 +273,24 @@ int gemm_plan_set_debug(gemm_plan_t plan, unsigned flags);
 /* Bytes of workspace the plan currently holds. */
 int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 
+/* Tuning options of a plan, for benchmark sweeps and tests; the defaults are
+ * the measured best and a caller never needs to change them.  No option
+ * changes a result, only how the work is scheduled. */
+#define GEMM_OPT_GROUP_M 1         /* tile-rows per rasterisation group, 1..1024 (default 8) */
+#define GEMM_OPT_TAIL_SPLIT 2      /* 0/1: run the last partial wave as half tiles (default 1) */
+#define GEMM_OPT_K_SNAKE 3         /* 0/1: every other tile of a worker walks k backwards (default 1) */
+#define GEMM_OPT_PDL 4             /* 0/1: programmatic dependent launch (default 1) */
+#define GEMM_OPT_L2_POLICY 5       /* 0: A evict-last; 1: B evict-last; 2: both normal (default 0) */
+#define GEMM_OPT_SKINNY_SPLITS 6   /* small-M kernel k-slices: 0 = automatic (default), 1, 2, 4, 8 */
+#define GEMM_OPT_SKINNY_STAGES 7   /* small-M kernel ring depth: 0 = automatic (default), 2..8 */
+#define GEMM_OPT_SKINNY_X_LSU 8    /* 0/1: small-M kernel copies X with cp.async (default 0) */
+#define GEMM_OPT_LOG 9             /* 0/1: one line per launch on stderr (default 0) */
+
+/* Set / read a GEMM_OPT_* option.  GEMM_ERR_INVALID_ARG for a NULL plan, an
+ * unknown option or a value outside the option's range (nothing changes). */
+int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value);
+int gemm_plan_get_option(gemm_plan_t plan, int option, int64_t* value);
+
 /* Host-only argument check: the code gemm_run would return for these
  * arguments before touching the GPU (GEMM_OK if they are acceptable).
  * `flags` are the plan flags.  Needs no device and launches nothing. */
@@ -286,8 +310,8 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K,
  * accept cudaMalloc/cudaFree (which may synchronise the whole device).
  *
  * Same operation, layouts and codes as gemm_run, on the CURRENT device, with
- * the plan flags passed directly (`flags`: GEMM_B_KN or GEMM_B_NK) and no
- * plan.  It allocates nothing: operands that break the 16-byte TMA rule are
+ * the plan flags passed directly (`flags`: GEMM_B_KN or GEMM_B_NK; any other
+ * bit is GEMM_ERR_INVALID_ARG) and no plan.  It allocates nothing: operands that break the 16-byte TMA rule are
  * packed into a fixed scratch array of GEMM_NOALLOC_SCRATCH_BYTES (minus 256
  * bytes for a status word) that the library holds on each device; a call
  * whose packed operands would not fit returns GEMM_ERR_UNSUPPORTED and

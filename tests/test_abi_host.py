@@ -64,7 +64,7 @@ def test_validate_rejects_bad_arguments(lib):
     assert val(dtype=10) == G.ERR_INVALID_ARG
     assert val(dtype=G.TF32_F32OUT) == G.OK and val(dtype=G.TF32_BF16OUT) == G.OK
     assert val(flags=16) == G.ERR_INVALID_ARG
-    assert val(flags=G.TC_MULTICAST) == G.OK
+    assert val(flags=4) == G.ERR_INVALID_ARG             # not a flag
     # A stored K x M: lda counts M
     assert val(flags=G.A_KM, M=96, K=32, lda=96, ldc=64) == G.OK
     assert val(flags=G.A_KM, M=96, K=32, lda=95, ldc=64) == G.ERR_INVALID_ARG    # lda < M
@@ -95,6 +95,10 @@ def test_null_plan_is_rejected(lib):
     assert lib.gemm_plan_destroy(None) == G.OK
     assert lib.gemm_plan_set_kernel(None, 0) == G.ERR_INVALID_ARG
     assert lib.gemm_plan_last_kernel(None) == -1
+    assert lib.gemm_plan_set_option(None, G.OPT_GROUP_M, 8) == G.ERR_INVALID_ARG
+    v = ctypes.c_int64(-7)
+    assert lib.gemm_plan_get_option(None, G.OPT_GROUP_M, ctypes.byref(v)) == G.ERR_INVALID_ARG
+    assert v.value == -7
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour on a host without a GPU")
@@ -130,7 +134,9 @@ def test_noalloc_refuses_the_operand_forms_it_does_not_take(lib):
                                     args["ldc"], 0, dtype, flags, None, None)
     for dtype in (G.E4M3_F32OUT, G.E5M2_BF16OUT, G.TF32_F32OUT, G.TF32_BF16OUT):
         assert call(dtype, G.B_NK) == G.ERR_UNSUPPORTED
-    assert call(G.BF16_F32OUT, G.A_KM) == G.ERR_UNSUPPORTED
+    # only the B-layout flag applies without a plan
+    for flags in (G.A_KM, G.B_CONST, G.B_NK | G.B_CONST, 4):
+        assert call(G.BF16_F32OUT, flags) == G.ERR_INVALID_ARG
 
 
 def test_attention_rejects_null_plan_and_bad_arguments(lib):

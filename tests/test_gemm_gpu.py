@@ -110,18 +110,38 @@ def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
     check(plans, GemmCase("tail_split", M, N, K, b_nk=b_nk, bias=True, out="bf16", integer=True, seed=K), kernel)
 
 
-@pytest.mark.parametrize("b_nk", [False, True])
-@pytest.mark.parametrize("shape", [(600, 700, 333), (1024, 768, 256), (4096, 4096, 72), (1300, 530, 200)])
-def test_multicast_clusters_integer_exact(b_nk, shape):
-    """Clusters of two CTA pairs sharing B by TMA multicast (plan flag): exact
-    on integers, including odd numbers of 256-row tiles and split last waves."""
+@pytest.mark.parametrize("option,value", [(G.OPT_GROUP_M, 1), (G.OPT_GROUP_M, 16), (G.OPT_TAIL_SPLIT, 0),
+                                          (G.OPT_K_SNAKE, 0), (G.OPT_PDL, 0), (G.OPT_L2_POLICY, 1),
+                                          (G.OPT_L2_POLICY, 2), (G.OPT_SKINNY_SPLITS, 1),
+                                          (G.OPT_SKINNY_STAGES, 2), (G.OPT_SKINNY_X_LSU, 1)])
+@pytest.mark.parametrize("shape", [(1300, 530, 200), (4096, 4096, 72), (16, 1000, 1000)])
+def test_scheduling_options_change_no_result(plans, option, value, shape):
+    """Every plan option only reschedules work: the results stay exact on
+    integers (large shapes on the paired kernel, M = 16 on the small-M one)."""
     M, N, K = shape
-    p = G.Plan(0, "nk" if b_nk else "kn", multicast=True)
-    case = GemmCase("multicast", M, N, K, b_nk=b_nk, bias=True, relu=True, out="bf16", integer=True, seed=M)
-    A, B, bias, C = run_case(p, case, kernel=G.KERNEL_TC_PAIR)
-    assert p.last_kernel == G.KERNEL_TC_PAIR
+    p = G.Plan(0, "nk")
+    default = p.get_option(option)
+    p.set_option(option, value)
+    assert p.get_option(option) == value
+    case = GemmCase("options", M, N, K, b_nk=True, bias=True, relu=True, out="bf16", integer=True, seed=M)
+    A, B, bias, C = run_case(p, case)
     C_ref, S = oracle_full(case, A, B, bias)
     compare(case, C, C_ref, S)
+    p.set_option(option, default)
+    assert p.get_option(option) == default
+    p.close()
+
+
+def test_option_ranges_are_checked(plans):
+    p = G.Plan(0)
+    for option, bad in [(G.OPT_GROUP_M, 0), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
+                        (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9), (0, 0),
+                        (99, 0)]:
+        before = p.get_option(option) if 1 <= option <= 9 else None
+        with pytest.raises(G.GemmError):
+            p.set_option(option, bad)
+        if before is not None:
+            assert p.get_option(option) == before
     p.close()
 
 
