@@ -72,10 +72,13 @@ WORKLOADS = {
     "linear_m16_4096x14336": (16, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m128_4096x14336": (128, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m1_4096x4096": (1, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
+    "linear_m4_4096x14336": (4, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
+    "linear_m4_4096x4096": (4, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m16_4096x4096": (16, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m128_4096x4096": (128, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     # the same decode layers with e4m3 weights and activations (per-tensor scales belong in alpha)
     "linear_m1_4096x14336_e4m3": (1, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
+    "linear_m4_4096x14336_e4m3": (4, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
     "linear_m16_4096x14336_e4m3": (16, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
     "linear_m128_4096x14336_e4m3": (128, 14336, 4096, "nk", (True, False), "bf16", 1.0, 1.0),
 }
@@ -113,6 +116,7 @@ def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float)
 KERNEL_SOURCES = {
     "tc": ["kernels_tc.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
     "skinny": ["kernels_skinny.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
+    "gemv": ["kernels_gemv.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
     "attn": ["kernels_attn.cu", "ptx.cuh", "internal.h", "gemm_api.cu"],
 }
 
@@ -287,7 +291,8 @@ def run_ours(args):
     # Linear-layer weights are constant model parameters: say so to the plan
     plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"), a_layout="km" if "_transa_" in name else "mk")
     if args.kernel != "auto":
-        plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY}[args.kernel])
+        plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY,
+                         "gemv": G.KERNEL_GEMV}[args.kernel])
     stream = torch.cuda.current_stream(dev)
     flops = attention_flops(name) if attn else 2.0 * M * N * K
     conv = name.startswith(("conv_implicit", "conv_pool"))
@@ -485,7 +490,8 @@ def run_ours(args):
                               if n_copies == 1 else
                               f"{n_copies} rotating operand copies ({n_copies * nbytes / 1e6:.0f} MB > 2 x L2)"),
                        "kernel": "attention" if attn else
-                                 {1: "tc_pair", 2: "tc_single", 4: "skinny"}.get(plan.last_kernel, str(plan.last_kernel)),
+                                 {1: "tc_pair", 2: "tc_single", 4: "skinny", 5: "gemv"}.get(plan.last_kernel,
+                                                                                         str(plan.last_kernel)),
                        "timing": "CUDA graph of the K steps, one replay" if graph is not None else "eager launches"},
             "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                          "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
@@ -626,7 +632,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a graph replay")
-    ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny", "gemv"], default="auto",
                     help="force a kernel (sweeps); the default lets the library choose")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -17,8 +17,8 @@ CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 OBJ = PKG / "_build"
 LIB = PKG / "libgb300gemm.so"
-SOURCES = ["kernels_tc.cu", "kernels_skinny.cu", "kernels_aux.cu", "kernels_attn.cu", "gemm_api.cu",
-           "gemm_noalloc.cu"]
+SOURCES = ["kernels_tc.cu", "kernels_skinny.cu", "kernels_gemv.cu", "kernels_aux.cu", "kernels_attn.cu",
+           "gemm_api.cu", "gemm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

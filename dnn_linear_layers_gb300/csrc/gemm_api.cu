@@ -42,6 +42,12 @@ struct gemm_plan {
     int skinny_splits = 0;        // 0: automatic; otherwise forced split count (sweeps)
     int skinny_stages = 0;        // 0: automatic; otherwise forced ring depth (sweeps)
     int skinny_x_lsu = 0;         // 1: skinny kernel copies X with cp.async (sweeps)
+    // M up to which an N x K Linear layer runs on the CUDA-core GEMV.  Measured
+    // on GB300 (4096 -> 14336, bf16): M = 1 0.93 of HBM against 0.80 on the
+    // tensor-core small-M kernel; M = 4 0.55 against 0.79 (the CUDA cores run
+    // out of issue slots for 4 tokens per weight element), so only M = 1.
+    int gemv_max_m = 1;
+    int gemv_blocks[3][kNumDtypes] = {};   // co-resident GEMV CTAs per SM, by tokens held (1, 2, 4)
     int smem_per_sm = 0;          // shared memory of one SM (bytes)
     int smem_reserved = 0;        // shared memory the system reserves per CTA (bytes)
     cudaStream_t last_stream = nullptr;
@@ -316,6 +322,35 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     return GEMM_OK;
 }
 
+// GEMV launch (M <= 4, W stored N x K): the rows of W split evenly over a
+// grid that is resident at once.
+int run_gemv(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* W,
+             int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, const EpiArgs& ex, int dtype,
+             cudaStream_t stream) {
+    const int mt = gemv_tokens_held((int)M);
+    const int bps = p->gemv_blocks[mt == 1 ? 0 : (mt == 2 ? 1 : 2)][dtype];
+    if (mt == 0 || bps < 1) return GEMM_ERR_UNSUPPORTED;
+    const int warps = kGemvThreads / 32;
+    int64_t grid = (int64_t)p->sm_count * bps;
+    const int64_t need = (N + warps - 1) / warps;   // one row per warp at least
+    if (grid > need) grid = need;
+    GemvParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.M = (int32_t)M; gp.N = (int32_t)N; gp.K = (int32_t)K;
+    gp.X = X; gp.ldx = ldx; gp.W = W; gp.ldw = ldw;
+    gp.bias = bias; gp.Y = Y; gp.ldy = ldy;
+    gp.epi = epi; gp.ex = ex;
+    gp.pdl = p->pdl;
+    gp.w_prefetch = (p->pdl && (p->flags & GEMM_B_CONST)) ? 1u : 0u;
+    if (p->debug_log)
+        std::fprintf(stderr, "[gemm] gemv M=%lld N=%lld K=%lld tokens=%d grid=%lld prefetch=%u pdl=%u\n",
+                     (long long)M, (long long)N, (long long)K, mt, (long long)grid, gp.w_prefetch, gp.pdl);
+    cudaError_t e = launch_gemv(dtype, gp, (int)grid, stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -374,6 +409,10 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     for (int dt = 0; dt <= DT_E5M2_BF16; ++dt) {
         e = skinny_prepare(dt);
         if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+        for (int i = 0; i < 3; ++i) {
+            e = gemv_prepare(1 << i, dt, &p->gemv_blocks[i][dt]);
+            if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+        }
     }
     p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
     p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
@@ -396,7 +435,7 @@ int gemm_plan_destroy(gemm_plan_t p) {
 }
 
 int gemm_plan_set_kernel(gemm_plan_t p, int kernel) {
-    if (!p || kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_SKINNY) return GEMM_ERR_INVALID_ARG;
+    if (!p || kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_GEMV) return GEMM_ERR_INVALID_ARG;
     p->forced_kernel = kernel;
     return GEMM_OK;
 }
@@ -455,6 +494,9 @@ int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
         case GEMM_OPT_LOG:
             if (!b01) return GEMM_ERR_INVALID_ARG;
             p->debug_log = (int)v; return GEMM_OK;
+        case GEMM_OPT_GEMV_MAX_M:
+            if (v < 0 || v > kGemvMaxM) return GEMM_ERR_INVALID_ARG;
+            p->gemv_max_m = (int)v; return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -471,6 +513,7 @@ int gemm_plan_get_option(gemm_plan_t p, int option, int64_t* v) {
         case GEMM_OPT_SKINNY_STAGES: *v = p->skinny_stages; return GEMM_OK;
         case GEMM_OPT_SKINNY_X_LSU: *v = p->skinny_x_lsu; return GEMM_OK;
         case GEMM_OPT_LOG: *v = p->debug_log; return GEMM_OK;
+        case GEMM_OPT_GEMV_MAX_M: *v = p->gemv_max_m; return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -571,14 +614,20 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const bool fp8 = dtype_is_fp8(dtype) || dtype_is_tf32(dtype);
     if (fp8 && (!b_nk || conv || a_km)) return GEMM_ERR_UNSUPPORTED;
     if (a_km && conv) return GEMM_ERR_UNSUPPORTED;
-    // the small-M kernel takes 16-bit and fp8 operands with an M x K A
+    // the small-M kernels take 16-bit and fp8 operands with an M x K A; the
+    // CUDA-core GEMV also needs the weight stored N x K
     const bool tf32 = dtype_is_tf32(dtype);
+    const bool small_ok = !conv && !tf32 && !a_km;
     int kernel = p->forced_kernel;
     if (kernel == GEMM_KERNEL_AUTO)
-        kernel = (M <= 128 && !conv && !tf32 && !a_km) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
-    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || conv || tf32 || a_km)) return GEMM_ERR_UNSUPPORTED;
-    if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY)
+        kernel = (small_ok && b_nk && M <= p->gemv_max_m) ? GEMM_KERNEL_GEMV
+               : (small_ok && M <= 128) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
+    if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || !small_ok)) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_GEMV && (M > kGemvMaxM || !small_ok || !b_nk)) return GEMM_ERR_UNSUPPORTED;
+    if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY &&
+        kernel != GEMM_KERNEL_GEMV)
         return GEMM_ERR_UNSUPPORTED;
+    const bool gemv = kernel == GEMM_KERNEL_GEMV;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
     const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
 
@@ -590,8 +639,8 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const int kbk = 128 / es;                       // elements per 128-byte k-block row
     const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
     const bool b_ok = aligned16(B) && (ldb * es) % 16 == 0;
-    // the skinny kernel stores C with plain stores: any pitch is fine
-    const bool c_ok = skinny || (aligned16(C) && (ldc * ob) % 16 == 0);
+    // the small-M kernels store C with plain stores: any pitch is fine
+    const bool c_ok = skinny || gemv || (aligned16(C) && (ldc * ob) % 16 == 0);
     const void* A_use = A; int64_t lda_use = lda;
     const void* B_use = B; int64_t ldb_use = ldb;
     void* C_use = C; int64_t ldc_use = ldc;
@@ -620,6 +669,13 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
     }
 
+    if (gemv) {
+        rc = run_gemv(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, stream);
+        if (rc != GEMM_OK) return rc;
+        p->last_kernel = kernel;
+        p->last_stream = stream; p->have_stream = true;
+        return GEMM_OK;
+    }
     const CUtensorMapDataType in_dt = in_map_type(dtype);
     if (skinny) {
         rc = run_skinny(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, b_nk, in_dt, stream);

@@ -143,6 +143,28 @@ cudaError_t skinny_prepare(int dtype);
 cudaError_t launch_skinny(int dtype, const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyParams& p,
                           int grid, cudaStream_t stream);
 
+// GEMV / very-small-M Linear layer on the CUDA cores (M <= 4, W stored N x K)
+struct GemvParams {
+    int32_t M, N, K;
+    const void* X;         // M x K, row pitch ldx elements (rows 16-byte aligned)
+    int64_t ldx;
+    const void* W;         // N x K, row pitch ldw elements (rows 16-byte aligned)
+    int64_t ldw;
+    const void* bias;      // N elements (bf16 for fp8 operands), or null
+    void* Y;               // M x N, row pitch ldy elements
+    int64_t ldy;
+    uint32_t epi;          // EpiFlags
+    EpiArgs ex;
+    uint32_t pdl;          // host only: launch with programmatic stream serialisation
+    uint32_t w_prefetch;   // 1: W may be read before the previous kernel of the stream ends
+};
+constexpr int kGemvThreads = 256;
+constexpr int kGemvMaxM = 4;
+// tokens a kernel instantiation holds for M tokens (1, 2 or 4; 0 if M > 4)
+int gemv_tokens_held(int M);
+cudaError_t gemv_prepare(int M, int dtype, int* blocks_per_sm);
+cudaError_t launch_gemv(int dtype, const GemvParams& p, int grid, cudaStream_t stream);
+
 // Fused attention forward -------------------------------------------------
 // O = softmax(scale * Q K^T (masked)) V per (batch, head); Q, K, V, O are
 // [B*H][S][D] row-major (D = 64 or 128); one CTA per 128 queries of one head.

@@ -1,0 +1,299 @@
+// GEMV / very-small-M Linear layer on the CUDA cores:
+//
+//   Y[m][n] = epilogue( sum_k X[m][k] * W[n][k] ),   m < M <= 4, W stored N x K
+//
+// (a Linear weight, out x in).  With M <= 4 every weight byte feeds at most a
+// few multiply-adds (arithmetic intensity about M FLOP per byte: youngju.dev
+// "GEMM to FlashAttention", arithmetic-intensity listing, batch-1 case; CMU
+// 15-418 notes, question 1 on GEMV), so the kernel is bound by streaming W
+// from HBM and the tensor cores buy nothing.  The form follows the warp-level
+// reduction of the CMU 15-418 notes, section 3.3 (example three): each warp
+// owns output rows, its lanes stride the reduction dimension, and a butterfly
+// of warp shuffles combines the lanes' partial sums.
+//
+// Design for sm_103a:
+//   * every lane moves 16-byte pieces: lane l of a warp reads pieces
+//     l, l + 32, l + 64, ... of a W row, so each warp-wide load covers 512
+//     contiguous bytes (coalesced); W is read once, through the non-caching
+//     path (ld.global.nc.L1::no_allocate), X through L1, where every warp of
+//     the SM finds it;
+//   * a warp works on R rows and U pieces per row at a time: R x U
+//     independent 16-byte loads per lane are in flight before the first
+//     multiply, and each X piece is reused for the R rows;
+//   * the rows are split evenly over a grid sized to be resident at once
+//     (contiguous row ranges of floor(N / warps) or one more per warp), so
+//     every SM streams the same number of bytes;
+//   * products and sums in fp32 with the paired fp32 instructions
+//     (fma.rn.f32x2), 16-bit values widened exactly, fp8 codes through the
+//     exact e4m3 / e5m2 -> f16x2 conversion;
+//   * a K tail that does not fill a 16-byte piece is read element by element
+//     (nothing past K is touched);
+//   * the epilogue (alpha, per-column scale, bias, beta * previous Y, ReLU,
+//     the single cast) runs in the lane that holds the finished sum;
+//   * programmatic dependent launch: the grid releases its dependents at once;
+//     with constant weights (plan flag GEMM_B_CONST) each warp issues its first
+//     W loads before waiting for the previous kernel of the stream, whose
+//     output may be this layer's X.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int kWarps = kGemvThreads / 32;
+
+// W: streamed once, kept out of L1.  Volatile: issued in program order, so
+// the prefetched loads stay ahead of the dependency wait.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// X: read by every warp of the SM, cached in L1.
+__device__ __forceinline__ uint4 ld_keep16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// The elements k0 .. k0 + kPer - 1 of a row whose valid length is K (k0 < K
+// < k0 + kPer), one element at a time, zeros past K.
+template <int ES>
+__device__ __forceinline__ uint4 ld_tail16(const char* row, int k0, int K) {
+    union { uint4 u; uint8_t b[16]; uint16_t h[8]; } v;
+    v.u = make_uint4(0u, 0u, 0u, 0u);
+    constexpr int kPer = 16 / ES;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        if (k0 + e < K) {
+            if constexpr (ES == 2) v.h[e] = *reinterpret_cast<const uint16_t*>(row + (int64_t)(k0 + e) * 2);
+            else v.b[e] = *reinterpret_cast<const uint8_t*>(row + (k0 + e));
+        }
+    }
+    return v.u;
+}
+
+// ---- operand kinds: 16-byte piece -> pairs of fp32 values (exact) ----
+// OP 0: bf16, 1: fp16, 2: e4m3, 3: e5m2.  kPairs pairs per piece.
+template <int OP> struct Op;
+template <> struct Op<0> {
+    static constexpr int kEs = 2, kPairs = 4;
+    static __device__ __forceinline__ uint64_t pair(const uint4& v, int j) {
+        const uint32_t u = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+        return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    }
+};
+template <> struct Op<1> {
+    static constexpr int kEs = 2, kPairs = 4;
+    static __device__ __forceinline__ uint64_t pair(const uint4& v, int j) {
+        const uint32_t u = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+        __half2 h = *reinterpret_cast<const __half2*>(&u);
+        const float2 f = __half22float2(h);
+        return f2_pack(f.x, f.y);
+    }
+};
+template <int E5M2> struct OpFp8 {
+    static constexpr int kEs = 1, kPairs = 8;
+    // codes 2j, 2j + 1 of the piece -> f16x2 (exact) -> two fp32 values
+    static __device__ __forceinline__ uint64_t pair(const uint4& v, int j) {
+        const uint32_t u = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
+        const uint16_t c = (uint16_t)((j & 1) ? (u >> 16) : (u & 0xFFFFu));
+        uint32_t h2;
+        if constexpr (E5M2) asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
+        else asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+        __half2 h = *reinterpret_cast<const __half2*>(&h2);
+        const float2 f = __half22float2(h);
+        return f2_pack(f.x, f.y);
+    }
+};
+template <> struct Op<2> : OpFp8<0> {};
+template <> struct Op<3> : OpFp8<1> {};
+
+template <typename T> __device__ __forceinline__ float vec_f32(T v);
+template <> __device__ __forceinline__ float vec_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float vec_f32<__half>(__half v) { return __half2float(v); }
+__device__ __forceinline__ float y_f32(float v) { return v; }
+__device__ __forceinline__ float y_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float y_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float y_cvt(float v, float*) { return v; }
+__device__ __forceinline__ __nv_bfloat16 y_cvt(float v, __nv_bfloat16*) { return __float2bfloat16_rn(v); }
+__device__ __forceinline__ __half y_cvt(float v, __half*) { return __float2half_rn(v); }
+
+// MT: tokens held (M <= MT); R rows x U pieces per lane in flight; OP operand
+// kind; VecT type of bias / scale; OutT type of Y.
+template <int MT, int R, int U, int OP, typename VecT, typename OutT>
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_kernel(const GemvParams p) {
+    using O = Op<OP>;
+    constexpr int kPer = 16 / O::kEs;          // elements per 16-byte piece
+    constexpr int kBlk = 32 * U * kPer;        // elements of a row per block of pieces
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31u);
+    const int64_t TW = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int r_begin = (int)(gw * p.N / TW), r_end = (int)((gw + 1) * p.N / TW);
+    const int M = p.M, K = p.K;
+    const char* const W = static_cast<const char*>(p.W);
+    const char* const X = static_cast<const char*>(p.X);
+
+    grid_launch_dependents();
+    bool waited = false;
+    if (!p.w_prefetch || r_begin >= r_end) {
+        grid_dependency_wait();
+        waited = true;
+    }
+
+    for (int n0 = r_begin; n0 < r_end; n0 += R) {
+        const int nr = min(R, r_end - n0);     // warp-uniform
+        uint64_t acc[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = 0ull;
+        for (int kb = 0; kb < K; kb += kBlk) {
+            const bool full = kb + kBlk <= K;  // warp-uniform
+            uint4 w[R][U];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const char* row = W + (int64_t)(n0 + r) * p.ldw * O::kEs;
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    const int k = kb + (i * 32 + lane) * kPer;
+                    if (r >= nr) w[r][i] = make_uint4(0u, 0u, 0u, 0u);
+                    else if (full || k + kPer <= K) w[r][i] = ld_stream16(row + (int64_t)k * O::kEs);
+                    else if (k < K) w[r][i] = ld_tail16<O::kEs>(row, k, K);
+                    else w[r][i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            if (!waited) {                     // W loads are in flight during the wait
+                grid_dependency_wait();
+                waited = true;
+            }
+            uint4 x[MT][U];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const char* row = X + (int64_t)m * p.ldx * O::kEs;
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    const int k = kb + (i * 32 + lane) * kPer;
+                    if (m >= M) x[m][i] = make_uint4(0u, 0u, 0u, 0u);
+                    else if (full || k + kPer <= K) x[m][i] = ld_keep16(row + (int64_t)k * O::kEs);
+                    else if (k < K) x[m][i] = ld_tail16<O::kEs>(row, k, K);
+                    else x[m][i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+#pragma unroll
+                for (int j = 0; j < O::kPairs; ++j) {
+                    uint64_t xp[MT];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) xp[m] = O::pair(x[m][i], j);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint64_t wp = O::pair(w[r][i], j);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) acc[r][m] = f2_fma(wp, xp[m], acc[r][m]);
+                    }
+                }
+            }
+        }
+        // butterfly: every lane ends with every (row, token) sum; lane
+        // r * MT + m keeps sum (r, m) for the epilogue
+        float mine = 0.0f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float lo, hi;
+                f2_unpack(acc[r][m], lo, hi);
+                float v = lo + hi;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+                if (lane == r * MT + m) mine = v;
+            }
+        }
+        const int r = lane / MT, m = lane - (lane / MT) * MT;
+        if (lane < R * MT && r < nr && m < M) {
+            const int n = n0 + r;
+            float t = mine;
+            if (p.epi & EPI_ALPHA) t *= p.ex.alpha;
+            if (p.epi & EPI_SCALE) t *= vec_f32<VecT>(reinterpret_cast<const VecT*>(p.ex.scale)[n]);
+            if (p.epi & EPI_BIAS) t += vec_f32<VecT>(reinterpret_cast<const VecT*>(p.bias)[n]);
+            if (p.epi & EPI_BETA)
+                t += p.ex.beta * y_f32(reinterpret_cast<const OutT*>(p.ex.c_old)[(int64_t)m * p.ex.ldc_old + n]);
+            if (p.epi & EPI_RELU) t = fmaxf(t, 0.0f);
+            reinterpret_cast<OutT*>(p.Y)[(int64_t)m * p.ldy + n] = y_cvt(t, (OutT*)nullptr);
+        }
+    }
+}
+
+// Pieces in flight per lane: MT = 1: 2 rows x 8 pieces; MT = 2: 2 x 4;
+// MT = 4: 4 x 2 (each X piece serves four rows).
+template <int MT> struct Shape;
+template <> struct Shape<1> { static constexpr int R = 2, U = 8; };
+template <> struct Shape<2> { static constexpr int R = 2, U = 4; };
+template <> struct Shape<4> { static constexpr int R = 4, U = 2; };
+
+// Kernel of (tokens held, operand type); nullptr if there is none.
+using GemvFn = void (*)(const GemvParams);
+
+template <int MT>
+GemvFn kernel_for(int dtype) {
+    constexpr int R = Shape<MT>::R, U = Shape<MT>::U;
+    switch (dtype) {
+        case DT_BF16_F32: return gemv_kernel<MT, R, U, 0, __nv_bfloat16, float>;
+        case DT_BF16_BF16: return gemv_kernel<MT, R, U, 0, __nv_bfloat16, __nv_bfloat16>;
+        case DT_F16_F32: return gemv_kernel<MT, R, U, 1, __half, float>;
+        case DT_F16_F16: return gemv_kernel<MT, R, U, 1, __half, __half>;
+        // fp8 codes; bf16 bias / scale
+        case DT_E4M3_F32: return gemv_kernel<MT, R, U, 2, __nv_bfloat16, float>;
+        case DT_E4M3_BF16: return gemv_kernel<MT, R, U, 2, __nv_bfloat16, __nv_bfloat16>;
+        case DT_E5M2_F32: return gemv_kernel<MT, R, U, 3, __nv_bfloat16, float>;
+        case DT_E5M2_BF16: return gemv_kernel<MT, R, U, 3, __nv_bfloat16, __nv_bfloat16>;
+    }
+    return nullptr;
+}
+
+GemvFn kernel_for(int mt, int dtype) {
+    switch (mt) {
+        case 1: return kernel_for<1>(dtype);
+        case 2: return kernel_for<2>(dtype);
+        case 4: return kernel_for<4>(dtype);
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+int gemv_tokens_held(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 0)); }
+
+cudaError_t gemv_prepare(int M, int dtype, int* blocks_per_sm) {
+    GemvFn fn = kernel_for(gemv_tokens_held(M), dtype);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kGemvThreads, 0);
+}
+
+cudaError_t launch_gemv(int dtype, const GemvParams& p, int grid, cudaStream_t stream) {
+    GemvFn fn = kernel_for(gemv_tokens_held(p.M), dtype);
+    if (fn == nullptr || grid < 1) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace gb300

@@ -101,7 +101,8 @@ typedef enum {
 #define GEMM_KERNEL_TC_PAIR 1   /* tcgen05, 2-CTA clusters (cta_group::2), 256 x 256 tiles */
 #define GEMM_KERNEL_TC_SINGLE 2 /* tcgen05, one CTA per tile (cta_group::1), 128 x 256 tiles */
 #define GEMM_KERNEL_FILL 3      /* K == 0: epilogue of an empty sum */
-#define GEMM_KERNEL_SKINNY 4    /* small-M Linear layer (weight streaming) */
+#define GEMM_KERNEL_SKINNY 4    /* small-M Linear layer (weight streaming, tensor cores) */
+#define GEMM_KERNEL_GEMV 5      /* M <= 4, B stored N x K: CUDA-core GEMV (weight streaming; auto for M = 1) */
 
 /* Return codes. */
 #define GEMM_OK 0
@@ -285,6 +286,7 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 #define GEMM_OPT_SKINNY_STAGES 7   /* small-M kernel ring depth: 0 = automatic (default), 2..8 */
 #define GEMM_OPT_SKINNY_X_LSU 8    /* 0/1: small-M kernel copies X with cp.async (default 0) */
 #define GEMM_OPT_LOG 9             /* 0/1: one line per launch on stderr (default 0) */
+#define GEMM_OPT_GEMV_MAX_M 10     /* M up to which the CUDA-core GEMV is chosen, 0..4 (default 1) */
 
 /* Set / read a GEMM_OPT_* option.  GEMM_ERR_INVALID_ARG for a NULL plan, an
  * unknown option or a value outside the option's range (nothing changes). */

@@ -137,7 +137,7 @@ def test_option_ranges_are_checked(plans):
     for option, bad in [(G.OPT_GROUP_M, 0), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
                         (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9), (0, 0),
                         (99, 0)]:
-        before = p.get_option(option) if 1 <= option <= 9 else None
+        before = p.get_option(option) if 1 <= option <= 10 else None
         with pytest.raises(G.GemmError):
             p.set_option(option, bad)
         if before is not None:
@@ -196,10 +196,12 @@ def test_skinny_chained_layers_see_previous_outputs(plans, b_const):
 
 
 def test_skinny_is_auto_choice_for_small_m(plans):
+    """2 <= M <= 128: the tensor-core small-M kernel (M = 1 with an N x K
+    weight takes the CUDA-core GEMV, tests/test_gemv_gpu.py)."""
     p = plans["nk"]
-    A = torch.ones(4, 256, dtype=torch.bfloat16, device="cuda")
+    A = torch.ones(5, 256, dtype=torch.bfloat16, device="cuda")
     W = torch.ones(512, 256, dtype=torch.bfloat16, device="cuda")
-    C = torch.empty(4, 512, device="cuda")
+    C = torch.empty(5, 512, device="cuda")
     p.set_kernel(G.KERNEL_AUTO)
     p.run(A, W, C)
     assert p.status() == 0 and p.last_kernel == G.KERNEL_SKINNY
