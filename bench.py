@@ -43,6 +43,10 @@ WORKLOADS = {
     # name: (M, N, K, b_layout, epilogue(bias, relu), out, a_std, b_std)
     "square8192_bf16": (8192, 8192, 8192, "kn", (False, False), "bf16", 1.0, 1.0),
     "square4096_bf16": (4096, 4096, 4096, "kn", (False, False), "bf16", 1.0, 1.0),
+    "square2048_bf16": (2048, 2048, 2048, "kn", (False, False), "bf16", 1.0, 1.0),
+    "square1024_bf16": (1024, 1024, 1024, "kn", (False, False), "bf16", 1.0, 1.0),
+    # the small single GEMM: fp32 output, no epilogue
+    "square512_f32": (512, 512, 512, "kn", (False, False), "f32", 1.0, 1.0),
     "square8192_nk_bf16": (8192, 8192, 8192, "nk", (False, False), "bf16", 1.0, 1.0),
     "square4096_nk_bf16": (4096, 4096, 4096, "nk", (False, False), "bf16", 1.0, 1.0),
     "qkv_8192x4096x12288": (8192, 12288, 4096, "kn", (False, False), "bf16", 1.0, 4096 ** -0.5),
@@ -72,6 +76,7 @@ WORKLOADS = {
     "linear_m16_4096x14336": (16, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m128_4096x14336": (128, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m1_4096x4096": (1, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
+    "linear_m2_4096x14336": (2, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m4_4096x14336": (4, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m4_4096x4096": (4, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m16_4096x4096": (16, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
@@ -266,11 +271,202 @@ def make_inputs(name, device, seed=0):
     return A, B, bias
 
 
+class Workload:
+    """One workload on one GPU: inputs resident in HBM (rotating copies when
+    they are smaller than twice the L2), a plan, and the K timed steps
+    captured once into a CUDA graph."""
+
+    def __init__(self, name, dev, local_rank, args):
+        import torch
+        from dnn_linear_layers_gb300 import gemm as G
+        from dnn_linear_layers_gb300 import roofline as R
+        self.name = name
+        self.dev = dev
+        self.args = args
+        M, N, K, lay, (has_bias, relu), out, _, _ = WORKLOADS[name]
+        self.M, self.N, self.K, self.lay, self.has_bias, self.relu = M, N, K, lay, has_bias, relu
+        self.out_dtype = torch.float32 if out == "f32" else torch.bfloat16
+        self.A_h, self.B_h, self.bias_h = make_inputs(name, dev, seed=0)
+        A, B = self.A_h.to(dev), self.B_h.to(dev)
+        self.bias = self.bias_h.to(dev) if self.bias_h is not None else None
+        self.pool = name.startswith("conv_pool")
+        self.attn = name.startswith("attention_")
+        self.causal = "causal" in name
+        self.conv = name.startswith(("conv_implicit", "conv_pool"))
+        self.f8 = fp8_dtype(name)
+        # the pooled convolution writes a quarter of the output rows; attention writes O like q
+        C = (torch.empty(tuple(A.shape), dtype=self.out_dtype, device=dev) if self.attn else
+             torch.empty((M // 4 if self.pool else M, N), dtype=self.out_dtype, device=dev))
+        self.A, self.B, self.C = A, B, C
+        # Linear-layer weights are constant model parameters: say so to the plan
+        self.plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"),
+                           a_layout="km" if "_transa_" in name else "mk")
+        if args.kernel != "auto":
+            self.plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY,
+                                  "gemv": G.KERNEL_GEMV}[args.kernel])
+        self.stream = torch.cuda.current_stream(dev)
+        self.flops = attention_flops(name) if self.attn else 2.0 * M * N * K
+        if self.attn:   # q, k, v read once, o written once
+            self.nbytes = float(A.numel() * 2 + B.numel() * 2 + C.numel() * C.element_size())
+        elif self.conv:   # activations, weights and output once each (no im2col matrix exists)
+            self.nbytes = float(A.numel() * 2 + B.numel() * 2 + C.numel() * C.element_size() +
+                                (N * 2 if has_bias else 0))
+        else:
+            es = A.element_size()
+            self.nbytes = R.gemm_bytes(M, N, K, es, es, C.element_size(), 2 if has_bias else 0)
+        # Workloads smaller than twice the L2 rotate through enough copies of their
+        # operands that each step reads HBM, not the previous step's L2 lines.
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.n_copies = 1 if self.nbytes >= 2 * self.l2 else int(2 * self.l2 // self.nbytes) + 2
+        self.copies = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(self.n_copies - 1)]
+        self.counter = 0
+        self.graph = None
+
+    def call(self, a, b, c):
+        if self.attn:
+            self.plan.attention(a, b[0], b[1], c, causal=self.causal)
+        elif self.pool:
+            self.plan.conv2d_maxpool(a, b, c, self.bias, self.relu, pad=1)
+        elif self.conv:
+            self.plan.conv2d(a, b, c, self.bias, self.relu, pad=1)
+        else:
+            self.plan.run(a, b, c, self.bias, self.relu)      # on torch's current stream
+
+    def step(self):
+        a, b, c = self.copies[self.counter % self.n_copies]
+        self.counter += 1
+        self.call(a, b, c)
+
+    def prepare(self):
+        """Warm-up steps, then capture the K timed steps into a CUDA graph, so
+        the GPU runs them back to back with no host launch gaps between steps
+        (short decode-like kernels would otherwise time the Python launch path)."""
+        import torch
+        args, dev = self.args, self.dev
+        for _ in range(args.warmup):
+            self.step()
+        torch.cuda.synchronize()
+        assert self.plan.status() == 0, "device status after warm-up"
+        launches0 = self.plan.launch_count
+        if not args.no_graph:
+            try:
+                side = torch.cuda.Stream(dev)
+                side.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(side):
+                    self.step()
+                torch.cuda.current_stream(dev).wait_stream(side)
+                torch.cuda.synchronize()
+                launches0 = self.plan.launch_count
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=side):
+                    for _ in range(args.steps):
+                        self.step()
+                torch.cuda.synchronize()
+                self.graph = graph
+            except Exception as exc:  # capture unsupported: time eager launches instead
+                self.graph = None
+                print(f"# graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+                torch.cuda.synchronize()
+        self.launches_per_run = self.plan.launch_count - launches0
+
+    def timed_run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            for _ in range(self.args.steps):
+                self.step()
+
+    def time(self, world, sampler=None):
+        """Device time (ms) of the K steps on the launching stream, and the
+        number of this library's kernels they launched.  With a clock sampler,
+        the GPU is first kept busy for a second (untimed) so the clocks settle."""
+        import torch
+        import torch.distributed as dist
+        self.timed_run()
+        torch.cuda.synchronize()
+        t_end = time.time() + (1.0 if sampler else 0.0)
+        while time.time() < t_end:
+            self.timed_run()
+            torch.cuda.synchronize()
+        launches0 = self.plan.launch_count
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        self.timed_run()
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        launches = self.launches_per_run if self.graph is not None else self.plan.launch_count - launches0
+        st = self.plan.status()
+        assert st == 0, f"device status {st}"
+        return t0.elapsed_time(t1), launches
+
+    def roofline(self, kernel_ms):
+        """(tensor_bound, achieved, peak, unit, peak_source, roofline_time_s, peak_src_kind)."""
+        from dnn_linear_layers_gb300 import roofline as R
+        peaks, src = R.load_peaks()
+        kind = self.name.rsplit("_", 1)[-1]
+        # an fp8 or tf32 contraction takes the measured bf16 peak times the nominal ratio of the two rates
+        t_peak = peaks["bf16_tflops"] * (PEAK_RATIO[kind] if self.f8 is not None else 1.0)
+        t_roof = R.roofline_time(self.flops, self.nbytes, t_peak * 1e12, peaks["hbm_gbs"] * 1e9)
+        tensor_bound = self.flops / (t_peak * 1e12) >= self.nbytes / (peaks["hbm_gbs"] * 1e9)
+        if tensor_bound:
+            achieved, peak, unit = self.flops / (kernel_ms * 1e-3) / 1e12, t_peak, "TFLOP/s"
+            peak_src = (f"MEASURED_PEAKS.json bf16_tflops (burst) x {PEAK_RATIO[kind]:.4g}, the nominal {kind} / "
+                        "bf16 ratio" if self.f8 is not None else "MEASURED_PEAKS.json bf16_tflops (burst)")
+        else:
+            achieved, peak, unit = self.nbytes / (kernel_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+            peak_src = "MEASURED_PEAKS.json hbm_gbs"
+        return tensor_bound, achieved, peak, unit, peak_src, t_roof, src
+
+    def kernel_name(self):
+        from dnn_linear_layers_gb300 import gemm as G
+        if self.attn:
+            return "attention"
+        return {G.KERNEL_TC_PAIR: "tc_pair", G.KERNEL_TC_SINGLE: "tc_single", G.KERNEL_SKINNY: "skinny",
+                G.KERNEL_GEMV: "gemv"}.get(self.plan.last_kernel, str(self.plan.last_kernel))
+
+    def close(self):
+        self.plan.close()
+
+
+# Decode-like Linear layers timed after the headline in the same process and
+# reported under "secondary" (the memory-bound half of the target).
+SECONDARY = ("linear_m1_4096x14336", "linear_m16_4096x14336")
+
+
+def secondary_lines(dev, local_rank, args, world):
+    out = {}
+    for name in SECONDARY:
+        w = Workload(name, dev, local_rank, args)
+        w.prepare()
+        sampler = ClockSampler(local_rank) if not args.no_clocks else None
+        total_ms, launches = w.time(world, sampler)
+        if sampler:
+            sampler.stop()
+        total_ms = max_over_ranks(total_ms, dev)
+        kernel_ms = total_ms / args.steps
+        tb, achieved, peak, unit, peak_src, t_roof, src = w.roofline(kernel_ms)
+        out[name] = {"value": round(w.nbytes * args.steps * world / (total_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                     "ms_per_step": round(total_ms / args.steps, 5), "kernel": w.kernel_name(),
+                     "roofline": {"bound": "tensor" if tb else "hbm", "achieved": round(achieved, 2), "peak": peak,
+                                  "unit": unit, "frac": round(achieved / peak, 4),
+                                  "peak_source": f"measured ({peak_src})" if src == "measured" else "fallback",
+                                  "algorithmic_bytes": w.nbytes, "traffic": profiled_traffic(name)},
+                     "config": {"M": w.M, "N": w.N, "K": w.K, "b_layout": w.lay, "epilogue": "bias",
+                                "l2": f"{w.n_copies} rotating operand copies"},
+                     "gpu_launches": int(launches),
+                     "clocks": sampler.summary() if sampler else None}
+        w.close()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from dnn_linear_layers_gb300 import gemm as G
-    from dnn_linear_layers_gb300 import roofline as R
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -278,131 +474,27 @@ def run_ours(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     name = args.workload
-    M, N, K, lay, (has_bias, relu), out, _, _ = WORKLOADS[name]
-    A_h, B_h, bias_h = make_inputs(name, dev, seed=0)
-    A, B = A_h.to(dev), B_h.to(dev)
-    bias = bias_h.to(dev) if bias_h is not None else None
-    pool = name.startswith("conv_pool")
-    attn = name.startswith("attention_")
-    causal = "causal" in name
-    # the pooled convolution writes a quarter of the output rows; attention writes O like q
-    C = (torch.empty(tuple(A.shape), dtype=torch.bfloat16, device=dev) if attn else
-         torch.empty((M // 4 if pool else M, N), dtype=torch.bfloat16, device=dev))
-    # Linear-layer weights are constant model parameters: say so to the plan
-    plan = G.Plan(local_rank, lay, b_const=name.startswith("linear_"), a_layout="km" if "_transa_" in name else "mk")
-    if args.kernel != "auto":
-        plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY,
-                         "gemv": G.KERNEL_GEMV}[args.kernel])
-    stream = torch.cuda.current_stream(dev)
-    flops = attention_flops(name) if attn else 2.0 * M * N * K
-    conv = name.startswith(("conv_implicit", "conv_pool"))
-    f8 = fp8_dtype(name)
-    if attn:   # q, k, v read once, o written once
-        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2)
-    elif conv:   # activations, weights and output once each (no im2col matrix exists)
-        nbytes_step = float(A.numel() * 2 + B.numel() * 2 + C.numel() * 2 + (N * 2 if has_bias else 0))
-    else:
-        es = A.element_size()
-        nbytes_step = R.gemm_bytes(M, N, K, es, es, 2, 2 if has_bias else 0)
-    # Workloads smaller than twice the L2 rotate through enough copies of their
-    # operands that each step reads HBM, not the previous step's L2 lines.
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_copies = 1 if nbytes_step >= 2 * l2 else int(2 * l2 // nbytes_step) + 2
-    copies = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n_copies - 1)]
-    counter = [0]
-
-    def call(a, b, c):
-        if attn:
-            plan.attention(a, b[0], b[1], c, causal=causal)
-        elif pool:
-            plan.conv2d_maxpool(a, b, c, bias, relu, pad=1)
-        elif conv:
-            plan.conv2d(a, b, c, bias, relu, pad=1)
-        else:
-            plan.run(a, b, c, bias, relu)      # on torch's current stream
-
-    def step():
-        a, b, c = copies[counter[0] % n_copies]
-        counter[0] += 1
-        call(a, b, c)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert plan.status() == 0, "device status after warm-up"
-
-    # The K timed steps are captured once into a CUDA graph and replayed, so
-    # the GPU runs them back to back with no host launch gaps between steps
-    # (short decode-like kernels would otherwise time the Python launch path).
-    graph = None
-    launches0 = plan.launch_count
-    if not args.no_graph:
-        try:
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(torch.cuda.current_stream(dev))
-            with torch.cuda.stream(side):
-                step()
-            torch.cuda.current_stream(dev).wait_stream(side)
-            torch.cuda.synchronize()
-            launches0 = plan.launch_count
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=side):
-                for _ in range(args.steps):
-                    step()
-            torch.cuda.synchronize()
-        except Exception as exc:  # capture unsupported: time eager launches instead
-            graph = None
-            print(f"# graph capture failed ({exc}); timing eager launches", file=sys.stderr)
-            torch.cuda.synchronize()
-    launches_per_run = plan.launch_count - launches0
-
-    def timed_run():
-        if graph is not None:
-            graph.replay()
-        else:
-            for _ in range(args.steps):
-                step()
-
-    timed_run()
-    torch.cuda.synchronize()
+    w = Workload(name, dev, local_rank, args)
+    M, N, K = w.M, w.N, w.K
+    w.prepare()
     sampler = ClockSampler(local_rank) if not args.no_clocks else None
-    # keep the GPU busy ~1 s (untimed) so the sampler is running and clocks settle
-    t_end = time.time() + (1.0 if sampler else 0.0)
-    while time.time() < t_end:
-        timed_run()
-        torch.cuda.synchronize()
-
-    launches0 = plan.launch_count
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    timed_run()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    launches = launches_per_run if graph is not None else plan.launch_count - launches0
+    total_ms, launches = w.time(world, sampler)
     if sampler:
         sampler.stop()
-    total_ms = t0.elapsed_time(t1)
     # steps run back to back on one stream: the average launch lasts total / K
     # (for single-kernel steps; with packing, a step also holds the copies)
     kernel_ms = total_ms / args.steps
-    st = plan.status()
-    assert st == 0, f"device status {st}"
-
     total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = job_throughput(flops, args.steps, world, total_ms)
+    value = job_throughput(w.flops, args.steps, world, total_ms)
 
     # ---- end to end: pinned host inputs -> device -> the library call -> host
     # result, every step.  Steps are pipelined over two device buffer sets and
     # three streams (copy in, compute, copy out): the copies of one step overlap
     # the computation of the one before, as a serving loop would run them.
-    A_p = A_h.pin_memory(); B_p = B_h.pin_memory()
-    C_p = [torch.empty(tuple(C.shape), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    A, B, C, stream = w.A, w.B, w.C, w.stream
+    A_p = w.A_h.pin_memory(); B_p = w.B_h.pin_memory()
+    C_p = [torch.empty(tuple(C.shape), dtype=C.dtype).pin_memory() for _ in range(2)]
     A_e = [torch.empty_like(A) for _ in range(2)]
     B_e = [torch.empty_like(B) for _ in range(2)]
     C_e = [torch.empty_like(C) for _ in range(2)]
@@ -425,7 +517,7 @@ def run_ours(args):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])
-        call(A_e[b], B_e[b], C_e[b])              # on torch's current stream
+        w.call(A_e[b], B_e[b], C_e[b])            # on torch's current stream
         ev_comp[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
@@ -449,32 +541,24 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms, dev)
-    e2e_value = job_throughput(flops, e2e_steps, world, e2e_ms) if not args.no_e2e else None
-    assert plan.status() == 0
+    e2e_value = job_throughput(w.flops, e2e_steps, world, e2e_ms) if not args.no_e2e else None
+    assert w.plan.status() == 0
 
-    peaks, src = R.load_peaks()
-    nbytes = nbytes_step
-    # an fp8 or tf32 contraction takes the measured bf16 peak times the nominal ratio of the two rates
+    tensor_bound, achieved, peak, r_unit, peak_src, t_roof, src = w.roofline(kernel_ms)
+    secondary = (secondary_lines(dev, local_rank, args, world)
+                 if name == DEFAULT_WORKLOAD and not args.no_secondary else None)
     kind = name.rsplit("_", 1)[-1]
-    t_peak = peaks["bf16_tflops"] * (PEAK_RATIO[kind] if f8 is not None else 1.0)
-    t_roof = R.roofline_time(flops, nbytes, t_peak * 1e12, peaks["hbm_gbs"] * 1e9)
-    tensor_bound = flops / (t_peak * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        achieved, peak, r_unit = flops / (kernel_ms * 1e-3) / 1e12, t_peak, "TFLOP/s"
-        peak_src = (f"MEASURED_PEAKS.json bf16_tflops (burst) x {PEAK_RATIO[kind]:.4g}, the nominal {kind} / bf16 "
-                    "ratio" if f8 is not None else "MEASURED_PEAKS.json bf16_tflops (burst)")
-    else:
-        achieved, peak, r_unit = nbytes / (kernel_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
-        peak_src = "MEASURED_PEAKS.json hbm_gbs"
+    f8, attn = w.f8, w.attn
+    has_bias, relu, lay, l2, n_copies, nbytes = w.has_bias, w.relu, w.lay, w.l2, w.n_copies, w.nbytes
     result = None
     if rank == 0:
-        cpu = None if args.no_cpu_baseline else cpu_baseline(name, A_h, B_h, bias_h, args.cpu_seconds)
+        cpu = None if args.no_cpu_baseline else cpu_baseline(name, w.A_h, w.B_h, w.bias_h, args.cpu_seconds)
         clocks = sampler.summary() if sampler else {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": name.rsplit("_", 1)[-1] if f8 is not None else "bf16",
+            "dtype": kind if f8 is not None else "bf16",
             "data": ("synthetic: N(0,1) fp32 (torch CPU generator, fixed seeds), resident in HBM" if kind == "tf32"
                      else "synthetic: N(0,1) drawn as bf16 (torch CPU generator, fixed seeds), rounded to "
                      f"{kind}, resident in HBM" if f8 is not None else
@@ -485,21 +569,20 @@ def run_ours(args):
                            "scale": "1/sqrt(D)"} if attn else
                           {"M": M, "N": N, "K": K, "b_layout": lay, "a_layout": "km" if "_transa_" in name else "mk",
                            "epilogue": ("bias" if has_bias else "") + ("+relu" if relu else "") or "none"}),
-                       "out": "bf16", "accumulate": "fp32", "parallelism": f"replicas x{world}",
+                       "out": "f32" if w.out_dtype == torch.float32 else "bf16", "accumulate": "fp32",
+                       "parallelism": f"replicas x{world}",
                        "l2": (f"inputs larger than L2 ({nbytes / 1e6:.1f} MB > {l2 / 1e6:.0f} MB), no flush"
                               if n_copies == 1 else
                               f"{n_copies} rotating operand copies ({n_copies * nbytes / 1e6:.0f} MB > 2 x L2)"),
-                       "kernel": "attention" if attn else
-                                 {1: "tc_pair", 2: "tc_single", 4: "skinny", 5: "gemv"}.get(plan.last_kernel,
-                                                                                         str(plan.last_kernel)),
-                       "timing": "CUDA graph of the K steps, one replay" if graph is not None else "eager launches"},
+                       "kernel": w.kernel_name(),
+                       "timing": "CUDA graph of the K steps, one replay" if w.graph is not None else "eager launches"},
             "roofline": {"bound": "tensor" if tensor_bound else "hbm",
                          "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
                          "frac": round(achieved / peak, 4),
                          "frac_of_roofline_time": round(t_roof / (kernel_ms * 1e-3), 4),
                          "peak_source": f"measured ({peak_src})" if src == "measured" else "fallback",
                          "traffic": profiled_traffic(name),
-                         "algorithmic_bytes": nbytes, "flops_per_launch": flops,
+                         "algorithmic_bytes": nbytes, "flops_per_launch": w.flops,
                          "kernel_ms": round(kernel_ms, 5)},
             "e2e": {"value": round(e2e_value, 2) if e2e_value else None, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(A_p.numel() * A_p.element_size() + B_p.numel() * B_p.element_size()),
@@ -510,8 +593,10 @@ def run_ours(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if secondary is not None:
+            result["secondary"] = secondary
         print(json.dumps(result), flush=True)
-    plan.close()
+    w.close()
     if world > 1:
         dist.destroy_process_group()
     return result
@@ -632,6 +717,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a graph replay")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the decode-layer lines appended to the default workload's result")
     ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny", "gemv"], default="auto",
                     help="force a kernel (sweeps); the default lets the library choose")
     args = ap.parse_args()

@@ -41,7 +41,6 @@ struct gemm_plan {
     int k_snake = 1;              // serpentine k order across a worker's tiles (measured: -30% DRAM reads)
     int skinny_splits = 0;        // 0: automatic; otherwise forced split count (sweeps)
     int skinny_stages = 0;        // 0: automatic; otherwise forced ring depth (sweeps)
-    int skinny_x_lsu = 0;         // 1: skinny kernel copies X with cp.async (sweeps)
     // M up to which an N x K Linear layer runs on the CUDA-core GEMV.  Measured
     // on GB300 (4096 -> 14336, bf16): M = 1 0.93 of HBM against 0.80 on the
     // tensor-core small-M kernel; M = 4 0.55 against 0.79 (the CUDA cores run
@@ -299,10 +298,7 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     sp.M = (int32_t)M; sp.N = (int32_t)N; sp.K = (int32_t)K;
     sp.mpad = mpad; sp.stages = stages;
     sp.w_prefetch = (p->pdl && (p->flags & GEMM_B_CONST)) ? 1u : 0u;
-    // X by TMA; the cp.async loader in the epilogue warps measured equal for
-    // M <= 16 and slower for M = 128 on GB300, so it is only a sweep option
-    sp.x_lsu = (p->skinny_x_lsu && es == 2) ? 1u : 0u;
-    sp.X = X; sp.ldx = ldx; sp.pdl = p->pdl; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
+    sp.pdl = p->pdl; sp.splits = S; sp.num_k_blocks = (int32_t)nkb; sp.tmem_cols = tmem_cols;
     sp.epi = epi;
     sp.ex = ex;
     // A = W (128 features; MN-major when stored K x N), B = X (mpad tokens, K-major)
@@ -314,8 +310,8 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     sp.timeout_ns = p->timeout_ns;
     if (p->debug_log)
         std::fprintf(stderr, "[gemm] skinny M=%lld N=%lld K=%lld mpad=%d tiles=%lld splits=%d stages=%d smem=%d "
-                     "prefetch=%u pdl=%u x_lsu=%u\n", (long long)M, (long long)N, (long long)K, mpad, (long long)n_tiles, S,
-                     stages, skinny_smem_bytes(mpad, stages), sp.w_prefetch, sp.pdl, sp.x_lsu);
+                     "prefetch=%u pdl=%u\n", (long long)M, (long long)N, (long long)K, mpad, (long long)n_tiles, S,
+                     stages, skinny_smem_bytes(mpad, stages), sp.w_prefetch, sp.pdl);
     cudaError_t e = launch_skinny(dtype, tmW, tmX, sp, (int)(n_tiles * S), stream);
     if (e != cudaSuccess) return record(p, e);
     p->launches += 1;
@@ -488,9 +484,6 @@ int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
         case GEMM_OPT_SKINNY_STAGES:
             if (v != 0 && (v < 2 || v > 8)) return GEMM_ERR_INVALID_ARG;
             p->skinny_stages = (int)v; return GEMM_OK;
-        case GEMM_OPT_SKINNY_X_LSU:
-            if (!b01) return GEMM_ERR_INVALID_ARG;
-            p->skinny_x_lsu = (int)v; return GEMM_OK;
         case GEMM_OPT_LOG:
             if (!b01) return GEMM_ERR_INVALID_ARG;
             p->debug_log = (int)v; return GEMM_OK;
@@ -511,7 +504,6 @@ int gemm_plan_get_option(gemm_plan_t p, int option, int64_t* v) {
         case GEMM_OPT_L2_POLICY: *v = p->l2_policy; return GEMM_OK;
         case GEMM_OPT_SKINNY_SPLITS: *v = p->skinny_splits; return GEMM_OK;
         case GEMM_OPT_SKINNY_STAGES: *v = p->skinny_stages; return GEMM_OK;
-        case GEMM_OPT_SKINNY_X_LSU: *v = p->skinny_x_lsu; return GEMM_OK;
         case GEMM_OPT_LOG: *v = p->debug_log; return GEMM_OK;
         case GEMM_OPT_GEMV_MAX_M: *v = p->gemv_max_m; return GEMM_OK;
     }

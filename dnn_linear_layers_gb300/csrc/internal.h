@@ -129,9 +129,6 @@ struct SkinnyParams {
     uint64_t timeout_ns;
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t w_prefetch;   // 1: W may be read before the previous kernel of the stream ends
-    uint32_t x_lsu;        // 1: the epilogue warps copy X with cp.async instead of TMA
-    const void* X;         // X (M x K, row pitch ldx elements), for the cp.async path
-    int64_t ldx;
     EpiArgs ex;            // alpha / scale / beta operands of the epilogue
 };
 

@@ -232,6 +232,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint64_t pol_kv = l2_policy_evict_last();   // read by every query block of the head
             uint32_t qi = 0;
             int gb0 = 0;
+            int k_issued = 0, v_issued = 0;   // key blocks whose K / V copies were issued
             bool ok = true;
             for (int step = 0, item; ok && (item = attn_item_index(p.causal != 0u, (int)blockIdx.x, (int)gridDim.x, step)) < items; ++step) {
                 const AttnItem it = attn_item(p, qblocks, item);
@@ -260,25 +261,35 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ok = w(bar(Cfg::kBarKEmpty + gb0 % Cfg::kStages), ring_phase(gb0));
                 if (!ok) break;
                 load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gb0, 0);
+                k_issued = gb0 + 1;
                 for (int j = 0; j < it.nkb && ok; ++j) {
                     if (j + 1 < it.nkb) {
                         const int gn = gb0 + j + 1;
                         ok = w(bar(Cfg::kBarKEmpty + gn % Cfg::kStages), ring_phase(gn));
                         if (!ok) break;
                         load_kv(&tmK, Cfg::kOffK, Cfg::kBarK, gn, j + 1);
+                        k_issued = gn + 1;
                     }
                     const int gb = gb0 + j;
                     ok = w(bar(Cfg::kBarVEmpty + gb % Cfg::kStages), ring_phase(gb));
                     if (!ok) break;
                     load_kv(&tmV, Cfg::kOffV, Cfg::kBarV, gb, j);
+                    v_issued = gb + 1;
                 }
                 gb0 += it.nkb;
             }
-            if (!ok) {
-                // let copies already issued land before shared memory is released
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 100000ull) { }
-            }
+            // Copies already issued land before shared memory is released:
+            // wait (bounded, whatever the abort flag) for the last phase of the
+            // Q tile and of each K and V slot -- immediately done in a run
+            // without abort, where every copy was consumed.
+            bool drained = qi == 0 || mbar_wait_bounded(bar(Cfg::kBarQFull), (qi - 1u) & 1u, p.timeout_ns);
+            for (int i = k_issued - Cfg::kStages < 0 ? 0 : k_issued - Cfg::kStages; i < k_issued; ++i)
+                drained &= mbar_wait_bounded(bar(Cfg::kBarK + i % Cfg::kStages), (uint32_t)(i / Cfg::kStages) & 1u,
+                                             p.timeout_ns);
+            for (int i = v_issued - Cfg::kStages < 0 ? 0 : v_issued - Cfg::kStages; i < v_issued; ++i)
+                drained &= mbar_wait_bounded(bar(Cfg::kBarV + i % Cfg::kStages), (uint32_t)(i / Cfg::kStages) & 1u,
+                                             p.timeout_ns);
+            if (!drained) atomicOr(p.status, ST_TIMEOUT_PRODUCER);
         }
     } else if (warp == 1) {
         // ---- S issuer: S_j = Q K_j^T into score buffer gb & 1

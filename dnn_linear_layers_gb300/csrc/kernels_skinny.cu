@@ -48,28 +48,6 @@ __device__ __forceinline__ void cluster_arrive_wait() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 16-byte global -> shared copy through the load/store path; bytes past
-// `src_bytes` (0..16) are written as zeros.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-// wait until at most `n` (0..7) of this thread's copy groups are still pending
-__device__ __forceinline__ void cp_async_wait_n(int n) {
-    switch (n) {
-        case 0: cp_async_wait<0>(); break;
-        case 1: cp_async_wait<1>(); break;
-        case 2: cp_async_wait<2>(); break;
-        case 3: cp_async_wait<3>(); break;
-        case 4: cp_async_wait<4>(); break;
-        case 5: cp_async_wait<5>(); break;
-        case 6: cp_async_wait<6>(); break;
-        default: cp_async_wait<7>(); break;
-    }
-}
-
 // store into the shared memory of a CTA of this cluster (address from mapa)
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
@@ -152,10 +130,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int kb_end = (int)(((int64_t)(rank + 1) * nkb) / S);
 
     if (threadIdx.x == 0) {
-        // a stage is full once the producer's W bytes have landed and, when the
-        // epilogue warps copy X, each of those four warps has arrived
+        // a stage is full once the producer's W and X bytes have landed
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full(s), p.x_lsu ? 5 : 1);
+            mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
         }
         mbar_init(bar_acc, 1);
@@ -198,29 +175,31 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // the ring's stages start empty, so no empty-barrier wait is needed
             const int nk = kb_end - kb_begin;
             const int pre = p.w_prefetch ? (nk < kStages ? nk : kStages) : 0;
-            const uint32_t tx = kWStage + (p.x_lsu ? 0u : x_stage);
+            const uint32_t tx = kWStage + x_stage;
             for (int it = 0; it < pre; ++it) {
                 mbar_arrive_expect_tx(bar_full(it), tx);
                 load_w(it, (kb_begin + it) * kKb);
             }
             grid_dependency_wait();
-            if (!p.x_lsu)
-                for (int it = 0; it < pre; ++it)
-                    tma_load_2d(base + off_x + it * x_stage, &tmX, bar_full(it), (kb_begin + it) * kKb, 0, pol_x);
-            bool ok = true;
+            for (int it = 0; it < pre; ++it)
+                tma_load_2d(base + off_x + it * x_stage, &tmX, bar_full(it), (kb_begin + it) * kKb, 0, pol_x);
+            int issued = pre;
             for (int it = pre; it < nk; ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!w(bar_empty(s), ph ^ 1u)) { ok = false; break; }
+                if (!w(bar_empty(s), ph ^ 1u)) break;
                 mbar_arrive_expect_tx(bar_full(s), tx);
                 const int k0 = (kb_begin + it) * kKb;
                 load_w(s, k0);
-                if (!p.x_lsu) tma_load_2d(base + off_x + s * x_stage, &tmX, bar_full(s), k0, 0, pol_x);
+                tma_load_2d(base + off_x + s * x_stage, &tmX, bar_full(s), k0, 0, pol_x);
+                issued = it + 1;
             }
-            if (!ok) {
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 100000ull) { }
-            }
+            // Copies already issued land before the ring is reused for the
+            // reduction or released: wait (bounded) for the last phase of each
+            // stage (immediately done in a run without abort).
+            for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
+                if (!mbar_wait_bounded(bar_full(it % kStages), (uint32_t)(it / kStages) & 1u, p.timeout_ns))
+                    atomicOr(p.status, ST_TIMEOUT_PRODUCER);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -243,52 +222,6 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // signals the epilogue once every MMA above has completed
             tc_commit_1(bar_acc);
         }
-    }
-
-    // ---- X tiles through the load/store path (epilogue warps, idle until the
-    // accumulator is ready), leaving the TMA unit to the weight stream.  Each
-    // 16-byte piece j of token row r lands at the 128-byte-swizzled position
-    // r*128 + ((j ^ (r % 8)) * 16) the MMA descriptor expects; pieces past M or
-    // K are zero-filled.  A stage is handed over (proxy fence, then one arrival
-    // per warp) once its copies are complete, up to stages-1 stages behind the
-    // issue (the producer of a stage needs the MMA to have drained the stage
-    // issued `stages` earlier, which this lag guarantees has been handed over).
-    if (KIND == 0 && warp >= 2 && p.x_lsu) {   // 16-bit X only
-        const int lag = kStages - 1;
-        const BoundedWait w{p.timeout_ns, abort_flag, p.status, ST_TIMEOUT_EPILOGUE};
-        const int et = (int)threadIdx.x - 64;          // 0..127
-        const int nk = kb_end - kb_begin;
-        const char* X = reinterpret_cast<const char*>(p.X);
-        auto hand_over = [&](int it) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar_full(it % kStages));
-        };
-        bool ok = true;
-        for (int it = 0; it < nk; ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            const bool free_slot = w(bar_empty(s), ph ^ 1u);
-            if (!__all_sync(0xffffffffu, free_slot)) { ok = false; break; }
-            const int k0 = (kb_begin + it) * 64;
-            const uint32_t xs = base + off_x + s * x_stage;
-            for (int c = et; c < mpad * 8; c += 128) {
-                const int r = c >> 3, j = c & 7;
-                const int kk = k0 + j * 8;
-                uint32_t bytes = 0;
-                if (r < p.M && kk < p.K) bytes = (p.K - kk) >= 8 ? 16u : (uint32_t)(p.K - kk) * 2u;
-                const void* src = bytes ? (const void*)(X + ((int64_t)r * p.ldx + kk) * 2) : p.X;
-                cp_async_16(xs + r * 128 + ((j ^ (r & 7)) << 4), src, bytes);
-            }
-            cp_async_commit();
-            if (it >= lag) {
-                cp_async_wait_n(lag);
-                hand_over(it - lag);
-            }
-        }
-        cp_async_wait<0>();
-        if (ok)
-            for (int it = nk - lag < 0 ? 0 : nk - lag; it < nk; ++it) hand_over(it);
     }
 
     // the epilogue warps, idle until the accumulator is ready, stage the

@@ -75,7 +75,9 @@ struct TcCfg {
     // max-pool hand-over between the lane quarters holding the two output rows
     static constexpr int kBarXFull = (kAbort + 4 + 7) / 8 * 8;
     static constexpr int kBarXEmpty = kBarXFull + 16;
-    static_assert(kBarXEmpty + 16 <= kMiscBytes, "misc layout");
+    // ring iterations each producer of the pair issued (read by the leader on exit)
+    static constexpr int kIssued = kBarXEmpty + 16;
+    static_assert(kIssued + 8 <= kMiscBytes, "misc layout");
     static_assert(kEpiWarps * 2 * kCStage >= 2 * 16384, "pool hand-over needs 16 KB per warp pair");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -204,6 +206,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto bar_xempty = [&](uint32_t i) { return misc + Cfg::kBarXEmpty + 8u * i; };
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + Cfg::kOffMisc + Cfg::kAbort);
+    volatile uint32_t* issued = reinterpret_cast<volatile uint32_t*>(base_ptr + Cfg::kOffMisc + Cfg::kIssued);
     uint32_t* tmem_ptr_smem = reinterpret_cast<uint32_t*>(base_ptr + Cfg::kOffMisc + Cfg::kTmemPtr);
 
     if (threadIdx.x == 0) {
@@ -221,6 +224,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(bar_xempty(i), 1);
         }
         *abort_flag = 0;
+        issued[0] = issued[1] = 0u;
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tmA);
         if (p.conv_pool) tma_prefetch_desc(&tmA2);
@@ -245,6 +249,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int nkb = p.num_k_blocks;
     // elements per 128-byte k-block row: 64 16-bit, 128 fp8 or 32 tf32
     constexpr int kBk = KIND == 1 ? 2 * TC_BK : (KIND == 2 ? TC_BK / 2 : TC_BK);
+
+    // K x N operand: one 64-column box per 64 columns a CTA holds; N x K
+    // operand: one full-height box (a half tile uses its top rows)
+    const bool boxes64 = p.b_mn_major != 0;
+    // bytes one CTA's copies bring per ring iteration of work item `item`
+    auto cta_bytes = [&](int item) -> uint32_t {
+        int tm, n0, nw;
+        work_item(item, p, tm, n0, nw);
+        return (uint32_t)Cfg::kAStage + (boxes64 ? (uint32_t)(nw / CG / 64) * 8192u : (uint32_t)Cfg::kBStage);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -317,9 +331,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         else tma_load_2d(dst, &tmA, bar, k0, m0, pol_a);
                     }
                 };
-                // K x N operand: one 64-column box per 64 columns this CTA holds;
-                // N x K operand: one full-height box (a half tile uses its top rows)
-                const bool boxes64 = p.b_mn_major != 0;
                 const int b_boxes = boxes64 ? nw / CG / 64 : 1;
                 const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBStage;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -354,11 +365,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             }
-            if (!ok) {
-                // Let copies already issued land before shared memory is released.
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 100000ull) { }
-            }
+            // iterations issued (a failed wait breaks before its copies): the
+            // leader reconciles both counts on exit (teardown below)
+            if (crank == 0) issued[0] = it;
+            else st_shared_cluster_u32(mapa_shared(smem_u32((const void*)(issued + 1)), 0), it);
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer ----
@@ -670,6 +680,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncwarp();
     tc_fence_before();
     if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+    if (warp == 0 && lane == 0 && crank == 0) {
+        // No CTA may release shared memory while one of its copies is in
+        // flight.  Every copy of the pair completes on the leader's full
+        // barriers, so the leader waits (bounded) for the last phase of each
+        // stage.  After an abort the two producers may have issued different
+        // numbers of iterations (at most one ring apart): phases only the peer
+        // issued are armed here with the peer's bytes; phases the leader armed
+        // for both but the peer never issued are credited the peer's bytes.
+        // In a run without abort both counts match and every phase is done.
+        const int nl = (int)issued[0];
+        const int np = CG == 2 ? (int)issued[1] : nl;
+        const int lo = nl < np ? nl : np, hi = nl < np ? np : nl;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t b = cta_bytes(unit + (i / nkb) * num_units);
+            if (i >= nl) mbar_arrive_expect_tx(bar_full(i % Cfg::kStages), b);
+            else mbar_complete_tx(bar_full(i % Cfg::kStages), b);
+        }
+        for (int i = hi - Cfg::kStages < 0 ? 0 : hi - Cfg::kStages; i < hi; ++i)
+            if (!mbar_wait_bounded(bar_full(i % Cfg::kStages), (uint32_t)(i / Cfg::kStages) & 1u, p.timeout_ns))
+                atomicOr(p.status, ST_TIMEOUT_PRODUCER);
+    }
+    __syncwarp();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, kTmemCols);

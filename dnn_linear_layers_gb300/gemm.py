@@ -21,8 +21,10 @@ E4M3_F32OUT, E4M3_BF16OUT, E5M2_F32OUT, E5M2_BF16OUT = 4, 5, 6, 7
 TF32_F32OUT, TF32_BF16OUT = 8, 9   # fp32 A and B, multiplied at tf32 precision
 FP8_DTYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
 B_KN, B_NK, B_CONST, A_KM = 0, 1, 2, 8
-(OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY, OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES,
- OPT_SKINNY_X_LSU, OPT_LOG, OPT_GEMV_MAX_M) = range(1, 11)
+OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY = 1, 2, 3, 4, 5
+OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES, OPT_LOG, OPT_GEMV_MAX_M = 6, 7, 9, 10
+OPTIONS = (OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY, OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES,
+           OPT_LOG, OPT_GEMV_MAX_M)
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_GEMV = 0, 1, 2, 3, 4, 5
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
     0, -1, -2, -3, -4, -5, -6)

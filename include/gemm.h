@@ -284,7 +284,6 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 #define GEMM_OPT_L2_POLICY 5       /* 0: A evict-last; 1: B evict-last; 2: both normal (default 0) */
 #define GEMM_OPT_SKINNY_SPLITS 6   /* small-M kernel k-slices: 0 = automatic (default), 1, 2, 4, 8 */
 #define GEMM_OPT_SKINNY_STAGES 7   /* small-M kernel ring depth: 0 = automatic (default), 2..8 */
-#define GEMM_OPT_SKINNY_X_LSU 8    /* 0/1: small-M kernel copies X with cp.async (default 0) */
 #define GEMM_OPT_LOG 9             /* 0/1: one line per launch on stderr (default 0) */
 #define GEMM_OPT_GEMV_MAX_M 10     /* M up to which the CUDA-core GEMV is chosen, 0..4 (default 1) */
 

@@ -162,6 +162,9 @@ void oracle_conv2d_at(int64_t Nb, int64_t H, int64_t W, int64_t Cin,
     (void)Nb;
     const int64_t OH = H + 2 * pad - R + 1, OW = W + 2 * pad - S_ + 1;
     (void)OH; (void)OW;
+    /* positions are independent: one thread per position, each sum in the
+     * order of the loop nest below */
+#pragma omp parallel for schedule(dynamic, 16)
     for (int64_t p = 0; p < npos; ++p) {
         const int64_t n = pos[3 * p], oh = pos[3 * p + 1], ow = pos[3 * p + 2];
         for (int64_t f = 0; f < Cout; ++f) {

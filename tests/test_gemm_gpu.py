@@ -113,7 +113,7 @@ def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
 @pytest.mark.parametrize("option,value", [(G.OPT_GROUP_M, 1), (G.OPT_GROUP_M, 16), (G.OPT_TAIL_SPLIT, 0),
                                           (G.OPT_K_SNAKE, 0), (G.OPT_PDL, 0), (G.OPT_L2_POLICY, 1),
                                           (G.OPT_L2_POLICY, 2), (G.OPT_SKINNY_SPLITS, 1),
-                                          (G.OPT_SKINNY_STAGES, 2), (G.OPT_SKINNY_X_LSU, 1)])
+                                          (G.OPT_SKINNY_STAGES, 2), (G.OPT_GEMV_MAX_M, 4)])
 @pytest.mark.parametrize("shape", [(1300, 530, 200), (4096, 4096, 72), (16, 1000, 1000)])
 def test_scheduling_options_change_no_result(plans, option, value, shape):
     """Every plan option only reschedules work: the results stay exact on
@@ -135,9 +135,9 @@ def test_scheduling_options_change_no_result(plans, option, value, shape):
 def test_option_ranges_are_checked(plans):
     p = G.Plan(0)
     for option, bad in [(G.OPT_GROUP_M, 0), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
-                        (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9), (0, 0),
-                        (99, 0)]:
-        before = p.get_option(option) if 1 <= option <= 10 else None
+                        (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9),
+                        (G.OPT_GEMV_MAX_M, 5), (0, 0), (8, 0), (99, 0)]:
+        before = p.get_option(option) if option in G.OPTIONS else None
         with pytest.raises(G.GemmError):
             p.set_option(option, bad)
         if before is not None:
@@ -301,14 +301,18 @@ def test_bounded_wait_reports_timeout_and_context_survives(plans, kernel):
     p = G.Plan(0, "kn")
     p.set_kernel(KERNELS[kernel])
     p.set_timeout_ns(20_000_000)          # 20 ms
-    p.set_debug(1)
-    A = torch.ones(256, 64, dtype=torch.bfloat16, device="cuda")
-    B = torch.ones(64, 256, dtype=torch.bfloat16, device="cuda")
-    C = torch.zeros(256, 256, device="cuda")
-    p.run(A, B, C)
-    assert p.status() == G.ERR_DEVICE_TIMEOUT
-    p.set_debug(0)
-    p.run(A, B, C)
-    assert p.status() == 0
-    assert torch.all(C == 64.0)
+    # one tile and one k-block; then several tiles per worker and a long K, so
+    # the abort comes while issued copies are still in flight (the exit path
+    # must let them land before shared memory is released)
+    for M, K in ((256, 64), (4096, 2048)):
+        p.set_debug(1)
+        A = torch.ones(M, K, dtype=torch.bfloat16, device="cuda")
+        B = torch.ones(K, M, dtype=torch.bfloat16, device="cuda")
+        C = torch.zeros(M, M, device="cuda")
+        p.run(A, B, C)
+        assert p.status() == G.ERR_DEVICE_TIMEOUT
+        p.set_debug(0)
+        p.run(A, B, C)
+        assert p.status() == 0
+        assert torch.all(C == float(K))
     p.close()

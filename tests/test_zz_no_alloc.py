@@ -6,8 +6,10 @@ scratch array that the library holds on each device instead of a plan
 workspace.
 
 Checked here through the C ABI: two calls in a row match the plan-based
-gemm_run within the parity tolerance, and a call whose packed operands would
-not fit in the scratch is refused before anything runs.  Collected last so a
+gemm_run within the parity tolerance; small M (the single-CTA branch) and
+K = 0 match the oracle exactly on integers; repeated calls change neither the
+device's free memory nor torch's allocator; and a call whose packed operands
+would not fit in the scratch is refused before anything runs.  Collected last so a
 run that stops at the first failure has run every other test first; passes
 alone in a fresh process as well.
 """
@@ -110,3 +112,70 @@ def test_noalloc_refuses_scratch_overflow_and_launches_nothing(lib):
     assert rc == G.OK
     torch.cuda.synchronize()
     assert torch.all(C == float(K))
+
+
+SMALL_M = [
+    # the single-CTA branch (M <= 128): misaligned A and B pitches, bias + ReLU
+    (GemmCase("noalloc_m1", 1, 1000, 777, b_nk=True, bias=True, relu=True, out="bf16", integer=True, seed=31),
+     (1, 3, 0)),
+    (GemmCase("noalloc_m128", 128, 520, 333, bias=True, relu=True, out="f32", integer=True, seed=32), (1, 1, 1)),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL_M)))
+def test_noalloc_small_m_exact(lib, idx):
+    case, (pa, pb, pc) = SMALL_M[idx]
+    A, B, bias = case.tensors()
+    Ad = strided(A, pa) if pa else A.cuda()
+    Bd = strided(B, pb) if pb else B.cuda()
+    od = torch.float32 if case.out == "f32" else torch.bfloat16
+    C = strided(torch.full((case.M, case.N), float("nan"), dtype=od), pc) if pc else \
+        torch.full((case.M, case.N), float("nan"), dtype=od, device="cuda")
+    for _ in range(2):
+        assert run_noalloc(lib, Ad, Bd, C, bias.cuda(), case.relu, case.b_nk) == G.OK
+        torch.cuda.synchronize()
+        ref = oracle.gemm(A, B, bias=bias, relu=case.relu, b_nk=case.b_nk)
+        want = oracle.bf16_round(ref) if od == torch.bfloat16 else ref
+        assert np.array_equal(C.double().cpu().numpy(), want), case.name
+
+
+def test_noalloc_k0_misaligned_c(lib):
+    """K = 0: C = epilogue(0) = ReLU(bias), written with any pitch."""
+    M, N = 37, 50
+    bias = torch.arange(-25, 25, dtype=torch.float32).to(torch.bfloat16).cuda()
+    C = strided(torch.full((M, N), float("nan")), 3)
+    A = torch.empty(M, 0, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
+    rc = lib.gemm_run_noalloc(M, N, 0, None, 0, None, 0, bias.data_ptr(), C.data_ptr(), _ld(C),
+                              G.EPI_BIAS_RELU, G.BF16_F32OUT, G.B_KN, None, torch.cuda.current_stream().cuda_stream)
+    assert rc == G.OK
+    torch.cuda.synchronize()
+    want = np.maximum(bias.double().cpu().numpy(), 0.0)[None, :].repeat(M, axis=0)
+    assert np.array_equal(C.double().cpu().numpy(), want)
+    del A, B
+
+
+def test_noalloc_allocates_no_device_memory(lib):
+    """Once a device is set up (first call: the scratch's address is looked up
+    and the kernels used are loaded), further calls -- including ones that pack
+    misaligned operands into the scratch -- change neither the device's free
+    memory nor torch's allocator: nothing is allocated."""
+    case, (pa, pb, pc) = CASES[0]
+    A, B, bias = case.tensors()
+    Ad, Bd, bd = strided(A, pa), strided(B, pb), bias.cuda()
+    C = strided(torch.empty((case.M, case.N), dtype=torch.bfloat16), pc)
+    A1, B1 = strided(A[:1], 1), strided(B.t().contiguous(), 3)      # M = 1, Linear weight layout
+    C1 = torch.empty((1, case.N), dtype=torch.bfloat16, device="cuda")
+
+    def calls():
+        assert run_noalloc(lib, Ad, Bd, C, bd, True, False) == G.OK
+        assert run_noalloc(lib, A1, B1, C1, bd, True, True) == G.OK
+        torch.cuda.synchronize()
+
+    calls()                                    # set-up and lazy kernel loading
+    free0, alloc0 = torch.cuda.mem_get_info(0)[0], torch.cuda.memory_allocated(0)
+    calls()
+    calls()
+    free1, alloc1 = torch.cuda.mem_get_info(0)[0], torch.cuda.memory_allocated(0)
+    assert alloc1 == alloc0
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
