@@ -12,10 +12,10 @@
 //   * one CTA owns 128 rows x 256 columns of the output; with cta_group::2 a
 //     pair of CTAs (a 2-CTA cluster) issues 256 x 256 x 16 MMAs, each CTA
 //     holding half of A's rows and half of B's columns in its own smem;
-//   * a k-block is one 128-byte swizzle row: 64 16-bit elements (kind::f16),
+//   * a k-atom is one 128-byte swizzle row: 64 16-bit elements (kind::f16),
 //     128 fp8 (kind::f8f6f4) or 32 tf32 (kind::tf32), four MMAs of 32 bytes
-//     each; a ring of stages (6 for a pair, 4 for a single CTA) keeps TMA loads
-//     ahead of the MMAs.  A (M x K, or K x M read MN-major) and B (N x K, or
+//     each; a ring of stages (3 stages of two atoms for a pair, 4 of one atom
+//     for a single CTA) keeps TMA loads ahead of the MMAs.  A (M x K, or K x M read MN-major) and B (N x K, or
 //     K x N read MN-major) come from 2-D tensor maps; for an implicit-GEMM
 //     convolution A comes through an im2col map of the NHWC activations (two
 //     maps, top and bottom rows of each row pair, for the fused max-pool);
@@ -53,10 +53,19 @@ constexpr int kUmmaK = 16;             // K per tcgen05.mma for 16-bit inputs
 
 template <int CG>
 struct TcCfg {
-    static constexpr int kStages = (CG == 2) ? 6 : 4;
+    // k-atoms (one 128-byte swizzle row per operand row: 64 16-bit, 128 fp8 or
+    // 32 tf32 elements) per ring stage.  A CTA pair takes two per stage: one
+    // full-barrier wait and one release per eight MMAs instead of four, which
+    // measured 6% faster at 8192^3 (the MMA thread's barrier round trip per
+    // stage, not the loads, held the tensor pipe back).  A single CTA keeps
+    // four one-atom stages (two slots would not cover the copy latency).
+    static constexpr int kAtoms = (CG == 2) ? 2 : 1;
+    static constexpr int kStages = (CG == 2) ? 3 : 4;
     static constexpr int kBnCta = TC_BN / CG;                    // B columns held per CTA
-    static constexpr int kAStage = TC_BM * TC_BK * 2;           // 16 KB
-    static constexpr int kBStage = kBnCta * TC_BK * 2;          // 16 or 32 KB
+    static constexpr int kAAtom = TC_BM * TC_BK * 2;            // 16 KB
+    static constexpr int kBAtom = kBnCta * TC_BK * 2;           // 16 or 32 KB
+    static constexpr int kAStage = kAtoms * kAAtom;
+    static constexpr int kBStage = kAtoms * kBAtom;
     static constexpr int kCStage = 32 * 128;                     // one warp's 32 rows x 128 B
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kAStage;
@@ -253,11 +262,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // K x N operand: one 64-column box per 64 columns a CTA holds; N x K
     // operand: one full-height box (a half tile uses its top rows)
     const bool boxes64 = p.b_mn_major != 0;
-    // bytes one CTA's copies bring per ring iteration of work item `item`
-    auto cta_bytes = [&](int item) -> uint32_t {
+    const int nst = (nkb + Cfg::kAtoms - 1) / Cfg::kAtoms;   // ring iterations per work item
+    auto atoms_of = [&](int stk) { return min(Cfg::kAtoms, nkb - stk * Cfg::kAtoms); };
+    // bytes one CTA's copies bring per k-atom of work item `item`
+    auto atom_bytes = [&](int item) -> uint32_t {
         int tm, n0, nw;
         work_item(item, p, tm, n0, nw);
-        return (uint32_t)Cfg::kAStage + (boxes64 ? (uint32_t)(nw / CG / 64) * 8192u : (uint32_t)Cfg::kBStage);
+        return (uint32_t)Cfg::kAAtom + (boxes64 ? (uint32_t)(nw / CG / 64) * 8192u : (uint32_t)Cfg::kBAtom);
+    };
+    // bytes of ring iteration i (counted over the whole persistent loop)
+    auto iter_bytes = [&](int i) -> uint32_t {
+        const int tc = i / nst, st = i - (i / nst) * nst;
+        const bool rv = p.k_snake && (tc & 1);
+        return (uint32_t)atoms_of(rv ? nst - 1 - st : st) * atom_bytes(unit + tc * num_units);
     };
 
     if (warp == 0) {
@@ -332,35 +349,43 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 };
                 const int b_boxes = boxes64 ? nw / CG / 64 : 1;
-                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBStage;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBAtom;
+                for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
                     if (!w.wait(bar_empty(s), ph ^ 1u)) { ok = false; break; }
-                    const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
-                    const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
-                    const int k0 = (rev ? nkb - 1 - kb : kb) * kBk;
+                    const int stk = rev ? nst - 1 - st : st;
+                    const int na = atoms_of(stk);
+                    const uint32_t bytes = (uint32_t)na * ((uint32_t)Cfg::kAAtom + b_bytes);
                     if constexpr (CG == 2) {
-                        const uint32_t fb = mapa_shared(bar_full(s), 0);
-                        if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * (Cfg::kAStage + b_bytes));
-                        load_a(sa, fb, k0, true);
-                        if (boxes64) {
-                            for (int c = 0; c < b_boxes; ++c) {
-                                const int bc = nb + 64 * c;
-                                if (p.b_mn_major) tma_load_2d_pair(sb + c * 8192, &tmB, fb, bc, k0, pol_b);
-                                else tma_load_2d_pair(sb + c * 8192, &tmB, fb, k0, bc, pol_b);
+                        if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * bytes);
+                    } else {
+                        mbar_arrive_expect_tx(bar_full(s), bytes);
+                    }
+                    for (int j = 0; j < na; ++j) {
+                        const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage + j * Cfg::kAAtom;
+                        const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage + j * Cfg::kBAtom;
+                        const int k0 = (stk * Cfg::kAtoms + j) * kBk;
+                        if constexpr (CG == 2) {
+                            const uint32_t fb = mapa_shared(bar_full(s), 0);
+                            load_a(sa, fb, k0, true);
+                            if (boxes64) {
+                                for (int c = 0; c < b_boxes; ++c) {
+                                    const int bc = nb + 64 * c;
+                                    if (p.b_mn_major) tma_load_2d_pair(sb + c * 8192, &tmB, fb, bc, k0, pol_b);
+                                    else tma_load_2d_pair(sb + c * 8192, &tmB, fb, k0, bc, pol_b);
+                                }
+                            } else {
+                                tma_load_2d_pair(sb, &tmB, fb, k0, nb, pol_b);
                             }
                         } else {
-                            tma_load_2d_pair(sb, &tmB, fb, k0, nb, pol_b);
-                        }
-                    } else {
-                        mbar_arrive_expect_tx(bar_full(s), Cfg::kAStage + b_bytes);
-                        load_a(sa, bar_full(s), k0, false);
-                        if (p.b_mn_major) {
-                            for (int c = 0; c < b_boxes; ++c)
-                                tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);
-                        } else {
-                            tma_load_2d(sb, &tmB, bar_full(s), k0, nb, pol_b);
+                            load_a(sa, bar_full(s), k0, false);
+                            if (p.b_mn_major) {
+                                for (int c = 0; c < b_boxes; ++c)
+                                    tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);
+                            } else {
+                                tma_load_2d(sb, &tmB, bar_full(s), k0, nb, pol_b);
+                            }
                         }
                     }
                 }
@@ -385,29 +410,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!w.wait(bar_tempty(a), aph ^ 1u)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + a * TC_BN;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const bool rev = p.k_snake && (tcount & 1u);
+                // descriptors built once; per stage, atom and MMA only the start
+                // address field (bits 0-13, address >> 4) moves
+                const uint64_t a0 = p.a_mn_major ? smem_desc_sw128(base + Cfg::kOffA, 8192, 1024)
+                                                 : smem_desc_sw128(base + Cfg::kOffA, 16, 1024);
+                const uint64_t b0 = p.b_mn_major ? smem_desc_sw128(base + Cfg::kOffB, 8192, 1024)
+                                                 : smem_desc_sw128(base + Cfg::kOffB, 16, 1024);
+                const uint32_t a_kstep = p.a_mn_major ? (kUmmaK * 128) >> 4 : 32 >> 4;
+                const uint32_t b_kstep = p.b_mn_major ? (kUmmaK * 128) >> 4 : 32 >> 4;
+                for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
                     // the stage's bytes arrived through the async proxy that the MMA
                     // reads with; the barrier wait alone orders them (no tcgen05 fence,
-                    // which would hold the tensor pipe at every k-block)
+                    // which would hold the tensor pipe at every stage)
                     if (!w.wait(bar_full(s), ph)) { ok = false; break; }
-                    const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage;
-                    const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage;
-                    // four MMAs per 128-byte k-block row: K = 16 bf16 / fp16 or
-                    // K = 32 fp8 elements, 32 bytes of every row each
+                    const int na = atoms_of(rev ? nst - 1 - st : st);
+                    const uint64_t as = a0 + (uint64_t)((s * Cfg::kAStage) >> 4);
+                    const uint64_t bs = b0 + (uint64_t)((s * Cfg::kBStage) >> 4);
+                    // four MMAs per k-atom, 32 bytes of every operand row each (K-major:
+                    // 32 bytes along the row; MN-major: 16 k-rows of 128 bytes)
+                    for (int j = 0; j < na; ++j)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // MN-major operands: 16 k-rows of 128 bytes per MMA, 64-wide
-                        // column boxes 8 KB apart
-                        const uint64_t adesc = p.a_mn_major
-                            ? smem_desc_sw128(sa + kk * (kUmmaK * 128), 8192, 1024)
-                            : smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bdesc = p.b_mn_major
-                            ? smem_desc_sw128(sb + kk * (kUmmaK * 128), 8192, 1024)
-                            : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                        tc_mma<CG, KIND>(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma<CG, KIND>(d_tmem, as + (uint64_t)((j * Cfg::kAAtom) >> 4) + kk * a_kstep,
+                                             bs + (uint64_t)((j * Cfg::kBAtom) >> 4) + kk * b_kstep, idesc,
+                                             (st | j | kk) != 0 ? 1u : 0u);
                     if constexpr (CG == 2) tc_commit_2(bar_empty(s), pair_mask); else tc_commit_1(bar_empty(s));
                 }
                 if (!ok) break;
@@ -693,7 +722,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int np = CG == 2 ? (int)issued[1] : nl;
         const int lo = nl < np ? nl : np, hi = nl < np ? np : nl;
         for (int i = lo; i < hi; ++i) {
-            const uint32_t b = cta_bytes(unit + (i / nkb) * num_units);
+            const uint32_t b = iter_bytes(i);
             if (i >= nl) mbar_arrive_expect_tx(bar_full(i % Cfg::kStages), b);
             else mbar_complete_tx(bar_full(i % Cfg::kStages), b);
         }
