@@ -304,6 +304,9 @@ class Workload:
         if args.kernel != "auto":
             self.plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY,
                                   "gemv": G.KERNEL_GEMV}[args.kernel])
+        for kv in args.opt or []:          # scheduling options (sweeps): NAME=VALUE, NAME as in GEMM_OPT_NAME
+            key, val = kv.split("=")
+            self.plan.set_option(getattr(G, "OPT_" + key.upper()), int(val))
         self.stream = torch.cuda.current_stream(dev)
         self.flops = attention_flops(name) if self.attn else 2.0 * M * N * K
         if self.attn:   # q, k, v read once, o written once
@@ -719,6 +722,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a graph replay")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode-layer lines appended to the default workload's result")
+    ap.add_argument("--opt", action="append", metavar="NAME=VALUE",
+                    help="set a plan scheduling option (sweeps), e.g. stream_k=0 or group_m=16")
     ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny", "gemv"], default="auto",
                     help="force a kernel (sweeps); the default lets the library choose")
     args = ap.parse_args()

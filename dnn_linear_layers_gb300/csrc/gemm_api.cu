@@ -39,6 +39,11 @@ struct gemm_plan {
     int debug_log = 0;            // GEMM_OPT_LOG: one line per launch on stderr
     int tail_split = 1;           // split the last wave's tiles into N-halves
     int k_snake = 1;              // serpentine k order across a worker's tiles (measured: -30% DRAM reads)
+    // stream-K: fewest k-atoms per worker, 0 = off.  Off by default: measured on
+    // GB300 it is within run-to-run noise or slower (FFN down 603 vs 589 us,
+    // 3000 x 5000 x 2048 53.2 vs 51.8 us): the partials' traffic and the
+    // reductions cost about what the balanced last wave gains.
+    int sk_min_atoms = 0;
     int skinny_splits = 0;        // 0: automatic; otherwise forced split count (sweeps)
     int skinny_stages = 0;        // 0: automatic; otherwise forced ring depth (sweeps)
     // M up to which an N x K Linear layer runs on the CUDA-core GEMV.  Measured
@@ -161,6 +166,41 @@ bool make_im2col_map(CUtensorMap* m, CUtensorMapDataType dt, const ConvA& c, int
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Device block owned by a plan: the status word, then the stream-K arrival
+// counters (zero between launches).
+constexpr size_t kStatusBlockBytes = 16384;
+constexpr int kSkCounterOffset = 64;                                  // ints
+constexpr int64_t kSkMaxTiles = (int64_t)(kStatusBlockBytes / 4 - kSkCounterOffset) / 8;
+
+// Stream-K split of a persistent launch of T >= U tiles on U workers with
+// nkb k-atoms per tile: the T mod U tiles of the last, partial wave are cut
+// into equal ranges of atoms over W <= U workers, at least min_atoms each, so
+// every worker carries the same number of atoms; the split pieces run first
+// and their reductions overlap the whole tiles that follow.  A grid of fewer
+// than U tiles is not split: measured on GB300, the reductions at the end of
+// such a launch (2048^3: 29 us against 17.4 us unsplit) cost more than the
+// balance gains.  maxc is the most workers sharing one tile; no split
+// (tiles = 0) when no tile would be shared.
+struct SkSplit { int64_t tiles = 0, workers = 0, maxc = 0; };
+SkSplit plan_stream_k(int64_t T, int64_t U, int64_t nkb, int64_t min_atoms) {
+    SkSplit sk;
+    if (min_atoms <= 0 || U < 2 || nkb < 1 || T < U) return sk;
+    const int64_t Tsk = T % U;
+    if (Tsk == 0 || Tsk > kSkMaxTiles) return sk;
+    const int64_t A = Tsk * nkb;
+    int64_t W = A / min_atoms;
+    if (W > U) W = U;
+    if (W < 2) return sk;
+    int64_t maxc = 1;
+    for (int64_t t = 0; t < Tsk; ++t) {
+        const int64_t wf = ((t * nkb + 1) * W - 1) / A, wl = ((t + 1) * nkb * W - 1) / A;
+        if (wl - wf + 1 > maxc) maxc = wl - wf + 1;
+    }
+    if (maxc < 2) return sk;
+    sk.tiles = Tsk; sk.workers = W; sk.maxc = maxc;
+    return sk;
+}
 
 bool in_is_bf16(int dtype) { return dtype == DT_BF16_F32 || dtype == DT_BF16_BF16; }
 int in_bytes(int dtype) { return dtype_is_fp8(dtype) ? 1 : (dtype_is_tf32(dtype) ? 4 : 2); }
@@ -412,9 +452,9 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
     }
     p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
     p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
-    e = cudaMalloc(&p->status_dev, sizeof(int));
+    e = cudaMalloc(&p->status_dev, kStatusBlockBytes);
     if (e != cudaSuccess) { delete p; return GEMM_ERR_NO_MEMORY; }
-    e = cudaMemset(p->status_dev, 0, sizeof(int));
+    e = cudaMemset(p->status_dev, 0, kStatusBlockBytes);
     if (e != cudaSuccess) { cudaFree(p->status_dev); delete p; return GEMM_ERR_CUDA; }
     *plan = p;
     return GEMM_OK;
@@ -490,6 +530,9 @@ int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
         case GEMM_OPT_GEMV_MAX_M:
             if (v < 0 || v > kGemvMaxM) return GEMM_ERR_INVALID_ARG;
             p->gemv_max_m = (int)v; return GEMM_OK;
+        case GEMM_OPT_STREAM_K:
+            if (v < 0 || v > 4096) return GEMM_ERR_INVALID_ARG;
+            p->sk_min_atoms = (int)v; return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -506,6 +549,7 @@ int gemm_plan_get_option(gemm_plan_t p, int option, int64_t* v) {
         case GEMM_OPT_SKINNY_STAGES: *v = p->skinny_stages; return GEMM_OK;
         case GEMM_OPT_LOG: *v = p->debug_log; return GEMM_OK;
         case GEMM_OPT_GEMV_MAX_M: *v = p->gemv_max_m; return GEMM_OK;
+        case GEMM_OPT_STREAM_K: *v = p->sk_min_atoms; return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -519,7 +563,9 @@ int gemm_plan_status(gemm_plan_t p) {
     e = cudaMemcpy(&st, p->status_dev, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return record(p, e);
     if (st != 0) {
-        cudaMemset(p->status_dev, 0, sizeof(int));
+        // an aborted launch may leave stream-K arrival counters behind: clear
+        // them with the status word
+        cudaMemset(p->status_dev, 0, kStatusBlockBytes);
         cudaDeviceSynchronize();
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
@@ -622,13 +668,22 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const bool gemv = kernel == GEMM_KERNEL_GEMV;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
     const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
+    const int kbk = 128 / in_bytes(dtype);          // elements per 128-byte k-atom row
+    // persistent grid of the tensor-core kernels, and the stream-K split of its
+    // last wave (not for the fused max-pool, whose epilogue pools whole tiles)
+    const int64_t num_m_tiles = (M + TC_BM * cg - 1) / (TC_BM * cg), num_n_tiles = (N + TC_BN - 1) / TC_BN;
+    const int64_t num_kb = (K + kbk - 1) / kbk;
+    const int64_t tiles = num_m_tiles * num_n_tiles;
+    const int64_t cap = cg == 2 ? p->max_pairs[dtype] : p->max_singles[dtype];
+    SkSplit sk;
+    if (!gemv && !skinny && !(conv && conv->pool)) sk = plan_stream_k(tiles, cap, num_kb, p->sk_min_atoms);
+    const size_t sk_bytes = (size_t)(sk.tiles * sk.maxc) * 8u * 32u * (size_t)TC_BN * 4u;
 
     // ---- operand alignment: pack anything that breaks the TMA 16-byte rule
     const int ob = out_bytes(dtype);
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
     const int64_t a_rows = a_km ? K : M, a_cols = a_km ? M : K;
     const int es = in_bytes(dtype);                 // element size of A and B
-    const int kbk = 128 / es;                       // elements per 128-byte k-block row
     const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
     const bool b_ok = aligned16(B) && (ldb * es) % 16 == 0;
     // the small-M kernels store C with plain stores: any pitch is fine
@@ -636,6 +691,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const void* A_use = A; int64_t lda_use = lda;
     const void* B_use = B; int64_t ldb_use = ldb;
     void* C_use = C; int64_t ldc_use = ldc;
+    float* sk_part = nullptr;
     if (!a_ok || !b_ok || !c_ok) {
         if (!p->packing) return GEMM_ERR_ALIGNMENT;
         const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es),
@@ -643,9 +699,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         const size_t a_bytes = a_ok ? 0 : (size_t)round_up(a_rows * lda_p * es, 256);
         const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * es, 256);
         const size_t c_bytes = c_ok ? 0 : (size_t)round_up(M * ldc_p * ob, 256);
-        rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes);
+        rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes + sk_bytes);
         if (rc != GEMM_OK) return rc;
         char* ws = static_cast<char*>(p->workspace);
+        if (sk_bytes) sk_part = reinterpret_cast<float*>(ws + a_bytes + b_bytes + c_bytes);
         if (!a_ok) {
             e = launch_copy2d(A, lda, ws, lda_p, a_rows, a_cols, es, stream);
             if (e != cudaSuccess) return record(p, e);
@@ -659,6 +716,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
             B_use = ws + a_bytes; ldb_use = ldb_p;
         }
         if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
+    } else if (sk_bytes) {
+        rc = ensure_workspace(p, sk_bytes);
+        if (rc != GEMM_OK) return rc;
+        sk_part = static_cast<float*>(p->workspace);
     }
 
     if (gemv) {
@@ -700,9 +761,9 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
     prm.M = (int32_t)M; prm.N = (int32_t)N; prm.K = (int32_t)K;
-    prm.num_m_tiles = (int32_t)((M + TC_BM * cg - 1) / (TC_BM * cg));
-    prm.num_n_tiles = (int32_t)((N + TC_BN - 1) / TC_BN);
-    prm.num_k_blocks = (int32_t)((K + kbk - 1) / kbk);
+    prm.num_m_tiles = (int32_t)num_m_tiles;
+    prm.num_n_tiles = (int32_t)num_n_tiles;
+    prm.num_k_blocks = (int32_t)num_kb;
     prm.group_m = p->group_m;
     prm.epi = epi;
     prm.ex = ex;
@@ -733,15 +794,26 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
             prm.pool_vec16 = (aligned16(conv->pool_y) && (conv->pool_ldy * ob) % 16 == 0) ? 1u : 0u;
         }
     }
-    const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
-    const int64_t cap = cg == 2 ? p->max_pairs[dtype] : p->max_singles[dtype];
-    const int64_t units = tiles < cap ? tiles : cap;
-    prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
+    // workers: one per co-resident CTA (pair), fewer for small problems
+    int64_t units = tiles < cap ? tiles : cap;
+    if (sk.tiles) {
+        if (sk.workers > units) units = sk.workers;
+        prm.sk_tiles = (int32_t)sk.tiles;
+        prm.sk_workers = (int32_t)sk.workers;
+        prm.sk_maxc = (int32_t)sk.maxc;
+        prm.sk_cnt = p->status_dev + kSkCounterOffset;
+        prm.sk_part = sk_part;
+        prm.num_full = (int32_t)(tiles - sk.tiles);   // the rest are whole waves
+    } else {
+        prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
+    }
     prm.idesc_half = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN / 2, a_km);
     if (p->debug_log)
-        std::fprintf(stderr, "[gemm] tc cta_group=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld split=%lld grid=%lld packed=%d%d%d\n",
-                     cg, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)(tiles - prm.num_full),
+        std::fprintf(stderr, "[gemm] tc cta_group=%d conv=%u M=%lld N=%lld K=%lld tiles=%lld sk=%lldx%lld/%lld "
+                     "split=%lld grid=%lld packed=%d%d%d\n",
+                     cg, prm.conv, (long long)M, (long long)N, (long long)K, (long long)tiles, (long long)sk.tiles,
+                     (long long)sk.maxc, (long long)sk.workers, (long long)(tiles - sk.tiles - prm.num_full),
                      (long long)(units * cg), A_use != A, B_use != B, C_use != C);
     e = launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream,
                        (conv && conv->pool) ? &tmA2 : nullptr);

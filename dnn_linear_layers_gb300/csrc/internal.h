@@ -58,7 +58,7 @@ struct TcParams {
     int32_t num_n_tiles;   // tiles of TC_BN columns
     int32_t num_k_blocks;  // ceil(K / TC_BK)
     int32_t group_m;       // rasterisation: m-tiles per group
-    int32_t num_full;      // tiles run whole; the tiles after them run as two N-halves
+    int32_t num_full;      // tiles after the split ones run whole; the rest as two N-halves
     uint32_t idesc_half;   // instruction descriptor for a half tile (N = TC_BN / 2)
     uint32_t epi;          // EpiFlags
     uint32_t idesc;        // tcgen05 instruction descriptor
@@ -73,6 +73,20 @@ struct TcParams {
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
     EpiArgs ex;            // alpha / scale / beta operands of the epilogue
+    // Stream-K (sk_tiles > 0): tiles [0, sk_tiles) of the raster are split into
+    // equal ranges of k-atoms over workers [0, sk_workers) (worker w takes atoms
+    // [w A / W, (w + 1) A / W) of the A = sk_tiles * num_k_blocks atoms, in tile
+    // order); each worker runs its pieces of them first, then whole tiles from
+    // sk_tiles on.  A split tile's contributors leave fp32 partials in sk_part
+    // (sk_tiles x sk_maxc x 8 slots of 32 rows x 256 columns) and count their
+    // arrival in sk_cnt (sk_tiles x 8, zero between launches); the last arrival
+    // of each 32-row slot adds the partials in contributor order and applies
+    // the epilogue.
+    int32_t sk_tiles;
+    int32_t sk_workers;
+    int32_t sk_maxc;
+    int* sk_cnt;
+    float* sk_part;
     // Implicit-GEMM convolution (conv != 0): A is not a matrix but an NHWC
     // activation tensor read through an im2col tensor map; row m of A is
     // output pixel m = (n * out_h + oh) * out_w + ow and k-block kb is channel

@@ -126,23 +126,84 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n
     tn = r / rows;
 }
 
-// Work item -> output region.  Items [0, num_full) are whole 256-column
-// tiles in raster order; each later tile is split into two 128-column halves
-// (two consecutive items), which evens out the last, partial wave of the
-// persistent grid.
+// Whole-tile work item -> output region.  Items [0, num_full) are whole
+// 256-column tiles in raster order from tile sk_tiles on; each later tile is
+// split into two 128-column halves (two consecutive items), which evens out
+// the last, partial wave of the persistent grid when stream-K is off.
 __device__ __forceinline__ void work_item(int item, const TcParams& p, int& tm, int& n0, int& nw) {
     int tile, half = -1;
     if (item < p.num_full) {
-        tile = item;
+        tile = p.sk_tiles + item;
     } else {
         const int j = item - p.num_full;
-        tile = p.num_full + (j >> 1);
+        tile = p.sk_tiles + p.num_full + (j >> 1);
         half = j & 1;
     }
     int tn;
     tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.group_m, tm, tn);
     n0 = tn * TC_BN + (half > 0 ? TC_BN / 2 : 0);
     nw = half < 0 ? TC_BN : TC_BN / 2;
+}
+
+// One piece of a worker's sequence: a k-range of a split tile (stream-K) or
+// a whole tile (or N-half).
+struct Piece {
+    int tm, n0, nw;          // output region: tile row, first column, width
+    int kb0, nkb;            // k-atoms [kb0, kb0 + nkb) of the tile
+    int tile;                // split tiles: tile index (< sk_tiles)
+    int contrib, ncontrib;   // split tiles: this worker's rank among the contributors (k order), their number
+    bool partial;            // the tile has other contributors
+    bool rev;                // walk the tile's k-stages backwards (serpentine order)
+};
+
+// Worker owning stream-K atom a when A atoms are split over W workers in
+// equal ranges [w A / W, (w + 1) A / W): the largest w with w A / W <= a.
+__device__ __forceinline__ int sk_owner(int64_t a, int64_t A, int64_t W) { return (int)(((a + 1) * W - 1) / A); }
+
+// Piece idx of worker `unit`'s sequence (stream-K pieces, then whole tiles
+// every num_units); false past its end.  Producer, MMA issuer and epilogue
+// walk the same sequence.
+__device__ __forceinline__ bool piece_at(const TcParams& p, int unit, int num_units, int idx, Piece& pc) {
+    const int nkb = p.num_k_blocks;
+    const int64_t A = (int64_t)p.sk_tiles * nkb, W = p.sk_workers;
+    int n_sk = 0;
+    int64_t s = 0, e = 0;
+    if (unit < p.sk_workers) {                 // W <= A: every range is non-empty
+        s = (int64_t)unit * A / W;
+        e = (int64_t)(unit + 1) * A / W;
+        n_sk = (int)((e - 1) / nkb - s / nkb + 1);
+    }
+    if (idx < n_sk) {
+        const int t = (int)(s / nkb) + idx;
+        const int64_t t0 = (int64_t)t * nkb;
+        const int64_t lo = s > t0 ? s : t0, hi = e < t0 + nkb ? e : t0 + nkb;
+        pc.kb0 = (int)(lo - t0);
+        pc.nkb = (int)(hi - lo);
+        const int wf = sk_owner(t0, A, W), wl = sk_owner(t0 + nkb - 1, A, W);
+        pc.ncontrib = wl - wf + 1;
+        pc.contrib = unit - wf;
+        pc.partial = pc.ncontrib > 1;
+        pc.tile = t;
+        pc.rev = false;
+        int tn;
+        tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, pc.tm, tn);
+        pc.n0 = tn * TC_BN;
+        pc.nw = TC_BN;
+        return true;
+    }
+    const int j = idx - n_sk;
+    const int dp_items = p.num_full + 2 * (p.num_m_tiles * p.num_n_tiles - p.sk_tiles - p.num_full);
+    const int item = unit + j * num_units;
+    if (item >= dp_items) return false;
+    work_item(item, p, pc.tm, pc.n0, pc.nw);
+    pc.kb0 = 0;
+    pc.nkb = nkb;
+    pc.tile = -1;
+    pc.contrib = 0;
+    pc.ncontrib = 1;
+    pc.partial = false;
+    pc.rev = p.k_snake && (j & 1);
+    return true;
 }
 
 template <typename OutT> struct OutTraits;
@@ -253,8 +314,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     grid_dependency_wait();
     grid_launch_dependents();
 
-    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
-    const int num_items = p.num_full + 2 * (num_tiles - p.num_full);
     const int nkb = p.num_k_blocks;
     // elements per 128-byte k-block row: 64 16-bit, 128 fp8 or 32 tf32
     constexpr int kBk = KIND == 1 ? 2 * TC_BK : (KIND == 2 ? TC_BK / 2 : TC_BK);
@@ -262,19 +321,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // K x N operand: one 64-column box per 64 columns a CTA holds; N x K
     // operand: one full-height box (a half tile uses its top rows)
     const bool boxes64 = p.b_mn_major != 0;
-    const int nst = (nkb + Cfg::kAtoms - 1) / Cfg::kAtoms;   // ring iterations per work item
-    auto atoms_of = [&](int stk) { return min(Cfg::kAtoms, nkb - stk * Cfg::kAtoms); };
-    // bytes one CTA's copies bring per k-atom of work item `item`
-    auto atom_bytes = [&](int item) -> uint32_t {
-        int tm, n0, nw;
-        work_item(item, p, tm, n0, nw);
+    // ring iterations (stages) of a piece, and the k-atoms of its stage stk
+    auto stages_of = [](const Piece& pc) { return (pc.nkb + Cfg::kAtoms - 1) / Cfg::kAtoms; };
+    auto atoms_of = [](const Piece& pc, int stk) { return min(Cfg::kAtoms, pc.nkb - stk * Cfg::kAtoms); };
+    // bytes one CTA's copies bring per k-atom of a piece nw columns wide
+    auto atom_bytes = [&](int nw) -> uint32_t {
         return (uint32_t)Cfg::kAAtom + (boxes64 ? (uint32_t)(nw / CG / 64) * 8192u : (uint32_t)Cfg::kBAtom);
     };
-    // bytes of ring iteration i (counted over the whole persistent loop)
+    // bytes of ring iteration i (counted over the worker's whole sequence)
     auto iter_bytes = [&](int i) -> uint32_t {
-        const int tc = i / nst, st = i - (i / nst) * nst;
-        const bool rv = p.k_snake && (tc & 1);
-        return (uint32_t)atoms_of(rv ? nst - 1 - st : st) * atom_bytes(unit + tc * num_units);
+        for (int idx = 0;; ++idx) {
+            Piece pc;
+            if (!piece_at(p, unit, num_units, idx, pc)) return 0u;
+            const int n = stages_of(pc);
+            if (i < n) return (uint32_t)atoms_of(pc, pc.rev ? n - 1 - i : i) * atom_bytes(pc.nw);
+            i -= n;
+        }
     };
 
     if (warp == 0) {
@@ -285,14 +347,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // each B panel only across the group's rows, so A is the operand to keep.
             const uint64_t pol_a = p.l2_policy == 0 ? l2_policy_evict_last() : l2_policy_evict_normal();
             const uint64_t pol_b = p.l2_policy == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
-            uint32_t it = 0, tcount = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int item = unit; item < num_items && ok; item += num_units, ++tcount) {
-                int tm, n0, nw;
-                work_item(item, p, tm, n0, nw);
-                // serpentine k order: a tile starts on the k-slabs the previous one
-                // ended on, which are the ones most likely still in L2
-                const bool rev = p.k_snake && (tcount & 1u);
+            for (int idx = 0; ok; ++idx) {
+                Piece pc;
+                if (!piece_at(p, unit, num_units, idx, pc)) break;
+                const int tm = pc.tm, n0 = pc.n0, nw = pc.nw;
+                // serpentine k order (whole tiles): a tile starts on the k-slabs the
+                // previous one ended on, which are the ones most likely still in L2
+                const bool rev = pc.rev;
+                const int nst = stages_of(pc);
                 const int m0 = tm * TC_BM * CG + (int)crank * TC_BM;
                 const int nb = n0 + (int)crank * (nw / CG);
                 // implicit GEMM: base pixel (top-left of the filter window) of row m0
@@ -355,7 +419,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
                     if (!w.wait(bar_empty(s), ph ^ 1u)) { ok = false; break; }
                     const int stk = rev ? nst - 1 - st : st;
-                    const int na = atoms_of(stk);
+                    const int na = atoms_of(pc, stk);
                     const uint32_t bytes = (uint32_t)na * ((uint32_t)Cfg::kAAtom + b_bytes);
                     if constexpr (CG == 2) {
                         if (crank == 0) mbar_arrive_expect_tx(bar_full(s), 2u * bytes);
@@ -365,7 +429,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int j = 0; j < na; ++j) {
                         const uint32_t sa = base + Cfg::kOffA + s * Cfg::kAStage + j * Cfg::kAAtom;
                         const uint32_t sb = base + Cfg::kOffB + s * Cfg::kBStage + j * Cfg::kBAtom;
-                        const int k0 = (stk * Cfg::kAtoms + j) * kBk;
+                        const int k0 = (pc.kb0 + stk * Cfg::kAtoms + j) * kBk;
                         if constexpr (CG == 2) {
                             const uint32_t fb = mapa_shared(bar_full(s), 0);
                             load_a(sa, fb, k0, true);
@@ -403,14 +467,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint16_t pair_mask = 0x3u;
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int item = unit; item < num_items && ok; item += num_units, ++tcount) {
-                const uint32_t idesc = (item < p.num_full) ? p.idesc : p.idesc_half;
+            for (int idx = 0; ok; ++idx, ++tcount) {
+                Piece pc;
+                if (!piece_at(p, unit, num_units, idx, pc)) break;
+                const uint32_t idesc = pc.nw == TC_BN ? p.idesc : p.idesc_half;
+                const int nst = stages_of(pc);
                 const uint32_t a = tcount & 1u;
                 const uint32_t aph = (tcount >> 1) & 1u;
                 if (!w.wait(bar_tempty(a), aph ^ 1u)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + a * TC_BN;
-                const bool rev = p.k_snake && (tcount & 1u);
+                const bool rev = pc.rev;
                 // descriptors built once; per stage, atom and MMA only the start
                 // address field (bits 0-13, address >> 4) moves
                 const uint64_t a0 = p.a_mn_major ? smem_desc_sw128(base + Cfg::kOffA, 8192, 1024)
@@ -426,7 +493,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // reads with; the barrier wait alone orders them (no tcgen05 fence,
                     // which would hold the tensor pipe at every stage)
                     if (!w.wait(bar_full(s), ph)) { ok = false; break; }
-                    const int na = atoms_of(rev ? nst - 1 - st : st);
+                    const int na = atoms_of(pc, rev ? nst - 1 - st : st);
                     const uint64_t as = a0 + (uint64_t)((s * Cfg::kAStage) >> 4);
                     const uint64_t bs = b0 + (uint64_t)((s * Cfg::kBStage) >> 4);
                     // four MMAs per k-atom, 32 bytes of every operand row each (K-major:
@@ -465,9 +532,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t tempty_leader0 = (CG == 2) ? mapa_shared(bar_tempty(0), 0) : bar_tempty(0);
         const uint32_t tempty_leader1 = (CG == 2) ? mapa_shared(bar_tempty(1), 0) : bar_tempty(1);
         uint32_t tcount = 0, cstore = 0;
-        for (int item = unit; item < num_items; item += num_units, ++tcount) {
-            int tm, n0, nw;
-            work_item(item, p, tm, n0, nw);
+        for (int idx = 0;; ++idx, ++tcount) {
+            Piece pc;
+            if (!piece_at(p, unit, num_units, idx, pc)) break;
+            const int tm = pc.tm, n0 = pc.n0, nw = pc.nw;
             const int kChunks = nw / kCols;
             const int m0 = tm * TC_BM * CG + (int)crank * TC_BM;
             const int row0 = m0 + 32 * (int)q;
@@ -591,22 +659,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (!ok) break;
                 continue;
             }
-            for (int c = 0; c < kChunks; ++c) {
-                float v[kCols];
-#pragma unroll
-                for (int h = 0; h < kCols / 32; ++h) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(t_row + c * kCols + h * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[h * 32 + j] = __uint_as_float(r[j]);
-                }
-                if (c == kChunks - 1) {
-                    // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
-                }
+            // A chunk of kCols columns (each lane its row's values): alpha, scale,
+            // bias, beta * previous C, ReLU, cast, swizzled staging, TMA store.
+            auto finish_chunk = [&](int c, float (&v)[kCols]) {
                 const int cb = n0 + c * kCols;
                 if (p.epi & EPI_ALPHA) {
 #pragma unroll
@@ -699,6 +754,85 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     bulk_commit_group();
                 }
                 ++cstore;
+            };
+            if (pc.partial) {
+                // Stream-K: this worker holds part of the tile's K range.  The warp
+                // writes its fp32 partial (32 rows x 256 columns) into its slot of
+                // the tile: 16-byte piece j (columns 4j .. 4j + 3) of 32-column chunk
+                // cc of lane l's row at float4 (cc * 8 + j) * 32 + l, so each warp
+                // access covers 512 contiguous bytes (coalesced),
+                // frees the accumulator, and counts its arrival once its stores are
+                // visible (fence, then atomic).  The last arrival of the slot (which
+                // waits for no one) adds the contributors' partials in k order,
+                // its own included, so the sum does not depend on arrival order,
+                // runs the epilogue and resets the counter for the next launch.
+                const int g = (int)crank * 4 + (int)q;
+                auto slot = [&](int c) {
+                    return p.sk_part + ((((int64_t)pc.tile * p.sk_maxc + c) * 8 + g) << 13);
+                };
+                float* const mine = slot(pc.contrib);
+                for (int cc = 0; cc < TC_BN / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + cc * 32, r);
+                    tmem_ld_wait();
+                    float4* dst = reinterpret_cast<float4*>(mine) + cc * 256 + (int)lane;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(dst + 32 * j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+                __threadfence();
+                __syncwarp();
+                int old = 0;
+                if (lane == 0) old = atomicAdd(p.sk_cnt + pc.tile * 8 + g, 1);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old != pc.ncontrib - 1) continue;
+                __threadfence();
+                for (int c = 0; c < kChunks; ++c) {
+                    float v[kCols];
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) v[j] = 0.0f;
+                    for (int k = 0; k < pc.ncontrib; ++k) {
+                        const float* src = slot(k);
+#pragma unroll
+                        for (int h = 0; h < kCols / 32; ++h) {
+                            const float4* s4 =
+                                reinterpret_cast<const float4*>(src) + (c * (kCols / 32) + h) * 256 + (int)lane;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 x = __ldcg(s4 + 32 * j);
+                                v[h * 32 + 4 * j] += x.x;
+                                v[h * 32 + 4 * j + 1] += x.y;
+                                v[h * 32 + 4 * j + 2] += x.z;
+                                v[h * 32 + 4 * j + 3] += x.w;
+                            }
+                        }
+                    }
+                    finish_chunk(c, v);
+                }
+                if (lane == 0) p.sk_cnt[pc.tile * 8 + g] = 0;
+                continue;
+            }
+            for (int c = 0; c < kChunks; ++c) {
+                float v[kCols];
+#pragma unroll
+                for (int h = 0; h < kCols / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c * kCols + h * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[h * 32 + j] = __uint_as_float(r[j]);
+                }
+                if (c == kChunks - 1) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(a ? tempty_leader1 : tempty_leader0);
+                }
+                finish_chunk(c, v);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

@@ -286,6 +286,13 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 #define GEMM_OPT_SKINNY_STAGES 7   /* small-M kernel ring depth: 0 = automatic (default), 2..8 */
 #define GEMM_OPT_LOG 9             /* 0/1: one line per launch on stderr (default 0) */
 #define GEMM_OPT_GEMV_MAX_M 10     /* M up to which the CUDA-core GEMV is chosen, 0..4 (default 1) */
+/* Stream-K on the tensor-core kernels: in a launch of at least one full wave
+ * of tiles, the tiles of the last, partial wave are split by k over the
+ * workers so every worker carries the same work; the value is the fewest
+ * k-atoms a worker takes (0: off, the last wave runs as N-halves; default
+ * 0, off; 8 is a good value).  Split tiles keep fp32 partials in the plan's
+ * workspace. */
+#define GEMM_OPT_STREAM_K 11
 
 /* Set / read a GEMM_OPT_* option.  GEMM_ERR_INVALID_ARG for a NULL plan, an
  * unknown option or a value outside the option's range (nothing changes). */

@@ -127,6 +127,7 @@ def test_conv2d_scale_bias_relu_residual_exact(implicit):
     res = ints((Nb * H * W, Cout), 55, -40, 40).float()
     y = res.clone().cuda()
     with G.Plan(0, "nk") as p:
+        p.set_option(G.OPT_STREAM_K, 0)   # the workspace then holds only an im2col matrix
         p.conv2d(x.cuda(), w.cuda(), y, bias.cuda(), True, pad=pad, beta=1.0, scale=scale.cuda())
         assert p.status() == 0
         assert (p.workspace_bytes == 0) == implicit

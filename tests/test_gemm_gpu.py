@@ -104,16 +104,24 @@ def test_tails_integer_exact(plans, M, N, K, kernel):
 @pytest.mark.parametrize("b_nk", [False, True])
 @pytest.mark.parametrize("shape", [(4096, 4096, 72), (2304, 4352, 40)])
 def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
-    """Shapes whose last persistent wave is partial: its tiles run as two
-    128-column halves (whole tiles first, then halves); every output checked."""
+    """Shapes whose last persistent wave is partial, with stream-K off: its
+    tiles run as two 128-column halves (whole tiles first, then halves); every
+    output checked."""
     M, N, K = shape
-    check(plans, GemmCase("tail_split", M, N, K, b_nk=b_nk, bias=True, out="bf16", integer=True, seed=K), kernel)
+    with G.Plan(0, "nk" if b_nk else "kn") as p:
+        p.set_option(G.OPT_STREAM_K, 0)
+        case = GemmCase("tail_split", M, N, K, b_nk=b_nk, bias=True, out="bf16", integer=True, seed=K)
+        A, B, bias, C = run_case(p, case, kernel=KERNELS[kernel])
+        assert p.workspace_bytes == 0
+        C_ref, S = oracle_full(case, A, B, bias)
+        compare(case, C, C_ref, S)
 
 
 @pytest.mark.parametrize("option,value", [(G.OPT_GROUP_M, 1), (G.OPT_GROUP_M, 16), (G.OPT_TAIL_SPLIT, 0),
                                           (G.OPT_K_SNAKE, 0), (G.OPT_PDL, 0), (G.OPT_L2_POLICY, 1),
                                           (G.OPT_L2_POLICY, 2), (G.OPT_SKINNY_SPLITS, 1),
-                                          (G.OPT_SKINNY_STAGES, 2), (G.OPT_GEMV_MAX_M, 4)])
+                                          (G.OPT_SKINNY_STAGES, 2), (G.OPT_GEMV_MAX_M, 4), (G.OPT_STREAM_K, 0),
+                                          (G.OPT_STREAM_K, 1)])
 @pytest.mark.parametrize("shape", [(1300, 530, 200), (4096, 4096, 72), (16, 1000, 1000)])
 def test_scheduling_options_change_no_result(plans, option, value, shape):
     """Every plan option only reschedules work: the results stay exact on
@@ -136,7 +144,8 @@ def test_option_ranges_are_checked(plans):
     p = G.Plan(0)
     for option, bad in [(G.OPT_GROUP_M, 0), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
                         (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9),
-                        (G.OPT_GEMV_MAX_M, 5), (0, 0), (8, 0), (99, 0)]:
+                        (G.OPT_GEMV_MAX_M, 5), (G.OPT_STREAM_K, -1), (G.OPT_STREAM_K, 5000), (0, 0), (8, 0),
+                        (99, 0)]:
         before = p.get_option(option) if option in G.OPTIONS else None
         with pytest.raises(G.GemmError):
             p.set_option(option, bad)
