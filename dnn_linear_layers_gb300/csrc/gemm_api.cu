@@ -686,8 +686,14 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const int es = in_bytes(dtype);                 // element size of A and B
     const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
     const bool b_ok = aligned16(B) && (ldb * es) % 16 == 0;
-    // the small-M kernels store C with plain stores: any pitch is fine
-    const bool c_ok = skinny || gemv || (aligned16(C) && (ldc * ob) % 16 == 0);
+    // the small-M kernels store C with plain stores, and so does the
+    // tensor-core epilogue when C breaks the TMA rule: any pitch is fine.  A
+    // TMA store also needs the right edge of C on a 16-byte boundary: at an
+    // edge inside a 16-byte granule it writes the whole granule, i.e. up to
+    // 15 bytes of each row past column N (measured on GB300).
+    const bool c_tma = aligned16(C) && (ldc * ob) % 16 == 0 && (N * ob) % 16 == 0;
+    const bool c_direct = !skinny && !gemv && !c_tma && !(conv && conv->pool);
+    const bool c_ok = skinny || gemv || c_tma || c_direct;
     const void* A_use = A; int64_t lda_use = lda;
     const void* B_use = B; int64_t ldb_use = ldb;
     void* C_use = C; int64_t ldc_use = ldc;
@@ -703,17 +709,20 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         if (rc != GEMM_OK) return rc;
         char* ws = static_cast<char*>(p->workspace);
         if (sk_bytes) sk_part = reinterpret_cast<float*>(ws + a_bytes + b_bytes + c_bytes);
+        // A and B packed in one launch
+        PackJob ja = {}, jb = {};
         if (!a_ok) {
-            e = launch_copy2d(A, lda, ws, lda_p, a_rows, a_cols, es, stream);
-            if (e != cudaSuccess) return record(p, e);
-            p->launches += 1;
+            ja = pack_job(A, lda, ws, lda_p, a_rows, a_cols, es);
             A_use = ws; lda_use = lda_p;
         }
         if (!b_ok) {
-            e = launch_copy2d(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, es, stream);
+            jb = pack_job(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, es);
+            B_use = ws + a_bytes; ldb_use = ldb_p;
+        }
+        if (!a_ok || !b_ok) {
+            e = launch_pack2(ja, jb, stream);
             if (e != cudaSuccess) return record(p, e);
             p->launches += 1;
-            B_use = ws + a_bytes; ldb_use = ldb_p;
         }
         if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
     } else if (sk_bytes) {
@@ -755,8 +764,11 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * es, kbk, TC_BN / cg)
                     : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * es, 64, TC_BK);
     if (!okb) return GEMM_ERR_CUDA;
-    if (!make_map(&tmC, out_dt, C_use, (uint64_t)N, (uint64_t)M, (uint64_t)ldc_use * ob, 128 / ob, 32))
+    if (c_direct) {
+        std::memset(&tmC, 0, sizeof(tmC));   // not used: the epilogue stores C itself
+    } else if (!make_map(&tmC, out_dt, C_use, (uint64_t)N, (uint64_t)M, (uint64_t)ldc_use * ob, 128 / ob, 32)) {
         return GEMM_ERR_CUDA;
+    }
 
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -778,6 +790,11 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     prm.l2_policy = p->l2_policy;
     prm.pdl = p->pdl;
     prm.k_snake = p->k_snake ? 1u : 0u;
+    if (c_direct) {
+        prm.c_direct = 1u;
+        prm.c_ptr = C;
+        prm.ldc = ldc;
+    }
     if (conv) {
         prm.conv = 1u;
         prm.conv_cb = (int32_t)(conv->C / TC_BK);

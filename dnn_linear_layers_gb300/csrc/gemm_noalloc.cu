@@ -123,12 +123,14 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
     const bool a_ok = K == 0 || (al16(A) && (lda * 2) % 16 == 0);
     const bool b_ok = K == 0 || (al16(B) && (ldb * 2) % 16 == 0);
-    const bool c_ok = al16(C) && (ldc * ob) % 16 == 0;
-    const int64_t lda_p = rup(K, 8), ldb_p = rup(b_cols, 8), ldc_p = rup(N, 16 / ob);
+    // C that breaks the TMA rule (base, pitch, or a right edge inside a
+    // 16-byte granule, where a TMA store would write past column N) is stored
+    // by the epilogue itself
+    const bool c_direct = !(al16(C) && (ldc * ob) % 16 == 0 && (N * ob) % 16 == 0);
+    const int64_t lda_p = rup(K, 8), ldb_p = rup(b_cols, 8);
     const int64_t a_bytes = a_ok ? 0 : rup(M * lda_p * 2, 256);
     const int64_t b_bytes = b_ok ? 0 : rup(b_rows * ldb_p * 2, 256);
-    const int64_t c_bytes = (c_ok || K == 0) ? 0 : rup(M * ldc_p * ob, 256);
-    if (a_bytes + b_bytes + c_bytes > (int64_t)(GEMM_NOALLOC_SCRATCH_BYTES - kStatusBytes))
+    if (a_bytes + b_bytes > (int64_t)(GEMM_NOALLOC_SCRATCH_BYTES - kStatusBytes))
         return GEMM_ERR_UNSUPPORTED;
 
     int dev = 0;
@@ -156,18 +158,19 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     unsigned char* ws = s->scratch + kStatusBytes;
     const void* A_use = A; int64_t lda_use = lda;
     const void* B_use = B; int64_t ldb_use = ldb;
-    void* C_use = C; int64_t ldc_use = ldc;
+    gb300::PackJob ja = {}, jb = {};
     if (!a_ok) {
-        e = gb300::launch_copy2d(A, lda, ws, lda_p, M, K, 2, stream);
-        if (e != cudaSuccess) return GEMM_ERR_CUDA;
+        ja = gb300::pack_job(A, lda, ws, lda_p, M, K, 2);
         A_use = ws; lda_use = lda_p;
     }
     if (!b_ok) {
-        e = gb300::launch_copy2d(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, 2, stream);
-        if (e != cudaSuccess) return GEMM_ERR_CUDA;
+        jb = gb300::pack_job(B, ldb, ws + a_bytes, ldb_p, b_rows, b_cols, 2);
         B_use = ws + a_bytes; ldb_use = ldb_p;
     }
-    if (!c_ok) { C_use = ws + a_bytes + b_bytes; ldc_use = ldc_p; }
+    if (!a_ok || !b_ok) {
+        e = gb300::launch_pack2(ja, jb, stream);
+        if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    }
 
     const int cg = (M <= 128) ? 1 : 2;
     const bool bf16_in = (dtype == GEMM_BF16_F32OUT || dtype == GEMM_BF16_BF16OUT);
@@ -180,7 +183,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
                                   gb300::TC_BN / cg)
                           : map2d(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * 2, 64, gb300::TC_BK);
     if (!okb) return GEMM_ERR_CUDA;
-    if (!map2d(&tmC, out_dt, C_use, (uint64_t)N, (uint64_t)M, (uint64_t)ldc_use * ob, 128 / ob, 32))
+    if (c_direct) std::memset(&tmC, 0, sizeof(tmC));   // not used: the epilogue stores C itself
+    else if (!map2d(&tmC, out_dt, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * ob, 128 / ob, 32))
         return GEMM_ERR_CUDA;
 
     gb300::TcParams prm;
@@ -202,15 +206,16 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     prm.debug = 0;
     prm.l2_policy = 0;
     prm.num_full = prm.num_m_tiles * prm.num_n_tiles;   // whole tiles only
+    if (c_direct) {
+        prm.c_direct = 1u;
+        prm.c_ptr = C;
+        prm.ldc = ldc;
+    }
     const int64_t tiles = (int64_t)prm.num_m_tiles * prm.num_n_tiles;
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t cap = (cg == 2) ? s->max_pairs[dtype] : s->max_singles[dtype];
     const int64_t units = tiles < cap ? tiles : cap;
     e = gb300::launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
-    if (C_use != C) {
-        e = gb300::launch_copy2d(C_use, ldc_use, C, ldc, M, N, ob, stream);
-        if (e != cudaSuccess) return GEMM_ERR_CUDA;
-    }
     return GEMM_OK;
 }

@@ -72,6 +72,9 @@ struct TcParams {
     uint32_t l2_policy;    // 0: A evict_last, B evict_normal; 1: A normal, B last; 2: both normal
     uint32_t pdl;          // host only: launch with programmatic stream serialisation
     uint32_t k_snake;      // 1: every other tile of a worker walks k backwards
+    uint32_t c_direct;     // 1: C breaks the TMA rule: the epilogue stores it with plain stores
+    void* c_ptr;           // c_direct: C (M x N, row pitch ldc elements, any alignment of its type)
+    int64_t ldc;
     EpiArgs ex;            // alpha / scale / beta operands of the epilogue
     // Stream-K (sk_tiles > 0): tiles [0, sk_tiles) of the raster are split into
     // equal ranges of k-atoms over workers [0, sk_workers) (worker w takes atoms
@@ -205,6 +208,25 @@ cudaError_t launch_fill_epilogue(int dtype, int64_t M, int64_t N, const void* bi
 // 16 bytes, the columns up to that boundary are zero-filled as well.
 cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
                           int64_t rows, int64_t cols, int elem_bytes, cudaStream_t stream);
+
+// Packing job: rows x row_bytes bytes from src (row pitch ld_src_bytes, any
+// alignment) into dst (16-byte aligned, pitch ld_dst_bytes a multiple of 16
+// and at least row_bytes rounded up to 16), zero-filling each row up to its
+// 16-byte boundary; chunks = 16-byte pieces per row.  A job with rows = 0 is
+// empty.
+struct PackJob {
+    const uint8_t* src;
+    int64_t ld_src_bytes;
+    uint8_t* dst;
+    int64_t ld_dst_bytes;
+    int64_t rows;
+    int64_t row_bytes;
+    int64_t chunks;
+};
+PackJob pack_job(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                 int elem_bytes);
+// Run up to two packing jobs in one launch.
+cudaError_t launch_pack2(const PackJob& j0, const PackJob& j1, cudaStream_t stream);
 
 // im2col of an NHWC tensor for an R x S convolution (zero padding `pad`,
 // stride `stride`): out[(n*OH + oh)*OW + ow][(r*S + s)*C + c], row pitch ld_out.

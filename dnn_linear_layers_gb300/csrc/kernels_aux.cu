@@ -81,6 +81,51 @@ __global__ void copy2d_vec_kernel(const T* __restrict__ src, int64_t ld_src, T* 
     }
 }
 
+// Packing of up to two operands in one launch (the GEMM's misaligned A and B):
+// each thread builds one 16-byte piece of a destination row.  Row bytes
+// [16 k, 16 k + 16) of the source start at any address; a piece whose aligned
+// 16-byte words lie inside the row is assembled from those two words by a
+// funnel shift (two 16-byte loads, one store), the row's first and last
+// pieces byte by byte, so nothing outside the row is read.  Bytes past the
+// row up to the piece boundary are written as zeros.
+__global__ void pack2_kernel(PackJob j0, PackJob j1, int64_t total0, int64_t total) {
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const bool first = t < total0;
+        const PackJob& j = first ? j0 : j1;
+        const int64_t c = first ? t : t - total0;
+        const int64_t r = c / j.chunks, k = c - r * j.chunks;
+        const uint8_t* row = j.src + r * j.ld_src_bytes;
+        const int64_t b0 = k * 16;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(row) + (uintptr_t)b0;
+        const uint32_t sh = (uint32_t)(addr & 15u);
+        uint4 out;
+        if (k >= 1 && b0 - (int64_t)sh + 32 <= j.row_bytes) {
+            const uint4* base = reinterpret_cast<const uint4*>(addr - sh);
+            const uint4 lo = __ldg(base);
+            const uint4 hi = sh ? __ldg(base + 1) : lo;
+            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            const uint32_t q = sh >> 2, bits = (sh & 3u) * 8u;
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
+                const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
+                o[i] = __funnelshift_r(a, b, bits);
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            union { uint4 u; uint8_t b[16]; } v;
+            v.u = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (b0 + e < j.row_bytes) v.b[e] = row[b0 + e];
+            out = v.u;
+        }
+        *reinterpret_cast<uint4*>(j.dst + r * j.ld_dst_bytes + b0) = out;
+    }
+}
+
 // im2col for a stride-s, zero-padded R x S convolution on NHWC input: one warp
 // per output row (n, oh, ow); the row is R*S segments of C contiguous input
 // channels, each copied in 16-byte pieces (or zero-filled outside the image).
@@ -205,6 +250,29 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
+}
+
+cudaError_t launch_pack2(const PackJob& j0, const PackJob& j1, cudaStream_t stream) {
+    const int64_t total0 = j0.rows * j0.chunks, total = total0 + j1.rows * j1.chunks;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    pack2_kernel<<<(int)blocks, threads, 0, stream>>>(j0, j1, total0, total);
+    return cudaGetLastError();
+}
+
+PackJob pack_job(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                 int elem_bytes) {
+    PackJob j;
+    j.src = static_cast<const uint8_t*>(src);
+    j.ld_src_bytes = ld_src * elem_bytes;
+    j.dst = static_cast<uint8_t*>(dst);
+    j.ld_dst_bytes = ld_dst * elem_bytes;
+    j.rows = rows;
+    j.row_bytes = cols * elem_bytes;
+    j.chunks = (j.row_bytes + 15) / 16;
+    return j;
 }
 
 cudaError_t launch_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad,

@@ -239,6 +239,11 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, __half*) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
@@ -299,7 +304,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tma_prefetch_desc(&tmA);
         if (p.conv_pool) tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmC);
+        if (!p.c_direct) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_ptr_smem), kTmemCols);
@@ -746,12 +751,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                     st_shared_v4(row_addr + ((j ^ (lane & 7u)) << 4), w0, w1, w2, w3);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int col = n0 + c * kCols;
-                    if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
-                    bulk_commit_group();
+                if (p.c_direct) {
+                    // C breaks the TMA rule (pitch or base): the warp writes its 32
+                    // staged rows itself, one row at a time, lane l the l-th 4-byte
+                    // word of the row's 128 bytes (coalesced; 16-bit halves where a
+                    // word of C is not 4-byte aligned)
+                    __syncwarp();
+                    OutT* const Cg = reinterpret_cast<OutT*>(p.c_ptr);
+                    constexpr int kPerWord = 4 / (int)sizeof(OutT);
+                    const int col = cb + (int)lane * kPerWord;
+                    for (int r = 0; r < 32 && row0 + r < p.M; ++r) {
+                        const uint32_t word = ld_shared_u32(buf + r * 128u + ((((lane >> 2) ^ (uint32_t)(r & 7)) << 4) |
+                                                                            ((lane & 3u) << 2)));
+                        OutT* dst = Cg + (int64_t)(row0 + r) * p.ldc + col;
+                        if constexpr (kPerWord == 1) {
+                            if (col < p.N) *reinterpret_cast<uint32_t*>(dst) = word;
+                        } else if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                            *reinterpret_cast<uint32_t*>(dst) = word;
+                        } else {
+                            if (col < p.N) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(word & 0xFFFFu);
+                            if (col + 1 < p.N) *reinterpret_cast<uint16_t*>(dst + 1) = (uint16_t)(word >> 16);
+                        }
+                    }
+                    __syncwarp();
+                } else {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int col = n0 + c * kCols;
+                        if (row0 < p.M && col < p.N) tma_store_2d(&tmC, buf, col, row0);
+                        bulk_commit_group();
+                    }
                 }
                 ++cstore;
             };

@@ -319,11 +319,12 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K,
  *
  * Same operation, layouts and codes as gemm_run, on the CURRENT device, with
  * the plan flags passed directly (`flags`: GEMM_B_KN or GEMM_B_NK; any other
- * bit is GEMM_ERR_INVALID_ARG) and no plan.  It allocates nothing: operands that break the 16-byte TMA rule are
- * packed into a fixed scratch array of GEMM_NOALLOC_SCRATCH_BYTES (minus 256
- * bytes for a status word) that the library holds on each device; a call
- * whose packed operands would not fit returns GEMM_ERR_UNSUPPORTED and
- * launches nothing.  Aligned operands need no scratch at any size.
+ * bit is GEMM_ERR_INVALID_ARG) and no plan.  It allocates nothing: A and B,
+ * when they break the 16-byte TMA rule, are packed into a fixed scratch array
+ * of GEMM_NOALLOC_SCRATCH_BYTES (minus 256 bytes for a status word) that the
+ * library holds on each device; a call whose packed operands would not fit
+ * returns GEMM_ERR_UNSUPPORTED and launches nothing.  C is written in place
+ * whatever its alignment, and aligned A and B need no scratch at any size.
  *
  * `dev_status` (device memory, may be NULL): when given, device-side waits
  * that run out of time OR a non-zero bit into it (the caller clears it); when

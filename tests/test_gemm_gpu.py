@@ -325,3 +325,67 @@ def test_bounded_wait_reports_timeout_and_context_survives(plans, kernel):
         assert p.status() == 0
         assert torch.all(C == float(K))
     p.close()
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("offs", [(0, 0, 1), (1, 3, 0), (5, 2, 3), (7, 7, 7)])
+def test_unaligned_operands_and_direct_c_store(plans, kernel, out, offs):
+    """A, B and C views starting 0..7 elements past a 16-byte boundary with odd
+    pitches: A and B go through the realigning pack (interior 16-byte pieces by
+    funnel shift, the first and last of each row byte by byte) in one launch,
+    and C is written by the epilogue itself (any pitch, any alignment of its
+    type); exact on integers, nothing outside C touched, beta * C read in place."""
+    oa, ob, oc = offs
+    M, N, K = 700, 523, 1037
+    A = int_bf16((M, K), 71)
+    B = int_bf16((K, N), 72)
+    C0 = int_bf16((M, N), 73, lo=-8, hi=8).float()
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    Ab = torch.zeros(M, K + 9, dtype=torch.bfloat16, device="cuda")
+    Bb = torch.zeros(K, N + 9, dtype=torch.bfloat16, device="cuda")
+    Ab[:, oa:oa + K] = A.cuda()
+    Bb[:, ob:ob + N] = B.cuda()
+    Cb = torch.full((M + 2, N + 9), float("nan"), dtype=od, device="cuda")
+    Cv = Cb[1:M + 1, oc:oc + N]
+    Cv.copy_(C0.to(od).cuda())
+    p = G.Plan(0, "kn")
+    p.set_kernel(KERNELS[kernel])
+    p.run(Ab[:, oa:oa + K], Bb[:, ob:ob + N], Cv, relu=True, beta=2.0)
+    assert p.status() == 0 and p.last_kernel == KERNELS[kernel]
+    ref, _ = oracle.gemm_ex(A, B, beta=2.0, C0=C0.double().numpy(), relu=True)
+    want = oracle.bf16_round(ref) if out == "bf16" else ref
+    assert np.array_equal(Cv.double().cpu().numpy(), want)
+    mask = torch.ones(M + 2, N + 9, dtype=torch.bool)
+    mask[1:M + 1, oc:oc + N] = False
+    assert torch.isnan(Cb.cpu()[mask].float()).all(), "write outside C"
+    p.close()
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [513, 519, 520, 523, 527])
+def test_right_edge_inside_a_16_byte_granule_is_not_overwritten(plans, kernel, out, N):
+    """C with a 16-byte aligned base and pitch whose right edge (N x element
+    size) is not a multiple of 16 bytes: the columns past N up to the next
+    16-byte boundary belong to the caller and must keep their contents (a TMA
+    store would write the whole granule, so the epilogue stores such a C
+    itself)."""
+    M, K = 300, 256
+    od = torch.float32 if out == "f32" else torch.bfloat16
+    per = 16 // (4 if out == "f32" else 2)
+    ld = (N + per - 1) // per * per + per
+    A = int_bf16((M, K), N)
+    B = int_bf16((K, N), N + 1)
+    Cb = torch.full((M + 2, ld), float("nan"), dtype=od, device="cuda")
+    Cv = Cb[1:M + 1, :N]
+    p = plans["kn"]
+    p.set_kernel(KERNELS[kernel])
+    p.run(A.cuda(), B.cuda(), Cv, relu=True)
+    assert p.status() == 0
+    ref = oracle.gemm(A, B, relu=True)
+    want = oracle.bf16_round(ref) if out == "bf16" else ref
+    assert np.array_equal(Cv.double().cpu().numpy(), want)
+    mask = torch.ones(M + 2, ld, dtype=torch.bool)
+    mask[1:M + 1, :N] = False
+    assert torch.isnan(Cb.cpu()[mask].float()).all(), "write outside C"

@@ -179,3 +179,17 @@ def test_noalloc_allocates_no_device_memory(lib):
     free1, alloc1 = torch.cuda.mem_get_info(0)[0], torch.cuda.memory_allocated(0)
     assert alloc1 == alloc0
     assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+
+
+def test_noalloc_right_edge_inside_a_16_byte_granule(lib):
+    """fp32 C with an aligned pitch and N = 523: nothing past column N is
+    written (the epilogue stores such a C itself)."""
+    M, N, K = 300, 523, 256
+    A = torch.randint(-4, 5, (M, K), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    B = torch.randint(-4, 5, (K, N), generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    Cb = torch.full((M, 528), float("nan"), device="cuda")
+    C = Cb[:, :N]
+    assert run_noalloc(lib, A.cuda(), B.cuda(), C, None, False, False) == G.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(C.double().cpu().numpy(), oracle.gemm(A, B))
+    assert torch.isnan(Cb[:, N:]).all()
