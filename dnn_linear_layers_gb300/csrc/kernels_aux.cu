@@ -88,41 +88,43 @@ __global__ void copy2d_vec_kernel(const T* __restrict__ src, int64_t ld_src, T* 
 // funnel shift (two 16-byte loads, one store), the row's first and last
 // pieces byte by byte, so nothing outside the row is read.  Bytes past the
 // row up to the piece boundary are written as zeros.
-__global__ void pack2_kernel(PackJob j0, PackJob j1, int64_t total0, int64_t total) {
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * blockDim.x) {
-        const bool first = t < total0;
+__global__ void pack2_kernel(PackJob j0, PackJob j1) {
+    // block-stride over the rows of both jobs, threads over a row's pieces
+    const int64_t rows = j0.rows + j1.rows;
+    for (int64_t rr = blockIdx.x; rr < rows; rr += gridDim.x) {
+        const bool first = rr < j0.rows;
         const PackJob& j = first ? j0 : j1;
-        const int64_t c = first ? t : t - total0;
-        const int64_t r = c / j.chunks, k = c - r * j.chunks;
+        const int64_t r = first ? rr : rr - j0.rows;
         const uint8_t* row = j.src + r * j.ld_src_bytes;
-        const int64_t b0 = k * 16;
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(row) + (uintptr_t)b0;
-        const uint32_t sh = (uint32_t)(addr & 15u);
-        uint4 out;
-        if (k >= 1 && b0 - (int64_t)sh + 32 <= j.row_bytes) {
-            const uint4* base = reinterpret_cast<const uint4*>(addr - sh);
-            const uint4 lo = __ldg(base);
-            const uint4 hi = sh ? __ldg(base + 1) : lo;
-            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            const uint32_t q = sh >> 2, bits = (sh & 3u) * 8u;
-            uint32_t o[4];
+        uint8_t* drow = j.dst + r * j.ld_dst_bytes;
+        const uint32_t row_sh = (uint32_t)(reinterpret_cast<uintptr_t>(row) & 15u);   // same for every piece
+        const uint4* abase = reinterpret_cast<const uint4*>(row - row_sh);
+        for (int64_t k = threadIdx.x; k < j.chunks; k += blockDim.x) {
+            const int64_t b0 = k * 16;
+            uint4 out;
+            if (k >= 1 && b0 - (int64_t)row_sh + 32 <= j.row_bytes) {
+                const uint4 lo = __ldg(abase + k);
+                const uint4 hi = row_sh ? __ldg(abase + k + 1) : lo;
+                const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                const uint32_t q = row_sh >> 2, bits = (row_sh & 3u) * 8u;
+                uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
-                const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
-                o[i] = __funnelshift_r(a, b, bits);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t a = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
+                    const uint32_t b = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
+                    o[i] = __funnelshift_r(a, b, bits);
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                union { uint4 u; uint8_t b[16]; } v;
+                v.u = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (b0 + e < j.row_bytes) v.b[e] = row[b0 + e];
+                out = v.u;
             }
-            out = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-            union { uint4 u; uint8_t b[16]; } v;
-            v.u = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (b0 + e < j.row_bytes) v.b[e] = row[b0 + e];
-            out = v.u;
+            *reinterpret_cast<uint4*>(drow + b0) = out;
         }
-        *reinterpret_cast<uint4*>(j.dst + r * j.ld_dst_bytes + b0) = out;
     }
 }
 
@@ -253,12 +255,12 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
 }
 
 cudaError_t launch_pack2(const PackJob& j0, const PackJob& j1, cudaStream_t stream) {
-    const int64_t total0 = j0.rows * j0.chunks, total = total0 + j1.rows * j1.chunks;
-    if (total == 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t blocks = (total + threads - 1) / threads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    pack2_kernel<<<(int)blocks, threads, 0, stream>>>(j0, j1, total0, total);
+    const int64_t rows = j0.rows + j1.rows;
+    if (rows == 0) return cudaSuccess;
+    const int64_t widest = j0.chunks > j1.chunks ? j0.chunks : j1.chunks;
+    const int threads = widest >= 256 ? 256 : (int)((widest + 31) / 32 * 32);
+    int64_t blocks = rows < 152 * 16 ? rows : 152 * 16;
+    pack2_kernel<<<(int)blocks, threads, 0, stream>>>(j0, j1);
     return cudaGetLastError();
 }
 
