@@ -329,7 +329,7 @@ int run_skinny(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int
     }
     CUtensorMap tmW, tmX;
     const bool okw = w_nk ? make_map(&tmW, in_dt, W, (uint64_t)K, (uint64_t)N, (uint64_t)ldw * es, kbk, 128)
-                          : make_map(&tmW, in_dt, W, (uint64_t)N, (uint64_t)K, (uint64_t)ldw * 2, 64, 64);
+                          : make_map(&tmW, in_dt, W, (uint64_t)N, (uint64_t)K, (uint64_t)ldw * es, kbk, kbk);
     if (!okw) return GEMM_ERR_CUDA;
     if (!make_map(&tmX, in_dt, X, (uint64_t)K, (uint64_t)M, (uint64_t)ldx * es, kbk, (uint32_t)mpad))
         return GEMM_ERR_CUDA;
@@ -406,6 +406,14 @@ int gemm_validate(unsigned flags, int64_t M, int64_t N, int64_t K, const void* A
         if (ldb < ((flags & GEMM_B_NK) ? K : N)) return GEMM_ERR_INVALID_ARG;
     }
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+    // every pointer on a boundary of its element size (bias: bf16 for the fp8
+    // and tf32 types)
+    const uintptr_t ie = (uintptr_t)in_bytes(dtype), oe = (uintptr_t)out_bytes(dtype);
+    const uintptr_t ve = (dtype_is_fp8(dtype) || dtype_is_tf32(dtype)) ? 2u : ie;
+    if (reinterpret_cast<uintptr_t>(C) % oe) return GEMM_ERR_INVALID_ARG;
+    if (bias && reinterpret_cast<uintptr_t>(bias) % ve) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % ie || reinterpret_cast<uintptr_t>(B) % ie))
+        return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
 
@@ -648,9 +656,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         return GEMM_OK;
     }
 
-    // fp8 and tf32: the paired / single-CTA kernel with both operands K-major (B stored N x K)
+    // fp8 and tf32 take every operand layout (MN-major operands through the
+    // instruction descriptor's major-ness bits), but no convolution
     const bool fp8 = dtype_is_fp8(dtype) || dtype_is_tf32(dtype);
-    if (fp8 && (!b_nk || conv || a_km)) return GEMM_ERR_UNSUPPORTED;
+    if (fp8 && conv) return GEMM_ERR_UNSUPPORTED;
     if (a_km && conv) return GEMM_ERR_UNSUPPORTED;
     // the small-M kernels take 16-bit and fp8 operands with an M x K A; the
     // CUDA-core GEMV also needs the weight stored N x K
@@ -684,8 +693,14 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const int64_t b_rows = b_nk ? N : K, b_cols = b_nk ? K : N;
     const int64_t a_rows = a_km ? K : M, a_cols = a_km ? M : K;
     const int es = in_bytes(dtype);                 // element size of A and B
-    const bool a_ok = conv || (aligned16(A) && (lda * es) % 16 == 0);
-    const bool b_ok = aligned16(B) && (ldb * es) % 16 == 0;
+    // tf32 operands stored MN-major (K x N B, K x M A) are first transposed
+    // into the workspace: the tensor cores take tf32 K-major only (MMAs with
+    // an MN-major tf32 operand gave wrong sums on GB300; 16-bit and fp8
+    // MN-major operands are read directly)
+    const bool t_a = tf32 && a_km, t_b = tf32 && !b_nk;
+    const int64_t ld_t = round_up(K, 4);            // 16-byte rows of the transposed copies
+    const bool a_ok = conv || t_a || (aligned16(A) && (lda * es) % 16 == 0);
+    const bool b_ok = t_b || (aligned16(B) && (ldb * es) % 16 == 0);
     // the small-M kernels store C with plain stores, and so does the
     // tensor-core epilogue when C breaks the TMA rule: any pitch is fine.  A
     // TMA store also needs the right edge of C on a 16-byte boundary: at an
@@ -698,17 +713,35 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     const void* B_use = B; int64_t ldb_use = ldb;
     void* C_use = C; int64_t ldc_use = ldc;
     float* sk_part = nullptr;
-    if (!a_ok || !b_ok || !c_ok) {
-        if (!p->packing) return GEMM_ERR_ALIGNMENT;
+    if (!a_ok || !b_ok || !c_ok || t_a || t_b) {
+        if ((!a_ok || !b_ok || !c_ok) && !p->packing) return GEMM_ERR_ALIGNMENT;
         const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es),
                       ldc_p = round_up(N, 16 / ob);
-        const size_t a_bytes = a_ok ? 0 : (size_t)round_up(a_rows * lda_p * es, 256);
-        const size_t b_bytes = b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * es, 256);
+        const size_t a_bytes = t_a ? (size_t)round_up(M * ld_t * 4, 256)
+                             : a_ok ? 0 : (size_t)round_up(a_rows * lda_p * es, 256);
+        const size_t b_bytes = t_b ? (size_t)round_up(N * ld_t * 4, 256)
+                             : b_ok ? 0 : (size_t)round_up(b_rows * ldb_p * es, 256);
         const size_t c_bytes = c_ok ? 0 : (size_t)round_up(M * ldc_p * ob, 256);
         rc = ensure_workspace(p, a_bytes + b_bytes + c_bytes + sk_bytes);
         if (rc != GEMM_OK) return rc;
         char* ws = static_cast<char*>(p->workspace);
         if (sk_bytes) sk_part = reinterpret_cast<float*>(ws + a_bytes + b_bytes + c_bytes);
+        // MN-major tf32 operands transposed (both in one launch); from here on
+        // the GEMM sees them K-major
+        if (t_a || t_b) {
+            TransJob ja = {}, jb = {};
+            if (t_a) {
+                ja = {static_cast<const uint32_t*>(A), lda, reinterpret_cast<uint32_t*>(ws), ld_t, K, M};
+                A_use = ws; lda_use = ld_t; a_km = false;
+            }
+            if (t_b) {
+                jb = {static_cast<const uint32_t*>(B), ldb, reinterpret_cast<uint32_t*>(ws + a_bytes), ld_t, K, N};
+                B_use = ws + a_bytes; ldb_use = ld_t; b_nk = true;
+            }
+            e = t_a ? launch_transpose2(ja, jb, stream) : launch_transpose2(jb, TransJob{}, stream);
+            if (e != cudaSuccess) return record(p, e);
+            p->launches += 1;
+        }
         // A and B packed in one launch
         PackJob ja = {}, jb = {};
         if (!a_ok) {
@@ -753,16 +786,16 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
             return GEMM_ERR_CUDA;
     } else if (conv) {
         if (!make_im2col_map(&tmA, in_dt, *conv)) return GEMM_ERR_CUDA;
-    } else if (a_km) {   // 64 rows (columns of the M x K operand) per box, two boxes per tile
-        if (!make_map(&tmA, in_dt, A_use, (uint64_t)M, (uint64_t)K, (uint64_t)lda_use * es, 64, TC_BK))
+    } else if (a_km) {   // boxes of kbk columns of the M x K operand (128 bytes) x kbk k-rows
+        if (!make_map(&tmA, in_dt, A_use, (uint64_t)M, (uint64_t)K, (uint64_t)lda_use * es, kbk, kbk))
             return GEMM_ERR_CUDA;
     } else if (!make_map(&tmA, in_dt, A_use, (uint64_t)K, (uint64_t)M, (uint64_t)lda_use * es, kbk, TC_BM)) {
         return GEMM_ERR_CUDA;
     }
-    // N x K B: one box of the CTA's columns per k-block row; K x N B (16-bit
-    // only, checked above): 64-column boxes, TC_BK k-rows each
+    // N x K B: one box of the CTA's columns per k-block row; K x N B: boxes
+    // of kbk columns (128 bytes) x kbk k-rows
     bool okb = b_nk ? make_map(&tmB, in_dt, B_use, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_use * es, kbk, TC_BN / cg)
-                    : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * es, 64, TC_BK);
+                    : make_map(&tmB, in_dt, B_use, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_use * es, kbk, kbk);
     if (!okb) return GEMM_ERR_CUDA;
     if (c_direct) {
         std::memset(&tmC, 0, sizeof(tmC));   // not used: the epilogue stores C itself
@@ -822,6 +855,10 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
         prm.sk_cnt = p->status_dev + kSkCounterOffset;
         prm.sk_part = sk_part;
         prm.num_full = (int32_t)(tiles - sk.tiles);   // the rest are whole waves
+    } else if (cg == 2 && !b_nk && dtype_is_fp8(dtype)) {
+        // a CTA's share of a half tile, 64 fp8 columns, is narrower than one
+        // 128-byte box of a K x N B: whole tiles only
+        prm.num_full = (int32_t)tiles;
     } else {
         prm.num_full = (int32_t)(tiles - tail_split(tiles, units, p->tail_split));
     }

@@ -228,6 +228,20 @@ PackJob pack_job(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int
 // Run up to two packing jobs in one launch.
 cudaError_t launch_pack2(const PackJob& j0, const PackJob& j1, cudaStream_t stream);
 
+// Transposition job of 32-bit elements: dst[c * ld_dst + r] = src[r * ld_src +
+// c] for r < rows, c < cols (pitches in elements; dst columns past rows are not
+// written).  src on a 4-byte boundary, dst on a 16-byte one with ld_dst a
+// multiple of 4.  A job with rows or cols = 0 is empty; j1 may be empty.
+struct TransJob {
+    const uint32_t* src;
+    int64_t ld_src;
+    uint32_t* dst;
+    int64_t ld_dst;
+    int64_t rows;
+    int64_t cols;
+};
+cudaError_t launch_transpose2(const TransJob& j0, const TransJob& j1, cudaStream_t stream);
+
 // im2col of an NHWC tensor for an R x S convolution (zero padding `pad`,
 // stride `stride`): out[(n*OH + oh)*OW + ow][(r*S + s)*C + c], row pitch ld_out.
 cudaError_t launch_im2col(const void* x, int64_t Nb, int64_t H, int64_t W, int64_t C, int R, int S, int pad,

@@ -8,6 +8,8 @@
 //    "pad to a multiple of 16" advice of youngju.dev "GEMM to FlashAttention"
 //    (PyTorch tips) and the tile/burst alignment remark of the devpress.csdn.net
 //    notes, section 3.6;
+//  * transpose2: tf32 operands stored MN-major, rewritten K-major into the
+//    workspace before the GEMM;
 //  * im2col: the explicit-GEMM form of a convolution, each R x S x C
 //    neighbourhood flattened into one row (CMU 15-418 notes, section 2.3), used
 //    to set up the convolution-as-GEMM workload.
@@ -125,6 +127,66 @@ __global__ void pack2_kernel(PackJob j0, PackJob j1) {
             }
             *reinterpret_cast<uint4*>(drow + b0) = out;
         }
+    }
+}
+
+// Transposition of up to two matrices of 32-bit elements in one launch (tf32
+// operands stored MN-major, which the tensor cores read K-major only):
+// blockIdx.y picks the job, blocks stride over its 64 x 64 tiles.  Thread
+// (ty, tx) of a 16 x 16 block reads 16-byte pieces (4 columns) of rows ty,
+// ty + 16, ty + 32, ty + 48 of the tile into shared memory (rows padded to 65
+// words: at most two-way bank conflicts either way), then writes 16-byte
+// pieces of the destination rows the same way.  Pieces at a ragged edge, or
+// in a source whose rows are not 16-byte aligned, go element by element.  Bits
+// are copied unchanged.
+__global__ void __launch_bounds__(256) transpose2_kernel(TransJob j0, TransJob j1) {
+    __shared__ uint32_t tile[64][65];
+    const TransJob j = blockIdx.y ? j1 : j0;
+    const int64_t tc = (j.cols + 63) / 64;
+    const int64_t tiles = ((j.rows + 63) / 64) * tc;
+    const int tx = (int)threadIdx.x & 15, ty = (int)threadIdx.x >> 4;
+    const bool src_vec = ((reinterpret_cast<uintptr_t>(j.src) & 15u) == 0) && (j.ld_src & 3) == 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t r0 = (t / tc) * 64, c0 = (t - (t / tc) * tc) * 64;
+        const int64_t c = c0 + 4 * tx;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = ty + 16 * i;
+            const int64_t r = r0 + rr;
+            uint32_t v[4] = {0u, 0u, 0u, 0u};
+            if (r < j.rows) {
+                const uint32_t* sp = j.src + r * j.ld_src + c;
+                if (src_vec && c + 4 <= j.cols) {
+                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(sp));
+                    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (c + e < j.cols) v[e] = __ldg(sp + e);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tile[rr][4 * tx + e] = v[e];
+        }
+        __syncthreads();
+        const int64_t r = r0 + 4 * tx;     // destination columns r .. r + 3
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int cc = ty + 16 * i;
+            const int64_t dc = c0 + cc;        // destination row
+            if (dc < j.cols) {
+                uint32_t* dp = j.dst + dc * j.ld_dst + r;
+                if (r + 4 <= j.rows) {
+                    *reinterpret_cast<uint4*>(dp) =
+                        make_uint4(tile[4 * tx][cc], tile[4 * tx + 1][cc], tile[4 * tx + 2][cc], tile[4 * tx + 3][cc]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (r + e < j.rows) dp[e] = tile[4 * tx + e][cc];
+                }
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -261,6 +323,20 @@ cudaError_t launch_pack2(const PackJob& j0, const PackJob& j1, cudaStream_t stre
     const int threads = widest >= 256 ? 256 : (int)((widest + 31) / 32 * 32);
     int64_t blocks = rows < 152 * 16 ? rows : 152 * 16;
     pack2_kernel<<<(int)blocks, threads, 0, stream>>>(j0, j1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose2(const TransJob& j0, const TransJob& j1, cudaStream_t stream) {
+    auto tiles = [](const TransJob& j) { return ((j.rows + 63) / 64) * ((j.cols + 63) / 64); };
+    const int64_t t0 = tiles(j0), t1 = tiles(j1);
+    const int64_t most = t0 > t1 ? t0 : t1;
+    if (most == 0) return cudaSuccess;
+    // the destination is written in 16-byte pieces: it must be aligned that way
+    if ((reinterpret_cast<uintptr_t>(j0.dst) & 15u) || (j0.ld_dst & 3) ||
+        (t1 && ((reinterpret_cast<uintptr_t>(j1.dst) & 15u) || (j1.ld_dst & 3))))
+        return cudaErrorInvalidValue;
+    const int64_t blocks = most < 152 * 8 ? most : 152 * 8;   // one wave of 8 blocks per SM
+    transpose2_kernel<<<dim3((unsigned)blocks, t1 ? 2u : 1u), 256, 0, stream>>>(j0, j1);
     return cudaGetLastError();
 }
 

@@ -165,8 +165,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             auto load_w = [&](int s, int k0) {
                 const uint32_t sw = base + s * kWStage;
                 if (p.w_mn_major) {
-                    tma_load_2d(sw, &tmW, bar_full(s), f0, k0, pol_w);
-                    tma_load_2d(sw + 8192, &tmW, bar_full(s), f0 + 64, k0, pol_w);
+                    // K x N weight: 128-byte boxes of kKb features x kKb k-rows
+                    // (two for 16-bit operands, one for fp8), side by side
+                    for (int c = 0; c < 128 / kKb; ++c)
+                        tma_load_2d(sw + c * kKb * 128, &tmW, bar_full(s), f0 + c * kKb, k0, pol_w);
                 } else {
                     tma_load_2d(sw, &tmW, bar_full(s), k0, f0, pol_w);
                 }
@@ -212,7 +214,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const uint32_t sx = base + off_x + s * x_stage;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t adesc = p.w_mn_major ? smem_desc_sw128(sw + kk * 2048, 8192, 1024)
+                    // MN-major: one MMA takes a quarter of the k-block, kKb / 4 k-rows
+                    // of 128 bytes, and the feature boxes lie kKb * 128 bytes apart
+                    const uint64_t adesc = p.w_mn_major ? smem_desc_sw128(sw + kk * kKb * 32, kKb * 128, 1024)
                                                         : smem_desc_sw128(sw + kk * 32, 16, 1024);
                     const uint64_t bdesc = smem_desc_sw128(sx + kk * 32, 16, 1024);
                     tc_mma<1, KIND>(tmem, adesc, bdesc, p.idesc, (it | kk) != 0 ? 1u : 0u);

@@ -49,7 +49,6 @@ namespace {
 constexpr int kThreads = 192;          // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 512;         // 2 accumulators x 256 fp32 columns
-constexpr int kUmmaK = 16;             // K per tcgen05.mma for 16-bit inputs
 
 template <int CG>
 struct TcCfg {
@@ -323,15 +322,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // elements per 128-byte k-block row: 64 16-bit, 128 fp8 or 32 tf32
     constexpr int kBk = KIND == 1 ? 2 * TC_BK : (KIND == 2 ? TC_BK / 2 : TC_BK);
 
-    // K x N operand: one 64-column box per 64 columns a CTA holds; N x K
-    // operand: one full-height box (a half tile uses its top rows)
+    // MN-major operands (K x N B, K x M A) arrive as boxes one 128-byte
+    // swizzle row wide (kBk columns) and kBk k-rows high, kBox bytes apart:
+    // 2 boxes per 128 columns for 16-bit types, 1 for fp8, 4 for tf32.  An
+    // N x K B is one full-height box (a half tile uses its top rows).
+    constexpr uint32_t kBox = (uint32_t)kBk * 128u;
     const bool boxes64 = p.b_mn_major != 0;
     // ring iterations (stages) of a piece, and the k-atoms of its stage stk
     auto stages_of = [](const Piece& pc) { return (pc.nkb + Cfg::kAtoms - 1) / Cfg::kAtoms; };
     auto atoms_of = [](const Piece& pc, int stk) { return min(Cfg::kAtoms, pc.nkb - stk * Cfg::kAtoms); };
     // bytes one CTA's copies bring per k-atom of a piece nw columns wide
     auto atom_bytes = [&](int nw) -> uint32_t {
-        return (uint32_t)Cfg::kAAtom + (boxes64 ? (uint32_t)(nw / CG / 64) * 8192u : (uint32_t)Cfg::kBAtom);
+        return (uint32_t)Cfg::kAAtom + (boxes64 ? (uint32_t)(nw / CG / kBk) * kBox : (uint32_t)Cfg::kBAtom);
     };
     // bytes of ring iteration i (counted over the worker's whole sequence)
     auto iter_bytes = [&](int i) -> uint32_t {
@@ -407,18 +409,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
                         }
                     } else if (p.a_mn_major) {
-                        // K x M operand: two boxes of 64 rows (M) x 64 k, 8 KB apart
-                        for (int c = 0; c < 2; ++c) {
-                            if (pair_bar) tma_load_2d_pair(dst + (uint32_t)c * 8192u, &tmA, bar, m0 + 64 * c, k0, pol_a);
-                            else tma_load_2d(dst + (uint32_t)c * 8192u, &tmA, bar, m0 + 64 * c, k0, pol_a);
+                        // K x M operand: TC_BM / kBk boxes of kBk rows (M) x kBk k
+                        for (int c = 0; c < TC_BM / kBk; ++c) {
+                            if (pair_bar) tma_load_2d_pair(dst + (uint32_t)c * kBox, &tmA, bar, m0 + kBk * c, k0, pol_a);
+                            else tma_load_2d(dst + (uint32_t)c * kBox, &tmA, bar, m0 + kBk * c, k0, pol_a);
                         }
                     } else {
                         if (pair_bar) tma_load_2d_pair(dst, &tmA, bar, k0, m0, pol_a);
                         else tma_load_2d(dst, &tmA, bar, k0, m0, pol_a);
                     }
                 };
-                const int b_boxes = boxes64 ? nw / CG / 64 : 1;
-                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * 8192u : (uint32_t)Cfg::kBAtom;
+                const int b_boxes = boxes64 ? nw / CG / kBk : 1;
+                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * kBox : (uint32_t)Cfg::kBAtom;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
@@ -439,11 +441,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             const uint32_t fb = mapa_shared(bar_full(s), 0);
                             load_a(sa, fb, k0, true);
                             if (boxes64) {
-                                for (int c = 0; c < b_boxes; ++c) {
-                                    const int bc = nb + 64 * c;
-                                    if (p.b_mn_major) tma_load_2d_pair(sb + c * 8192, &tmB, fb, bc, k0, pol_b);
-                                    else tma_load_2d_pair(sb + c * 8192, &tmB, fb, k0, bc, pol_b);
-                                }
+                                for (int c = 0; c < b_boxes; ++c)
+                                    tma_load_2d_pair(sb + c * kBox, &tmB, fb, nb + kBk * c, k0, pol_b);
                             } else {
                                 tma_load_2d_pair(sb, &tmB, fb, k0, nb, pol_b);
                             }
@@ -451,7 +450,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             load_a(sa, bar_full(s), k0, false);
                             if (p.b_mn_major) {
                                 for (int c = 0; c < b_boxes; ++c)
-                                    tma_load_2d(sb + c * 8192, &tmB, bar_full(s), nb + 64 * c, k0, pol_b);
+                                    tma_load_2d(sb + c * kBox, &tmB, bar_full(s), nb + kBk * c, k0, pol_b);
                             } else {
                                 tma_load_2d(sb, &tmB, bar_full(s), k0, nb, pol_b);
                             }
@@ -485,12 +484,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const bool rev = pc.rev;
                 // descriptors built once; per stage, atom and MMA only the start
                 // address field (bits 0-13, address >> 4) moves
-                const uint64_t a0 = p.a_mn_major ? smem_desc_sw128(base + Cfg::kOffA, 8192, 1024)
+                // (MN-major: leading byte offset = the distance between boxes)
+                const uint64_t a0 = p.a_mn_major ? smem_desc_sw128(base + Cfg::kOffA, kBox, 1024)
                                                  : smem_desc_sw128(base + Cfg::kOffA, 16, 1024);
-                const uint64_t b0 = p.b_mn_major ? smem_desc_sw128(base + Cfg::kOffB, 8192, 1024)
+                const uint64_t b0 = p.b_mn_major ? smem_desc_sw128(base + Cfg::kOffB, kBox, 1024)
                                                  : smem_desc_sw128(base + Cfg::kOffB, 16, 1024);
-                const uint32_t a_kstep = p.a_mn_major ? (kUmmaK * 128) >> 4 : 32 >> 4;
-                const uint32_t b_kstep = p.b_mn_major ? (kUmmaK * 128) >> 4 : 32 >> 4;
+                // one MMA takes a quarter of the k-atom: 32 bytes along a K-major
+                // row, or kBk / 4 k-rows of 128 bytes of an MN-major box
+                const uint32_t a_kstep = p.a_mn_major ? (uint32_t)(kBk * 32) >> 4 : 32u >> 4;
+                const uint32_t b_kstep = p.b_mn_major ? (uint32_t)(kBk * 32) >> 4 : 32u >> 4;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
@@ -501,8 +503,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const int na = atoms_of(pc, rev ? nst - 1 - st : st);
                     const uint64_t as = a0 + (uint64_t)((s * Cfg::kAStage) >> 4);
                     const uint64_t bs = b0 + (uint64_t)((s * Cfg::kBStage) >> 4);
-                    // four MMAs per k-atom, 32 bytes of every operand row each (K-major:
-                    // 32 bytes along the row; MN-major: 16 k-rows of 128 bytes)
+                    // four MMAs per k-atom
                     for (int j = 0; j < na; ++j)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)

@@ -61,14 +61,15 @@ typedef enum {
 /* Input type of A, B (and bias, scale) and output type of C.  The fp8 types
  * (OCP e4m3 / e5m2 bytes, both operands in one format; CMU 15-418 notes,
  * section 2.7: fewer bytes per operand, fp32 accumulation) take bf16 bias and
- * scale vectors, need B stored N x K (plan flag GEMM_B_NK: both operands
- * K-major) and run on the small-M kernel for M <= 128, on the large-M
- * kernels otherwise; per-tensor scale factors go in gemm_run_ex's alpha.  The
+ * scale vectors, B stored either way and A either way (GEMM_A_KM), and run on
+ * the small-M kernel for M <= 128 (A stored M x K), on the large-M kernels
+ * otherwise; per-tensor scale factors go in gemm_run_ex's alpha.  The
  * tf32 types take fp32 A and B in memory, which
  * the tensor cores multiply at tf32 precision (8-bit exponent, 10-bit
  * mantissa; CMU 15-418 notes, section 2.7), with fp32 accumulation; like fp8
- * they take bf16 bias and scale vectors, need GEMM_B_NK and run on the
- * large-M kernels. */
+ * they take bf16 bias and scale vectors and every operand layout, and run on
+ * the large-M kernels.  Neither type is taken by the convolution entry points
+ * or by gemm_run_noalloc (GEMM_ERR_UNSUPPORTED). */
 typedef enum {
     GEMM_BF16_F32OUT = 0,
     GEMM_BF16_BF16OUT = 1,
@@ -92,8 +93,7 @@ typedef enum {
 #define GEMM_B_CONST 2u
 /* A is stored K x M (the transpose of the M x K operand, BLAS "transa"):
  * A(i, k) = A[k * lda + i], lda >= M.  Runs on the tensor-core kernels (also for
- * M <= 128); 16-bit inputs only (fp8 operands must be K-major: refused with
- * GEMM_ERR_UNSUPPORTED); not taken by gemm_run_noalloc. */
+ * M <= 128), for every input type; not taken by gemm_run_noalloc. */
 #define GEMM_A_KM 8u
 
 /* Kernel selection (gemm_plan_set_kernel / gemm_plan_last_kernel). */
@@ -144,7 +144,12 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
 /* C = epilogue(A.B) (see above).  M, N, K >= 0; M == 0 or N == 0 is a no-op;
  * K == 0 writes epilogue(0).  `bias` may be NULL unless the epilogue adds it.
  * `epilogue` is a gemm_epilogue_t, `dtype` a gemm_dtype_t, `stream` a
- * cudaStream_t.  Returns after enqueueing the work. */
+ * cudaStream_t.  Every pointer must lie on a boundary of its element size
+ * (else GEMM_ERR_INVALID_ARG); pitches and 16-byte alignment are free (the
+ * plan packs what TMA cannot read).  tf32 operands stored MN-major (A with
+ * GEMM_A_KM, B without GEMM_B_NK) are transposed into the plan's workspace
+ * before the product, whatever gemm_plan_set_packing says.  Returns after
+ * enqueueing the work. */
 int gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
              const void* A, int64_t lda, const void* B, int64_t ldb, const void* bias,
              void* C, int64_t ldc, int epilogue, int dtype, void* stream);

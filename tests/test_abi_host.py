@@ -81,6 +81,20 @@ def test_validate_rejects_bad_arguments(lib):
     assert val(M=2 ** 31, lda=64) == G.ERR_UNSUPPORTED
 
 
+def test_validate_rejects_pointers_off_their_element_boundary(lib):
+    odd, two = ctypes.c_void_p(0x1001), ctypes.c_void_p(0x1002)
+    assert val(A=odd) == G.ERR_INVALID_ARG                       # bf16 A one byte off
+    assert val(Bp=odd) == G.ERR_INVALID_ARG
+    assert val(A=two, Bp=two) == G.OK                            # 2-byte boundary: fine for bf16
+    assert val(C=two, dtype=G.BF16_F32OUT) == G.ERR_INVALID_ARG  # fp32 C two bytes off
+    assert val(C=two, dtype=G.BF16_BF16OUT) == G.OK
+    assert val(epi=G.EPI_BIAS, bias=odd) == G.ERR_INVALID_ARG
+    assert val(A=two, dtype=G.TF32_F32OUT) == G.ERR_INVALID_ARG  # fp32 operands: 4-byte boundary
+    assert val(A=odd, Bp=odd, dtype=G.E4M3_F32OUT) == G.OK        # fp8: any byte
+    assert val(epi=G.EPI_BIAS, bias=two, dtype=G.E4M3_F32OUT) == G.OK   # bf16 bias of an fp8 product
+    assert val(K=0, A=odd, Bp=odd) == G.OK                       # A and B not read
+
+
 def test_validate_size_zero_is_a_noop(lib):
     assert val(M=0, A=None, Bp=None, C=None) == G.OK
     assert val(N=0, A=None, Bp=None, C=None) == G.OK

@@ -89,17 +89,15 @@ def test_fp8_misaligned_pitch_is_packed():
     assert np.array_equal(C.double().cpu().numpy(), oracle.gemm(A, B, b_nk=True))
 
 
-def test_fp8_unsupported_combinations_are_refused():
-    A = int_fp8((256, 128), 4, "e4m3").cuda()
-    C = torch.empty(256, 256, device="cuda")
-    with G.Plan(0, "kn") as p:                  # K x N B: not K-major
+def test_fp8_convolution_is_refused():
+    """fp8 operands run in every GEMM layout (see the layout tests), but the
+    convolution entry points take 16-bit inputs only."""
+    x = torch.zeros(1, 8, 8, 64, device="cuda").to(torch.float8_e4m3fn)
+    w = torch.zeros(64, 3, 3, 64, device="cuda").to(torch.float8_e4m3fn)
+    y = torch.zeros(64, 64, device="cuda")
+    with G.Plan(0, "nk") as p:
         with pytest.raises(G.GemmError) as e:
-            p.run(A, int_fp8((128, 256), 5, "e4m3").cuda(), C)
-        assert e.value.code == G.ERR_UNSUPPORTED
-    with G.Plan(0, "kn") as p:                  # nor on the small-M kernel
-        p.set_kernel(G.KERNEL_SKINNY)
-        with pytest.raises(G.GemmError) as e:
-            p.run(A[:16], int_fp8((128, 256), 6, "e4m3").cuda(), C[:16])
+            p.conv2d(x, w, y, pad=1)
         assert e.value.code == G.ERR_UNSUPPORTED
 
 

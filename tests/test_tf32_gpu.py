@@ -126,20 +126,24 @@ def test_tf32_k0_and_large(plan):
 
 
 def test_tf32_refusals():
+    """tf32 runs on the tensor-core kernels only (every operand layout: see the
+    layout tests); the small-M kernel and the convolution refuse it."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     A = torch.zeros(64, 32, device="cuda")
     C = torch.zeros(64, 16, device="cuda")
-    with G.Plan(0, "kn") as p:                                  # K x N B: not taken for tf32
-        with pytest.raises(G.GemmError):
-            p.run(A, torch.zeros(32, 16, device="cuda"), C)
-    with G.Plan(0, "nk", a_layout="km") as p:                   # K x M A: not taken for tf32
-        with pytest.raises(G.GemmError):
-            p.run(torch.zeros(32, 64, device="cuda"), torch.zeros(16, 32, device="cuda"), C)
     with G.Plan(0, "nk") as p:
         p.set_kernel(G.KERNEL_SKINNY)
-        with pytest.raises(G.GemmError):
+        with pytest.raises(G.GemmError) as e:
             p.run(A, torch.zeros(16, 32, device="cuda"), C)
+        assert e.value.code == G.ERR_UNSUPPORTED
+        p.set_kernel(G.KERNEL_AUTO)
+        x = torch.zeros(1, 8, 8, 64, device="cuda")
+        w = torch.zeros(64, 3, 3, 64, device="cuda")
+        y = torch.zeros(64, 64, device="cuda")
+        with pytest.raises(G.GemmError) as e:
+            p.conv2d(x, w, y, pad=1)
+        assert e.value.code == G.ERR_UNSUPPORTED
 
 
 def test_tf32_extended_epilogue_integer_exact(plan):

@@ -101,10 +101,6 @@ def test_transposed_a_refusals(plans):
     with pytest.raises(G.GemmError):
         p.run(A, B, C)
     p.set_kernel(G.KERNEL_AUTO)
-    A8 = torch.zeros(64, 32, device="cuda").to(torch.float8_e4m3fn)
-    B8 = torch.zeros(16, 64, device="cuda").to(torch.float8_e4m3fn)
-    with pytest.raises(G.GemmError):
-        p.run(A8, B8, C)
 
 
 @pytest.mark.parametrize("kernel", [G.KERNEL_TC_SINGLE, G.KERNEL_TC_PAIR])
