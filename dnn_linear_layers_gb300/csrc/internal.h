@@ -64,6 +64,8 @@ struct TcParams {
     uint32_t idesc;        // tcgen05 instruction descriptor
     uint32_t b_mn_major;   // 1: B is K x N (N contiguous); 0: B is N x K
     uint32_t a_mn_major;   // 1: A is K x M (M contiguous); 0: A is M x K
+    uint32_t a_chunks;     // 1: MN-major A tile in one copy ([M/64][K][64] map)
+    uint32_t b_chunks;     // 1: MN-major B tile in one copy ([N/64][K][64] map)
     const void* bias;      // N elements of the input type, or null
     uint32_t bias_vec16;   // 1: bias is 16-byte aligned (vector loads allowed)
     int* status;           // device status word (StatusBits)

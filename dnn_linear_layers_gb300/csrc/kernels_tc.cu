@@ -333,7 +333,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     auto atoms_of = [](const Piece& pc, int stk) { return min(Cfg::kAtoms, pc.nkb - stk * Cfg::kAtoms); };
     // bytes one CTA's copies bring per k-atom of a piece nw columns wide
     auto atom_bytes = [&](int nw) -> uint32_t {
-        return (uint32_t)Cfg::kAAtom + (boxes64 ? (uint32_t)(nw / CG / kBk) * kBox : (uint32_t)Cfg::kBAtom);
+        return (uint32_t)Cfg::kAAtom +
+               (boxes64 && !p.b_chunks ? (uint32_t)(nw / CG / kBk) * kBox : (uint32_t)Cfg::kBAtom);
     };
     // bytes of ring iteration i (counted over the worker's whole sequence)
     auto iter_bytes = [&](int i) -> uint32_t {
@@ -408,6 +409,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             if (pair_bar) tma_load_im2col_pair(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
                             else tma_load_im2col(dst, &tmA, bar, c0, px_w, px_h, px_n, off_w, off_h, pol_a);
                         }
+                    } else if (p.a_chunks) {
+                        // K x M operand, M a multiple of 64: the tile's two 64-column
+                        // chunks in one copy
+                        if (pair_bar) tma_load_3d_pair(dst, &tmA, bar, 0, k0, m0 / 64, pol_a);
+                        else tma_load_3d(dst, &tmA, bar, 0, k0, m0 / 64, pol_a);
                     } else if (p.a_mn_major) {
                         // K x M operand: TC_BM / kBk boxes of kBk rows (M) x kBk k
                         for (int c = 0; c < TC_BM / kBk; ++c) {
@@ -419,8 +425,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         else tma_load_2d(dst, &tmA, bar, k0, m0, pol_a);
                     }
                 };
+                // (a chunked K x N B always copies all of a CTA's chunks, also
+                // for a half tile, whose MMAs read only the first)
                 const int b_boxes = boxes64 ? nw / CG / kBk : 1;
-                const uint32_t b_bytes = boxes64 ? (uint32_t)b_boxes * kBox : (uint32_t)Cfg::kBAtom;
+                const uint32_t b_bytes = boxes64 && !p.b_chunks ? (uint32_t)b_boxes * kBox : (uint32_t)Cfg::kBAtom;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = (int)(it % Cfg::kStages);
                     const uint32_t ph = (it / Cfg::kStages) & 1u;
@@ -440,7 +448,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         if constexpr (CG == 2) {
                             const uint32_t fb = mapa_shared(bar_full(s), 0);
                             load_a(sa, fb, k0, true);
-                            if (boxes64) {
+                            if (p.b_chunks) {
+                                tma_load_3d_pair(sb, &tmB, fb, 0, k0, nb / 64, pol_b);
+                            } else if (boxes64) {
                                 for (int c = 0; c < b_boxes; ++c)
                                     tma_load_2d_pair(sb + c * kBox, &tmB, fb, nb + kBk * c, k0, pol_b);
                             } else {
@@ -448,7 +458,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             }
                         } else {
                             load_a(sa, bar_full(s), k0, false);
-                            if (p.b_mn_major) {
+                            if (p.b_chunks) {
+                                tma_load_3d(sb, &tmB, bar_full(s), 0, k0, nb / 64, pol_b);
+                            } else if (p.b_mn_major) {
                                 for (int c = 0; c < b_boxes; ++c)
                                     tma_load_2d(sb + c * kBox, &tmB, bar_full(s), nb + kBk * c, k0, pol_b);
                             } else {

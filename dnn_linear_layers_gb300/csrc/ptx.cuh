@@ -157,6 +157,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 3-D tiled load whose completion is counted on a barrier of either CTA of
+// the pair; coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar,
+                                                 int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // Implicit-GEMM (im2col) loads from an NHWC tensor map made by
 // cuTensorMapEncodeIm2col: starting at pixel (n, h, w) of the map's bounding
 // box, `pixelsPerColumn` consecutive pixels (w fastest, then h, then n) are
