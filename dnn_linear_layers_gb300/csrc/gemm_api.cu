@@ -33,7 +33,7 @@ struct gemm_plan {
     uint64_t timeout_ns = 1000000000ull;
     int packing = 1;
     unsigned debug = 0;
-    int group_m = 8;
+    int group_m = 0;                // 0: auto_group_m
     unsigned l2_policy = 0;
     unsigned pdl = 1;             // programmatic dependent launch of the GEMM kernels
     int debug_log = 0;            // GEMM_OPT_LOG: one line per launch on stderr
@@ -530,7 +530,7 @@ int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
     const bool b01 = v == 0 || v == 1;
     switch (option) {
         case GEMM_OPT_GROUP_M:
-            if (v < 1 || v > 1024) return GEMM_ERR_INVALID_ARG;
+            if (v < 0 || v > 1024) return GEMM_ERR_INVALID_ARG;
             p->group_m = (int)v; return GEMM_OK;
         case GEMM_OPT_TAIL_SPLIT:
             if (!b01) return GEMM_ERR_INVALID_ARG;
@@ -837,7 +837,6 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     prm.num_m_tiles = (int32_t)num_m_tiles;
     prm.num_n_tiles = (int32_t)num_n_tiles;
     prm.num_k_blocks = (int32_t)num_kb;
-    prm.group_m = p->group_m;
     prm.epi = epi;
     prm.ex = ex;
     prm.idesc = make_idesc(dtype, !b_nk, TC_BM * cg, TC_BN, a_km);
@@ -877,6 +876,7 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
     // workers: one per co-resident CTA (pair), fewer for small problems
     int64_t units = tiles < cap ? tiles : cap;
+    prm.group_m = p->group_m ? p->group_m : auto_group_m(num_n_tiles, cap);
     if (sk.tiles) {
         if (sk.workers > units) units = sk.workers;
         prm.sk_tiles = (int32_t)sk.tiles;

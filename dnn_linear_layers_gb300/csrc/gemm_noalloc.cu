@@ -193,7 +193,6 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     prm.num_m_tiles = (int32_t)((M + gb300::TC_BM * cg - 1) / (gb300::TC_BM * cg));
     prm.num_n_tiles = (int32_t)((N + gb300::TC_BN - 1) / gb300::TC_BN);
     prm.num_k_blocks = (int32_t)((K + gb300::TC_BK - 1) / gb300::TC_BK);
-    prm.group_m = 16;
     prm.epi = epi;
     const uint32_t ab = bf16_in ? 1u : 0u;
     prm.idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((b_nk ? 0u : 1u) << 16) |
@@ -215,6 +214,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     if (tiles > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
     const int64_t cap = (cg == 2) ? s->max_pairs[dtype] : s->max_singles[dtype];
     const int64_t units = tiles < cap ? tiles : cap;
+    prm.group_m = gb300::auto_group_m(prm.num_n_tiles, cap);
     e = gb300::launch_tc_gemm(cg, dtype, tmA, tmB, tmC, prm, (int)(units * cg), stream);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_OK;

@@ -282,7 +282,9 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 /* Tuning options of a plan, for benchmark sweeps and tests; the defaults are
  * the measured best and a caller never needs to change them.  No option
  * changes a result, only how the work is scheduled. */
-#define GEMM_OPT_GROUP_M 1         /* tile-rows per rasterisation group, 1..1024 (default 8) */
+/* tile-rows per rasterisation group, 1..1024, or 0 (default): 1 when one wave
+ * of tiles spans three or more whole tile-rows, else 8 */
+#define GEMM_OPT_GROUP_M 1
 #define GEMM_OPT_TAIL_SPLIT 2      /* 0/1: run the last partial wave as half tiles (default 1) */
 #define GEMM_OPT_K_SNAKE 3         /* 0/1: every other tile of a worker walks k backwards (default 1) */
 #define GEMM_OPT_PDL 4             /* 0/1: programmatic dependent launch (default 1) */

@@ -117,7 +117,8 @@ def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
         compare(case, C, C_ref, S)
 
 
-@pytest.mark.parametrize("option,value", [(G.OPT_GROUP_M, 1), (G.OPT_GROUP_M, 16), (G.OPT_TAIL_SPLIT, 0),
+@pytest.mark.parametrize("option,value", [(G.OPT_GROUP_M, 1), (G.OPT_GROUP_M, 8), (G.OPT_GROUP_M, 16),
+                                          (G.OPT_TAIL_SPLIT, 0),
                                           (G.OPT_K_SNAKE, 0), (G.OPT_PDL, 0), (G.OPT_L2_POLICY, 1),
                                           (G.OPT_L2_POLICY, 2), (G.OPT_SKINNY_SPLITS, 1),
                                           (G.OPT_SKINNY_STAGES, 2), (G.OPT_GEMV_MAX_M, 4), (G.OPT_STREAM_K, 0),
@@ -142,7 +143,7 @@ def test_scheduling_options_change_no_result(plans, option, value, shape):
 
 def test_option_ranges_are_checked(plans):
     p = G.Plan(0)
-    for option, bad in [(G.OPT_GROUP_M, 0), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
+    for option, bad in [(G.OPT_GROUP_M, -1), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
                         (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9),
                         (G.OPT_GEMV_MAX_M, 5), (G.OPT_STREAM_K, -1), (G.OPT_STREAM_K, 5000), (0, 0), (8, 0),
                         (99, 0)]:
