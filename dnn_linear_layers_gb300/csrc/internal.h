@@ -215,10 +215,11 @@ cudaError_t launch_copy2d(const void* src, int64_t ld_src, void* dst, int64_t ld
 // run by `workers` co-resident CTAs or CTA pairs: when one wave of tiles spans
 // three or more whole tile-rows, row-major order (1) measured best (4096^3 3.3%,
 // 6144^3 4.4%, 8192 x 4096 x 4096 5% faster than groups of 8); when it spans
-// fewer, groups of 8 tile-rows keep the panels of a wave in L2 (8192^3 5%,
-// 8192 x 4096 x 12288 8% faster than 1).
+// fewer, groups of 16 tile-rows keep the panels of a wave in L2 (against 1:
+// 8192^3 8%, 8192 x 4096 x 12288 10%; against 8: 1-3%, e.g. 8192 x 4096 x
+// 14336 2.8%, e4m3 8192^3 2.2%; 24 and 32 were slower again).
 inline int auto_group_m(int64_t num_n_tiles, int64_t workers) {
-    return num_n_tiles * 3 <= workers ? 1 : 8;
+    return num_n_tiles * 3 <= workers ? 1 : 16;
 }
 
 // Packing job: rows x row_bytes bytes from src (row pitch ld_src_bytes, any

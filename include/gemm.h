@@ -283,7 +283,7 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
  * the measured best and a caller never needs to change them.  No option
  * changes a result, only how the work is scheduled. */
 /* tile-rows per rasterisation group, 1..1024, or 0 (default): 1 when one wave
- * of tiles spans three or more whole tile-rows, else 8 */
+ * of tiles spans three or more whole tile-rows, else 16 */
 #define GEMM_OPT_GROUP_M 1
 #define GEMM_OPT_TAIL_SPLIT 2      /* 0/1: run the last partial wave as half tiles (default 1) */
 #define GEMM_OPT_K_SNAKE 3         /* 0/1: every other tile of a worker walks k backwards (default 1) */
