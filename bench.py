@@ -78,6 +78,7 @@ WORKLOADS = {
     "linear_m1_4096x4096": (1, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m2_4096x14336": (2, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m4_4096x14336": (4, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
+    "linear_m8_4096x14336": (8, 14336, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m4_4096x4096": (4, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m16_4096x4096": (16, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
     "linear_m128_4096x4096": (128, 4096, 4096, "nk", (True, False), "bf16", 1.0, 4096 ** -0.5),
@@ -303,7 +304,7 @@ class Workload:
                            a_layout="km" if "_transa_" in name else "mk")
         if args.kernel != "auto":
             self.plan.set_kernel({"pair": G.KERNEL_TC_PAIR, "single": G.KERNEL_TC_SINGLE, "skinny": G.KERNEL_SKINNY,
-                                  "gemv": G.KERNEL_GEMV}[args.kernel])
+                                  "gemv": G.KERNEL_GEMV, "warp_mma": G.KERNEL_WARP_MMA}[args.kernel])
         for kv in args.opt or []:          # scheduling options (sweeps): NAME=VALUE, NAME as in GEMM_OPT_NAME
             key, val = kv.split("=")
             self.plan.set_option(getattr(G, "OPT_" + key.upper()), int(val))
@@ -430,7 +431,8 @@ class Workload:
         if self.attn:
             return "attention"
         return {G.KERNEL_TC_PAIR: "tc_pair", G.KERNEL_TC_SINGLE: "tc_single", G.KERNEL_SKINNY: "skinny",
-                G.KERNEL_GEMV: "gemv"}.get(self.plan.last_kernel, str(self.plan.last_kernel))
+                G.KERNEL_GEMV: "gemv", G.KERNEL_WARP_MMA: "warp_mma"}.get(self.plan.last_kernel,
+                                                                          str(self.plan.last_kernel))
 
     def close(self):
         self.plan.close()
@@ -724,7 +726,7 @@ def main():
                     help="skip the decode-layer lines appended to the default workload's result")
     ap.add_argument("--opt", action="append", metavar="NAME=VALUE",
                     help="set a plan scheduling option (sweeps), e.g. stream_k=0 or group_m=16")
-    ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny", "gemv"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "pair", "single", "skinny", "gemv", "warp_mma"], default="auto",
                     help="force a kernel (sweeps); the default lets the library choose")
     args = ap.parse_args()
     if args.warmup < 3:

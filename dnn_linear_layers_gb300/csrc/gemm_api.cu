@@ -51,6 +51,12 @@ struct gemm_plan {
     // tensor-core small-M kernel; M = 4 0.55 against 0.79 (the CUDA cores run
     // out of issue slots for 4 tokens per weight element), so only M = 1.
     int gemv_max_m = 1;
+    // largest M for the warp-MMA kernel (16-bit, N x K weight): from 9 tokens
+    // its two MMAs per k-step run into the warp-level MMA rate (4096 -> 14336:
+    // M = 4 19.2 us against 22.3 on the tensor-core small-M kernel, M = 16 31.3
+    // against 22.7)
+    int warp_mma_max_m = 8;
+    int gemv_mma_blocks[2][4][4] = {};   // co-resident warp-MMA CTAs per SM: [groups - 1][log2 ks][dtype]
     int gemv_blocks[3][kNumDtypes] = {};   // co-resident GEMV CTAs per SM, by tokens held (1, 2, 4)
     int smem_per_sm = 0;          // shared memory of one SM (bytes)
     int smem_reserved = 0;        // shared memory the system reserves per CTA (bytes)
@@ -405,6 +411,45 @@ int run_gemv(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int64
     return GEMM_OK;
 }
 
+// Warp-MMA small-M kernel.  k-slices per row group: the fewest (1, 2, 4, 8)
+// that give every warp resident on the GPU a (row group, slice) unit, so the
+// whole grid streams at once; each slice keeps at least 256 k.
+int run_gemv_mma(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, int64_t ldx, const void* W,
+                 int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, const EpiArgs& ex, int dtype,
+                 cudaStream_t stream) {
+    const int nh = gemv_mma_groups((int)M);
+    if (nh == 0 || dtype >= 4) return GEMM_ERR_UNSUPPORTED;
+    const int64_t groups = (N + 15) / 16;
+    const int warps = kGemvThreads / 32;
+    int j = 0;
+    for (; j < 3; ++j) {
+        const int64_t resident = (int64_t)p->sm_count * p->gemv_mma_blocks[nh - 1][j][dtype] * warps;
+        if (groups * (1 << j) >= resident || K < 256 * (2 << j)) break;
+    }
+    const int ks = 1 << j;
+    const int bps = p->gemv_mma_blocks[nh - 1][j][dtype];
+    if (bps < 1) return GEMM_ERR_UNSUPPORTED;
+    int64_t grid = (int64_t)p->sm_count * bps;
+    const int64_t need = (groups + warps / ks - 1) / (warps / ks);
+    if (grid > need) grid = need;
+    GemvParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.M = (int32_t)M; gp.N = (int32_t)N; gp.K = (int32_t)K;
+    gp.X = X; gp.ldx = ldx; gp.W = W; gp.ldw = ldw;
+    gp.bias = bias; gp.Y = Y; gp.ldy = ldy;
+    gp.epi = epi; gp.ex = ex;
+    gp.pdl = p->pdl;
+    gp.w_prefetch = (p->pdl && (p->flags & GEMM_B_CONST)) ? 1u : 0u;
+    if (p->debug_log)
+        std::fprintf(stderr, "[gemm] warp-mma M=%lld N=%lld K=%lld groups=%lld ks=%d grid=%lld prefetch=%u pdl=%u\n",
+                     (long long)M, (long long)N, (long long)K, (long long)groups, ks, (long long)grid, gp.w_prefetch,
+                     gp.pdl);
+    cudaError_t e = launch_gemv_mma(dtype, ks, gp, (int)grid, stream);
+    if (e != cudaSuccess) return record(p, e);
+    p->launches += 1;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -475,6 +520,13 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
             e = gemv_prepare(1 << i, dt, &p->gemv_blocks[i][dt]);
             if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
         }
+        if (dt < 4) {                              // 16-bit operand types
+            for (int nh = 1; nh <= 2; ++nh)
+                for (int j = 0; j < 4; ++j) {
+                    e = gemv_mma_prepare(nh, 1 << j, dt, &p->gemv_mma_blocks[nh - 1][j][dt]);
+                    if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+                }
+        }
     }
     p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
     p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
@@ -497,7 +549,7 @@ int gemm_plan_destroy(gemm_plan_t p) {
 }
 
 int gemm_plan_set_kernel(gemm_plan_t p, int kernel) {
-    if (!p || kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_GEMV) return GEMM_ERR_INVALID_ARG;
+    if (!p || kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_WARP_MMA) return GEMM_ERR_INVALID_ARG;
     p->forced_kernel = kernel;
     return GEMM_OK;
 }
@@ -556,6 +608,9 @@ int gemm_plan_set_option(gemm_plan_t p, int option, int64_t v) {
         case GEMM_OPT_GEMV_MAX_M:
             if (v < 0 || v > kGemvMaxM) return GEMM_ERR_INVALID_ARG;
             p->gemv_max_m = (int)v; return GEMM_OK;
+        case GEMM_OPT_WARP_MMA_MAX_M:
+            if (v < 0 || v > kWarpMmaMaxM) return GEMM_ERR_INVALID_ARG;
+            p->warp_mma_max_m = (int)v; return GEMM_OK;
         case GEMM_OPT_STREAM_K:
             if (v < 0 || v > 4096) return GEMM_ERR_INVALID_ARG;
             p->sk_min_atoms = (int)v; return GEMM_OK;
@@ -575,6 +630,7 @@ int gemm_plan_get_option(gemm_plan_t p, int option, int64_t* v) {
         case GEMM_OPT_SKINNY_STAGES: *v = p->skinny_stages; return GEMM_OK;
         case GEMM_OPT_LOG: *v = p->debug_log; return GEMM_OK;
         case GEMM_OPT_GEMV_MAX_M: *v = p->gemv_max_m; return GEMM_OK;
+        case GEMM_OPT_WARP_MMA_MAX_M: *v = p->warp_mma_max_m; return GEMM_OK;
         case GEMM_OPT_STREAM_K: *v = p->sk_min_atoms; return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
@@ -683,16 +739,21 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     // CUDA-core GEMV also needs the weight stored N x K
     const bool tf32 = dtype_is_tf32(dtype);
     const bool small_ok = !conv && !tf32 && !a_km;
+    // the warp-MMA kernel: 16-bit operands, an N x K weight, M <= 16
+    const bool mma_ok = small_ok && b_nk && !fp8;
     int kernel = p->forced_kernel;
     if (kernel == GEMM_KERNEL_AUTO)
         kernel = (small_ok && b_nk && M <= p->gemv_max_m) ? GEMM_KERNEL_GEMV
+               : (mma_ok && M <= p->warp_mma_max_m) ? GEMM_KERNEL_WARP_MMA
                : (small_ok && M <= 128) ? GEMM_KERNEL_SKINNY : GEMM_KERNEL_TC_PAIR;
     if (kernel == GEMM_KERNEL_SKINNY && (M > 128 || !small_ok)) return GEMM_ERR_UNSUPPORTED;
     if (kernel == GEMM_KERNEL_GEMV && (M > kGemvMaxM || !small_ok || !b_nk)) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_WARP_MMA && (M > kWarpMmaMaxM || !mma_ok)) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TC_PAIR && kernel != GEMM_KERNEL_TC_SINGLE && kernel != GEMM_KERNEL_SKINNY &&
-        kernel != GEMM_KERNEL_GEMV)
+        kernel != GEMM_KERNEL_GEMV && kernel != GEMM_KERNEL_WARP_MMA)
         return GEMM_ERR_UNSUPPORTED;
-    const bool gemv = kernel == GEMM_KERNEL_GEMV;
+    // both weight-streaming kernels on the CUDA-core path store C with plain stores
+    const bool gemv = kernel == GEMM_KERNEL_GEMV || kernel == GEMM_KERNEL_WARP_MMA;
     const bool skinny = kernel == GEMM_KERNEL_SKINNY;
     const int cg = (kernel == GEMM_KERNEL_TC_PAIR) ? 2 : 1;
     const int kbk = 128 / in_bytes(dtype);          // elements per 128-byte k-atom row
@@ -783,7 +844,9 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     }
 
     if (gemv) {
-        rc = run_gemv(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, stream);
+        rc = kernel == GEMM_KERNEL_WARP_MMA
+                 ? run_gemv_mma(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, stream)
+                 : run_gemv(p, M, N, K, A_use, lda_use, B_use, ldb_use, bias, C, ldc, epi, ex, dtype, stream);
         if (rc != GEMM_OK) return rc;
         p->last_kernel = kernel;
         p->last_stream = stream; p->have_stream = true;

@@ -180,6 +180,13 @@ constexpr int kGemvMaxM = 4;
 int gemv_tokens_held(int M);
 cudaError_t gemv_prepare(int M, int dtype, int* blocks_per_sm);
 cudaError_t launch_gemv(int dtype, const GemvParams& p, int grid, cudaStream_t stream);
+// Warp-MMA small-M kernel (16-bit operands, 2 <= M <= 16, W stored N x K):
+// groups of 8 tokens held (1 or 2; 0 if M > 16); ks = warps of a CTA
+// splitting K (1, 2, 4 or 8).
+constexpr int kWarpMmaMaxM = 16;
+int gemv_mma_groups(int M);
+cudaError_t gemv_mma_prepare(int nh, int ks, int dtype, int* blocks_per_sm);
+cudaError_t launch_gemv_mma(int dtype, int ks, const GemvParams& p, int grid, cudaStream_t stream);
 
 // Fused attention forward -------------------------------------------------
 // O = softmax(scale * Q K^T (masked)) V per (batch, head); Q, K, V, O are

@@ -37,6 +37,8 @@
 //     with constant weights (plan flag GEMM_B_CONST) each warp issues its first
 //     W loads before waiting for the previous kernel of the stream, whose
 //     output may be this layer's X.
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -316,6 +318,186 @@ GemvFn kernel_for(int mt, int dtype) {
     return nullptr;
 }
 
+// ---- 2 <= M <= 16: weight streaming with warp-level tensor-core MMAs ----
+//
+// With a few tokens every weight element still feeds only M multiply-adds, so
+// the layer is bound by streaming W; beyond a couple of tokens the CUDA
+// cores' FMA rate no longer keeps up with HBM, but one warp-level mma.sync
+// m16n8k16 (16 weight rows x 8 tokens x 16 k) does 2048 of them.  The kernel
+// keeps the GEMV's structure -- plain 16-byte loads straight into registers,
+// no staging, no cluster, nothing to set up -- which is what a layer that
+// streams for a few microseconds needs; the CTA-level tensor-core kernel
+// spends ~6 us per launch on its pipeline fill, split-K reduction and set-up.
+// Measured on GB300 at 4096 -> 14336: 0.90 of HBM for M = 2 and 4 (the
+// tensor-core small-M kernel 0.78); with 9 to 16 tokens the second MMA per
+// k-step makes it bound by the warp-level MMA rate (M = 16: 31 against 23
+// us), so the dispatcher takes it up to M = 8.
+//
+// A warp owns 16 rows of W (rows g and g + 8 for lane group g = lane / 4) and
+// a k-slice; lane q = lane % 4 of a group reads the 16-byte pieces at
+// k = k0 + 8 q of its two rows and of tokens g and g + 8 of X.  A sum over k
+// does not depend on the order of its terms, so these eight k-values of a
+// lane are handed to two MMAs as their k-slots 2q, 2q + 1 (first two values)
+// and 2q + 8, 2q + 9 (next two), and so on, identically for W and X: every
+// slot of an MMA pairs W and X at the same k.  The warps of a CTA split K
+// (KS ways) and add their fp32 tiles through shared memory in a fixed order.
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+template <typename InT>
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    if constexpr (std::is_same<InT, __nv_bfloat16>::value)
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NH: groups of 8 tokens held (1: M <= 8, 2: M <= 16); U: 32-k chunks per
+// lane in flight; KS: warps sharing a row group (k-slices), RG = 8 / KS row
+// groups per CTA.
+template <int NH, int U, int KS, typename InT, typename OutT>
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_mma_kernel(const GemvParams p) {
+    constexpr int RG = kWarps / KS;
+    __shared__ float red[kWarps][16 * 16];     // [warp][row * 16 + token]
+    const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31u);
+    const int g = lane >> 2, q = lane & 3;
+    const int rgl = warp / KS, ks = warp - (warp / KS) * KS;
+    const int M = p.M, N = p.N, K = p.K;
+    const int G = (N + 15) / 16;
+    const int kc = ((K + KS - 1) / KS + 31) / 32 * 32;   // k per slice, a multiple of 32
+    const int kb = ks * kc, ke = min(K, kb + kc);
+    const char* const W = static_cast<const char*>(p.W);
+    const char* const X = static_cast<const char*>(p.X);
+    const int64_t ldw = p.ldw * 2, ldx = p.ldx * 2;
+    // tokens g, g + 8 of X (zeros past M)
+    const bool x0ok = g < M, x1ok = NH == 2 && g + 8 < M;
+    const char* const x0row = X + (int64_t)g * ldx;
+    const char* const x1row = X + (int64_t)(g + 8) * ldx;
+
+    grid_launch_dependents();
+    bool waited = false;
+    if (!p.w_prefetch) {
+        grid_dependency_wait();
+        waited = true;
+    }
+    // one 16-byte piece of a row at element k, zeros where [k, k + 8) leaves [kb, ke)
+    auto piece = [&](const char* row, bool ok, int k, bool stream) -> uint4 {
+        if (!ok || k >= ke) return make_uint4(0u, 0u, 0u, 0u);
+        if (k + 8 <= ke) return stream ? ld_stream16(row + (int64_t)k * 2) : ld_keep16(row + (int64_t)k * 2);
+        return ld_tail16<2>(row, k, ke);
+    };
+    for (int blk = blockIdx.x; blk * RG < G; blk += gridDim.x) {
+        const int grp = blk * RG + rgl;
+        const int n0 = grp * 16;
+        float acc[NH][4];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
+        if (grp < G) {                          // warp-uniform
+            const bool w0ok = n0 + g < N, w1ok = n0 + g + 8 < N;
+            const char* const w0row = W + (int64_t)(n0 + g) * ldw;
+            const char* const w1row = W + (int64_t)(n0 + g + 8) * ldw;
+            for (int k0 = kb; k0 < ke; k0 += 32 * U) {
+                uint4 wa[U], wb[U], xa[U], xb[U];
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    const int k = k0 + 32 * i + 8 * q;
+                    wa[i] = piece(w0row, w0ok, k, true);
+                    wb[i] = piece(w1row, w1ok, k, true);
+                }
+                if (!waited) {                  // the first W loads are in flight during the wait
+                    grid_dependency_wait();
+                    waited = true;
+                }
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    const int k = k0 + 32 * i + 8 * q;
+                    xa[i] = piece(x0row, x0ok, k, false);
+                    xb[i] = NH == 2 ? piece(x1row, x1ok, k, false) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {   // k-values 4h .. 4h + 3 of the lane's piece
+                        const uint32_t a0 = u4_at(wa[i], 2 * h), a2 = u4_at(wa[i], 2 * h + 1);
+                        const uint32_t a1 = u4_at(wb[i], 2 * h), a3 = u4_at(wb[i], 2 * h + 1);
+                        mma_16816<InT>(acc[0], a0, a1, a2, a3, u4_at(xa[i], 2 * h), u4_at(xa[i], 2 * h + 1));
+                        if constexpr (NH == 2)
+                            mma_16816<InT>(acc[1], a0, a1, a2, a3, u4_at(xb[i], 2 * h), u4_at(xb[i], 2 * h + 1));
+                    }
+                }
+            }
+        }
+        if (!waited) {                          // a CTA whose warps had no rows
+            grid_dependency_wait();
+            waited = true;
+        }
+        // fragment -> [row][token]: c0, c1 row g, tokens 2q, 2q + 1 (+ 8 h); c2, c3 row g + 8
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = 8 * h + 2 * q;
+            const float* c = acc[h < NH ? h : 0];
+            const bool live = h < NH;
+            red[warp][g * 16 + t] = live ? c[0] : 0.0f;
+            red[warp][g * 16 + t + 1] = live ? c[1] : 0.0f;
+            red[warp][(g + 8) * 16 + t] = live ? c[2] : 0.0f;
+            red[warp][(g + 8) * 16 + t + 1] = live ? c[3] : 0.0f;
+        }
+        __syncthreads();
+        // thread i: output (row i % 16, token i / 16) of each row group of the CTA,
+        // its k-slices added in slice order, then the epilogue
+        const int row = (int)(threadIdx.x & 15u), tok = (int)(threadIdx.x >> 4);
+        for (int r = 0; r < RG; ++r) {
+            const int n = (blk * RG + r) * 16 + row;
+            if (n < N && tok < M) {
+                float t = 0.0f;
+#pragma unroll
+                for (int j = 0; j < KS; ++j) t += red[r * KS + j][row * 16 + tok];
+                if (p.epi & EPI_ALPHA) t *= p.ex.alpha;
+                if (p.epi & EPI_SCALE) t *= vec_f32<InT>(reinterpret_cast<const InT*>(p.ex.scale)[n]);
+                if (p.epi & EPI_BIAS) t += vec_f32<InT>(reinterpret_cast<const InT*>(p.bias)[n]);
+                if (p.epi & EPI_BETA)
+                    t += p.ex.beta * y_f32(reinterpret_cast<const OutT*>(p.ex.c_old)[(int64_t)tok * p.ex.ldc_old + n]);
+                if (p.epi & EPI_RELU) t = fmaxf(t, 0.0f);
+                reinterpret_cast<OutT*>(p.Y)[(int64_t)tok * p.ldy + n] = y_cvt(t, (OutT*)nullptr);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int NH, int KS>
+GemvFn mma_kernel_for(int dtype) {
+    switch (dtype) {
+        case DT_BF16_F32: return gemv_mma_kernel<NH, 4, KS, __nv_bfloat16, float>;
+        case DT_BF16_BF16: return gemv_mma_kernel<NH, 4, KS, __nv_bfloat16, __nv_bfloat16>;
+        case DT_F16_F32: return gemv_mma_kernel<NH, 4, KS, __half, float>;
+        case DT_F16_F16: return gemv_mma_kernel<NH, 4, KS, __half, __half>;
+    }
+    return nullptr;
+}
+
+GemvFn mma_kernel_for(int nh, int ks, int dtype) {
+#define GB300_KS(NHV) \
+    switch (ks) { \
+        case 1: return mma_kernel_for<NHV, 1>(dtype); \
+        case 2: return mma_kernel_for<NHV, 2>(dtype); \
+        case 4: return mma_kernel_for<NHV, 4>(dtype); \
+        case 8: return mma_kernel_for<NHV, 8>(dtype); \
+    }
+    if (nh == 1) { GB300_KS(1) } else if (nh == 2) { GB300_KS(2) }
+#undef GB300_KS
+    return nullptr;
+}
+
 }  // namespace
 
 int gemv_tokens_held(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 0)); }
@@ -328,6 +510,30 @@ cudaError_t gemv_prepare(int M, int dtype, int* blocks_per_sm) {
 
 cudaError_t launch_gemv(int dtype, const GemvParams& p, int grid, cudaStream_t stream) {
     GemvFn fn = kernel_for(gemv_tokens_held(p.M), dtype);
+    if (fn == nullptr || grid < 1) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+int gemv_mma_groups(int M) { return M <= 8 ? 1 : (M <= 16 ? 2 : 0); }
+
+cudaError_t gemv_mma_prepare(int nh, int ks, int dtype, int* blocks_per_sm) {
+    GemvFn fn = mma_kernel_for(nh, ks, dtype);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kGemvThreads, 0);
+}
+
+cudaError_t launch_gemv_mma(int dtype, int ks, const GemvParams& p, int grid, cudaStream_t stream) {
+    GemvFn fn = mma_kernel_for(gemv_mma_groups(p.M), ks, dtype);
     if (fn == nullptr || grid < 1) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

@@ -23,9 +23,11 @@ FP8_DTYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
 B_KN, B_NK, B_CONST, A_KM = 0, 1, 2, 8
 OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY = 1, 2, 3, 4, 5
 OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES, OPT_LOG, OPT_GEMV_MAX_M, OPT_STREAM_K = 6, 7, 9, 10, 11
+OPT_WARP_MMA_MAX_M = 12
 OPTIONS = (OPT_GROUP_M, OPT_TAIL_SPLIT, OPT_K_SNAKE, OPT_PDL, OPT_L2_POLICY, OPT_SKINNY_SPLITS, OPT_SKINNY_STAGES,
-           OPT_LOG, OPT_GEMV_MAX_M, OPT_STREAM_K)
+           OPT_LOG, OPT_GEMV_MAX_M, OPT_STREAM_K, OPT_WARP_MMA_MAX_M)
 KERNEL_AUTO, KERNEL_TC_PAIR, KERNEL_TC_SINGLE, KERNEL_FILL, KERNEL_SKINNY, KERNEL_GEMV = 0, 1, 2, 3, 4, 5
+KERNEL_WARP_MMA = 6
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_NO_MEMORY = (
     0, -1, -2, -3, -4, -5, -6)
 

@@ -103,6 +103,9 @@ typedef enum {
 #define GEMM_KERNEL_FILL 3      /* K == 0: epilogue of an empty sum */
 #define GEMM_KERNEL_SKINNY 4    /* small-M Linear layer (weight streaming, tensor cores) */
 #define GEMM_KERNEL_GEMV 5      /* M <= 4, B stored N x K: CUDA-core GEMV (weight streaming; auto for M = 1) */
+/* 2 <= M <= 16, 16-bit operands, B stored N x K: weight streaming with
+ * warp-level tensor-core MMAs (mma.sync), no staging (auto for 2 <= M <= 8) */
+#define GEMM_KERNEL_WARP_MMA 6
 
 /* Return codes. */
 #define GEMM_OK 0
@@ -293,6 +296,7 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
 #define GEMM_OPT_SKINNY_STAGES 7   /* small-M kernel ring depth: 0 = automatic (default), 2..8 */
 #define GEMM_OPT_LOG 9             /* 0/1: one line per launch on stderr (default 0) */
 #define GEMM_OPT_GEMV_MAX_M 10     /* M up to which the CUDA-core GEMV is chosen, 0..4 (default 1) */
+#define GEMM_OPT_WARP_MMA_MAX_M 12 /* M up to which the warp-MMA kernel is chosen, 0..16 (default 8) */
 /* Stream-K on the tensor-core kernels: in a launch of at least one full wave
  * of tiles, the tiles of the last, partial wave are split by k over the
  * workers so every worker carries the same work; the value is the fewest

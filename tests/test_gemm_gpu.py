@@ -122,7 +122,8 @@ def test_last_wave_split_into_halves_integer_exact(plans, kernel, b_nk, shape):
                                           (G.OPT_K_SNAKE, 0), (G.OPT_PDL, 0), (G.OPT_L2_POLICY, 1),
                                           (G.OPT_L2_POLICY, 2), (G.OPT_SKINNY_SPLITS, 1),
                                           (G.OPT_SKINNY_STAGES, 2), (G.OPT_GEMV_MAX_M, 4), (G.OPT_STREAM_K, 0),
-                                          (G.OPT_STREAM_K, 1)])
+                                          (G.OPT_STREAM_K, 1), (G.OPT_WARP_MMA_MAX_M, 0),
+                                          (G.OPT_WARP_MMA_MAX_M, 8)])
 @pytest.mark.parametrize("shape", [(1300, 530, 200), (4096, 4096, 72), (16, 1000, 1000)])
 def test_scheduling_options_change_no_result(plans, option, value, shape):
     """Every plan option only reschedules work: the results stay exact on
@@ -145,7 +146,8 @@ def test_option_ranges_are_checked(plans):
     p = G.Plan(0)
     for option, bad in [(G.OPT_GROUP_M, -1), (G.OPT_GROUP_M, 1025), (G.OPT_TAIL_SPLIT, 2), (G.OPT_L2_POLICY, 3),
                         (G.OPT_SKINNY_SPLITS, 3), (G.OPT_SKINNY_STAGES, 1), (G.OPT_SKINNY_STAGES, 9),
-                        (G.OPT_GEMV_MAX_M, 5), (G.OPT_STREAM_K, -1), (G.OPT_STREAM_K, 5000), (0, 0), (8, 0),
+                        (G.OPT_GEMV_MAX_M, 5), (G.OPT_STREAM_K, -1), (G.OPT_STREAM_K, 5000),
+                        (G.OPT_WARP_MMA_MAX_M, -1), (G.OPT_WARP_MMA_MAX_M, 17), (0, 0), (8, 0),
                         (99, 0)]:
         before = p.get_option(option) if option in G.OPTIONS else None
         with pytest.raises(G.GemmError):
@@ -206,12 +208,13 @@ def test_skinny_chained_layers_see_previous_outputs(plans, b_const):
 
 
 def test_skinny_is_auto_choice_for_small_m(plans):
-    """2 <= M <= 128: the tensor-core small-M kernel (M = 1 with an N x K
-    weight takes the CUDA-core GEMV, tests/test_gemv_gpu.py)."""
+    """17 <= M <= 128: the tensor-core small-M kernel (M = 1 with an N x K
+    weight takes the CUDA-core GEMV, 2 <= M <= 16 the warp-MMA kernel:
+    tests/test_gemv_gpu.py, tests/test_warp_mma_gpu.py)."""
     p = plans["nk"]
-    A = torch.ones(5, 256, dtype=torch.bfloat16, device="cuda")
+    A = torch.ones(20, 256, dtype=torch.bfloat16, device="cuda")
     W = torch.ones(512, 256, dtype=torch.bfloat16, device="cuda")
-    C = torch.empty(5, 512, device="cuda")
+    C = torch.empty(20, 512, device="cuda")
     p.set_kernel(G.KERNEL_AUTO)
     p.run(A, W, C)
     assert p.status() == 0 and p.last_kernel == G.KERNEL_SKINNY

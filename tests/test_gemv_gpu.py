@@ -180,10 +180,12 @@ def test_gemv_refuses_what_it_does_not_take(plan):
 
 
 def test_dispatch_small_m():
-    """AUTO: M = 1 with an N x K weight -> GEMV; M >= 2, or a K x N weight ->
-    the tensor-core small-M kernel; GEMM_OPT_GEMV_MAX_M moves the threshold."""
+    """AUTO: M = 1 with an N x K weight -> GEMV; a K x N weight, or M >= 2 with
+    the warp-MMA kernel switched off -> the tensor-core small-M kernel;
+    GEMM_OPT_GEMV_MAX_M moves the threshold."""
     with G.Plan(0, "nk") as p, G.Plan(0, "kn") as pk:
         assert p.get_option(G.OPT_GEMV_MAX_M) == 1
+        p.set_option(G.OPT_WARP_MMA_MAX_M, 0)
         w = torch.ones(512, 256, dtype=torch.bfloat16, device="cuda")
         for M, want in [(1, G.KERNEL_GEMV), (2, G.KERNEL_SKINNY), (5, G.KERNEL_SKINNY)]:
             A = torch.ones(M, 256, dtype=torch.bfloat16, device="cuda")
