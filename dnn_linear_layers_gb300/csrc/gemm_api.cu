@@ -56,7 +56,7 @@ struct gemm_plan {
     // M = 4 19.2 us against 22.3 on the tensor-core small-M kernel, M = 16 31.3
     // against 22.7)
     int warp_mma_max_m = 8;
-    int gemv_mma_blocks[2][4][4] = {};   // co-resident warp-MMA CTAs per SM: [groups - 1][log2 ks][dtype]
+    int gemv_mma_blocks[2][4][8] = {};   // co-resident warp-MMA CTAs per SM: [groups - 1][log2 ks][dtype]
     int gemv_blocks[3][kNumDtypes] = {};   // co-resident GEMV CTAs per SM, by tokens held (1, 2, 4)
     int smem_per_sm = 0;          // shared memory of one SM (bytes)
     int smem_reserved = 0;        // shared memory the system reserves per CTA (bytes)
@@ -418,7 +418,7 @@ int run_gemv_mma(gemm_plan* p, int64_t M, int64_t N, int64_t K, const void* X, i
                  int64_t ldw, const void* bias, void* Y, int64_t ldy, uint32_t epi, const EpiArgs& ex, int dtype,
                  cudaStream_t stream) {
     const int nh = gemv_mma_groups((int)M);
-    if (nh == 0 || dtype >= 4) return GEMM_ERR_UNSUPPORTED;
+    if (nh == 0 || dtype > DT_E5M2_BF16) return GEMM_ERR_UNSUPPORTED;
     const int64_t groups = (N + 15) / 16;
     const int warps = kGemvThreads / 32;
     int j = 0;
@@ -520,13 +520,11 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags) {
             e = gemv_prepare(1 << i, dt, &p->gemv_blocks[i][dt]);
             if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
         }
-        if (dt < 4) {                              // 16-bit operand types
-            for (int nh = 1; nh <= 2; ++nh)
-                for (int j = 0; j < 4; ++j) {
-                    e = gemv_mma_prepare(nh, 1 << j, dt, &p->gemv_mma_blocks[nh - 1][j][dt]);
-                    if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
-                }
-        }
+        for (int nh = 1; nh <= 2; ++nh)
+            for (int j = 0; j < 4; ++j) {
+                e = gemv_mma_prepare(nh, 1 << j, dt, &p->gemv_mma_blocks[nh - 1][j][dt]);
+                if (e != cudaSuccess) { cudaGetLastError(); delete p; return GEMM_ERR_CUDA; }
+            }
     }
     p->smem_per_sm = (int)prop.sharedMemPerMultiprocessor;
     p->smem_reserved = (int)prop.reservedSharedMemPerBlock;
@@ -739,8 +737,8 @@ int run_impl(gemm_plan* p, bool b_nk, int64_t M, int64_t N, int64_t K, const voi
     // CUDA-core GEMV also needs the weight stored N x K
     const bool tf32 = dtype_is_tf32(dtype);
     const bool small_ok = !conv && !tf32 && !a_km;
-    // the warp-MMA kernel: 16-bit operands, an N x K weight, M <= 16
-    const bool mma_ok = small_ok && b_nk && !fp8;
+    // the warp-MMA kernel: 16-bit or fp8 operands, an N x K weight, M <= 16
+    const bool mma_ok = small_ok && b_nk;
     int kernel = p->forced_kernel;
     if (kernel == GEMM_KERNEL_AUTO)
         kernel = (small_ok && b_nk && M <= p->gemv_max_m) ? GEMM_KERNEL_GEMV

@@ -180,7 +180,7 @@ constexpr int kGemvMaxM = 4;
 int gemv_tokens_held(int M);
 cudaError_t gemv_prepare(int M, int dtype, int* blocks_per_sm);
 cudaError_t launch_gemv(int dtype, const GemvParams& p, int grid, cudaStream_t stream);
-// Warp-MMA small-M kernel (16-bit operands, 2 <= M <= 16, W stored N x K):
+// Warp-MMA small-M kernel (16-bit or fp8 operands, 2 <= M <= 16, W stored N x K):
 // groups of 8 tokens held (1 or 2; 0 if M > 16); ks = warps of a CTA
 // splitting K (1, 2, 4 or 8).
 constexpr int kWarpMmaMaxM = 16;

@@ -234,20 +234,20 @@ gemv_kernel(const GemvParams p) {
                         }
                     }
                 }
-                continue;
-            }
+            } else {
 #pragma unroll
-            for (int i = 0; i < U; ++i) {
+                for (int i = 0; i < U; ++i) {
 #pragma unroll
-                for (int j = 0; j < O::kPairs; ++j) {
-                    uint64_t xp[MT];
+                    for (int j = 0; j < O::kPairs; ++j) {
+                        uint64_t xp[MT];
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) xp[m] = O::pair(x[m][i], j);
+                        for (int m = 0; m < MT; ++m) xp[m] = O::pair(x[m][i], j);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint64_t wp = O::pair(w[r][i], j);
+                        for (int r = 0; r < R; ++r) {
+                            const uint64_t wp = O::pair(w[r][i], j);
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) acc[r][m] = f2_fma(wp, xp[m], acc[r][m]);
+                            for (int m = 0; m < MT; ++m) acc[r][m] = f2_fma(wp, xp[m], acc[r][m]);
+                        }
                     }
                 }
             }
@@ -345,39 +345,47 @@ __device__ __forceinline__ uint32_t u4_at(const uint4& v, int j) {
     return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-template <typename InT>
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    if constexpr (std::is_same<InT, __nv_bfloat16>::value)
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    else
-        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                     : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// One warp-level MMA, 16 weight rows x 8 tokens: m16n8k16 for 16-bit
+// operands (OPK 0 bf16, 1 fp16), m16n8k32 for fp8 codes (OPK 2 e4m3, 3 e5m2).
+// Per lane, a0 / a2 hold row g and a1 / a3 row g + 8 at the lane's first and
+// second k-slot group, b0 / b1 the same k-slot groups of token g.
+template <int OPK>
+__device__ __forceinline__ void mma_warp(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+#define GB300_MMA(SHAPE_TYPES)                                                                              \
+    asm volatile("mma.sync.aligned." SHAPE_TYPES " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};" \
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])                                            \
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1))
+    if constexpr (OPK == 0) GB300_MMA("m16n8k16.row.col.f32.bf16.bf16.f32");
+    else if constexpr (OPK == 1) GB300_MMA("m16n8k16.row.col.f32.f16.f16.f32");
+    else if constexpr (OPK == 2) GB300_MMA("m16n8k32.row.col.f32.e4m3.e4m3.f32");
+    else GB300_MMA("m16n8k32.row.col.f32.e5m2.e5m2.f32");
+#undef GB300_MMA
 }
 
-// NH: groups of 8 tokens held (1: M <= 8, 2: M <= 16); U: 32-k chunks per
-// lane in flight; KS: warps sharing a row group (k-slices), RG = 8 / KS row
-// groups per CTA.
-template <int NH, int U, int KS, typename InT, typename OutT>
+// NH: groups of 8 tokens held (1: M <= 8, 2: M <= 16); U: chunks per lane in
+// flight (a chunk is 4 pieces of 16 bytes across a lane group: 32 k of 16-bit
+// or 64 k of fp8 values); KS: warps sharing a row group (k-slices), RG = 8 / KS
+// row groups per CTA; OPK: operand kind as in mma_warp; VecT: type of the bias
+// and scale vectors.
+template <int NH, int U, int KS, int OPK, typename VecT, typename OutT>
 __global__ void __launch_bounds__(kGemvThreads)
 gemv_mma_kernel(const GemvParams p) {
     constexpr int RG = kWarps / KS;
+    constexpr int ES = OPK >= 2 ? 1 : 2;       // bytes per element
+    constexpr int kPer = 16 / ES;              // k-values per 16-byte piece
+    constexpr int kChunk = 4 * kPer;           // k-values per chunk (a lane group's four pieces)
     __shared__ float red[kWarps][16 * 16];     // [warp][row * 16 + token]
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31u);
     const int g = lane >> 2, q = lane & 3;
     const int rgl = warp / KS, ks = warp - (warp / KS) * KS;
     const int M = p.M, N = p.N, K = p.K;
     const int G = (N + 15) / 16;
-    const int kc = ((K + KS - 1) / KS + 31) / 32 * 32;   // k per slice, a multiple of 32
+    const int kc = ((K + KS - 1) / KS + kChunk - 1) / kChunk * kChunk;   // k per slice
     const int kb = ks * kc, ke = min(K, kb + kc);
     const char* const W = static_cast<const char*>(p.W);
     const char* const X = static_cast<const char*>(p.X);
-    const int64_t ldw = p.ldw * 2, ldx = p.ldx * 2;
+    const int64_t ldw = p.ldw * ES, ldx = p.ldx * ES;
     // tokens g, g + 8 of X (zeros past M)
     const bool x0ok = g < M, x1ok = NH == 2 && g + 8 < M;
     const char* const x0row = X + (int64_t)g * ldx;
@@ -389,11 +397,11 @@ gemv_mma_kernel(const GemvParams p) {
         grid_dependency_wait();
         waited = true;
     }
-    // one 16-byte piece of a row at element k, zeros where [k, k + 8) leaves [kb, ke)
+    // one 16-byte piece of a row at element k, zeros where [k, k + kPer) leaves [kb, ke)
     auto piece = [&](const char* row, bool ok, int k, bool stream) -> uint4 {
         if (!ok || k >= ke) return make_uint4(0u, 0u, 0u, 0u);
-        if (k + 8 <= ke) return stream ? ld_stream16(row + (int64_t)k * 2) : ld_keep16(row + (int64_t)k * 2);
-        return ld_tail16<2>(row, k, ke);
+        if (k + kPer <= ke) return stream ? ld_stream16(row + (int64_t)k * ES) : ld_keep16(row + (int64_t)k * ES);
+        return ld_tail16<ES>(row, k, ke);
     };
     for (int blk = blockIdx.x; blk * RG < G; blk += gridDim.x) {
         const int grp = blk * RG + rgl;
@@ -405,11 +413,11 @@ gemv_mma_kernel(const GemvParams p) {
             const bool w0ok = n0 + g < N, w1ok = n0 + g + 8 < N;
             const char* const w0row = W + (int64_t)(n0 + g) * ldw;
             const char* const w1row = W + (int64_t)(n0 + g + 8) * ldw;
-            for (int k0 = kb; k0 < ke; k0 += 32 * U) {
+            for (int k0 = kb; k0 < ke; k0 += kChunk * U) {
                 uint4 wa[U], wb[U], xa[U], xb[U];
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
-                    const int k = k0 + 32 * i + 8 * q;
+                    const int k = k0 + kChunk * i + kPer * q;
                     wa[i] = piece(w0row, w0ok, k, true);
                     wb[i] = piece(w1row, w1ok, k, true);
                 }
@@ -419,19 +427,19 @@ gemv_mma_kernel(const GemvParams p) {
                 }
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
-                    const int k = k0 + 32 * i + 8 * q;
+                    const int k = k0 + kChunk * i + kPer * q;
                     xa[i] = piece(x0row, x0ok, k, false);
                     xb[i] = NH == 2 ? piece(x1row, x1ok, k, false) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {   // k-values 4h .. 4h + 3 of the lane's piece
+                    for (int h = 0; h < 2; ++h) {   // words 2h, 2h + 1 of the lane's piece
                         const uint32_t a0 = u4_at(wa[i], 2 * h), a2 = u4_at(wa[i], 2 * h + 1);
                         const uint32_t a1 = u4_at(wb[i], 2 * h), a3 = u4_at(wb[i], 2 * h + 1);
-                        mma_16816<InT>(acc[0], a0, a1, a2, a3, u4_at(xa[i], 2 * h), u4_at(xa[i], 2 * h + 1));
+                        mma_warp<OPK>(acc[0], a0, a1, a2, a3, u4_at(xa[i], 2 * h), u4_at(xa[i], 2 * h + 1));
                         if constexpr (NH == 2)
-                            mma_16816<InT>(acc[1], a0, a1, a2, a3, u4_at(xb[i], 2 * h), u4_at(xb[i], 2 * h + 1));
+                            mma_warp<OPK>(acc[1], a0, a1, a2, a3, u4_at(xb[i], 2 * h), u4_at(xb[i], 2 * h + 1));
                     }
                 }
             }
@@ -462,8 +470,8 @@ gemv_mma_kernel(const GemvParams p) {
 #pragma unroll
                 for (int j = 0; j < KS; ++j) t += red[r * KS + j][row * 16 + tok];
                 if (p.epi & EPI_ALPHA) t *= p.ex.alpha;
-                if (p.epi & EPI_SCALE) t *= vec_f32<InT>(reinterpret_cast<const InT*>(p.ex.scale)[n]);
-                if (p.epi & EPI_BIAS) t += vec_f32<InT>(reinterpret_cast<const InT*>(p.bias)[n]);
+                if (p.epi & EPI_SCALE) t *= vec_f32<VecT>(reinterpret_cast<const VecT*>(p.ex.scale)[n]);
+                if (p.epi & EPI_BIAS) t += vec_f32<VecT>(reinterpret_cast<const VecT*>(p.bias)[n]);
                 if (p.epi & EPI_BETA)
                     t += p.ex.beta * y_f32(reinterpret_cast<const OutT*>(p.ex.c_old)[(int64_t)tok * p.ex.ldc_old + n]);
                 if (p.epi & EPI_RELU) t = fmaxf(t, 0.0f);
@@ -477,10 +485,15 @@ gemv_mma_kernel(const GemvParams p) {
 template <int NH, int KS>
 GemvFn mma_kernel_for(int dtype) {
     switch (dtype) {
-        case DT_BF16_F32: return gemv_mma_kernel<NH, 4, KS, __nv_bfloat16, float>;
-        case DT_BF16_BF16: return gemv_mma_kernel<NH, 4, KS, __nv_bfloat16, __nv_bfloat16>;
-        case DT_F16_F32: return gemv_mma_kernel<NH, 4, KS, __half, float>;
-        case DT_F16_F16: return gemv_mma_kernel<NH, 4, KS, __half, __half>;
+        case DT_BF16_F32: return gemv_mma_kernel<NH, 4, KS, 0, __nv_bfloat16, float>;
+        case DT_BF16_BF16: return gemv_mma_kernel<NH, 4, KS, 0, __nv_bfloat16, __nv_bfloat16>;
+        case DT_F16_F32: return gemv_mma_kernel<NH, 4, KS, 1, __half, float>;
+        case DT_F16_F16: return gemv_mma_kernel<NH, 4, KS, 1, __half, __half>;
+        // fp8 codes; bf16 bias / scale
+        case DT_E4M3_F32: return gemv_mma_kernel<NH, 4, KS, 2, __nv_bfloat16, float>;
+        case DT_E4M3_BF16: return gemv_mma_kernel<NH, 4, KS, 2, __nv_bfloat16, __nv_bfloat16>;
+        case DT_E5M2_F32: return gemv_mma_kernel<NH, 4, KS, 3, __nv_bfloat16, float>;
+        case DT_E5M2_BF16: return gemv_mma_kernel<NH, 4, KS, 3, __nv_bfloat16, __nv_bfloat16>;
     }
     return nullptr;
 }

@@ -103,7 +103,7 @@ typedef enum {
 #define GEMM_KERNEL_FILL 3      /* K == 0: epilogue of an empty sum */
 #define GEMM_KERNEL_SKINNY 4    /* small-M Linear layer (weight streaming, tensor cores) */
 #define GEMM_KERNEL_GEMV 5      /* M <= 4, B stored N x K: CUDA-core GEMV (weight streaming; auto for M = 1) */
-/* 2 <= M <= 16, 16-bit operands, B stored N x K: weight streaming with
+/* 2 <= M <= 16, 16-bit or fp8 operands, B stored N x K: weight streaming with
  * warp-level tensor-core MMAs (mma.sync), no staging (auto for 2 <= M <= 8) */
 #define GEMM_KERNEL_WARP_MMA 6
 

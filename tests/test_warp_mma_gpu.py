@@ -1,6 +1,6 @@
-"""GPU parity tests of the warp-MMA small-M kernel (2 <= M <= 16, 16-bit
-operands, weight stored N x K; chosen automatically up to M = 8) through the
-C ABI against the float64 oracle.
+"""GPU parity tests of the warp-MMA small-M kernel (2 <= M <= 16, 16-bit or
+fp8 operands, weight stored N x K; chosen automatically up to M = 8) through
+the C ABI against the float64 oracle.
 
 Integer inputs must match exactly (every partial sum is an integer below
 2^24, exact in fp32 in any order); float inputs within 1e-3 * sum|a b| + 1e-6
@@ -164,8 +164,8 @@ def test_warp_mma_refuses_what_it_does_not_take(plan):
     with pytest.raises(G.GemmError) as e:
         plan.run(x, w, y)                                       # M = 17 > 16
     assert e.value.code == G.ERR_UNSUPPORTED
-    with pytest.raises(G.GemmError) as e:                       # fp8 operands
-        plan.run(x[:4].to(torch.float8_e4m3fn), w.to(torch.float8_e4m3fn), y[:4])
+    with pytest.raises(G.GemmError) as e:                       # tf32 operands
+        plan.run(x[:4].float(), w.float(), y[:4])
     assert e.value.code == G.ERR_UNSUPPORTED
     with G.Plan(0, "kn") as pk:                                  # K x N weight
         pk.set_kernel(G.KERNEL_WARP_MMA)
@@ -175,8 +175,8 @@ def test_warp_mma_refuses_what_it_does_not_take(plan):
 
 
 def test_dispatch_warp_mma():
-    """AUTO: M = 1 -> GEMV, 2 <= M <= 8 with a 16-bit N x K weight -> warp-MMA,
-    M = 9, fp8 or a K x N weight -> the tensor-core small-M kernel;
+    """AUTO: M = 1 -> GEMV, 2 <= M <= 8 with a 16-bit or fp8 N x K weight ->
+    warp-MMA, M = 9 or a K x N weight -> the tensor-core small-M kernel;
     GEMM_OPT_WARP_MMA_MAX_M moves the threshold (up to 16)."""
     with G.Plan(0, "nk") as p:
         assert p.get_option(G.OPT_WARP_MMA_MAX_M) == 8
@@ -190,7 +190,7 @@ def test_dispatch_warp_mma():
         A8 = torch.ones(4, 256, device="cuda").to(torch.float8_e4m3fn)
         C = torch.empty(4, 512, device="cuda")
         p.run(A8, w.to(torch.float8_e4m3fn), C)
-        assert p.status() == 0 and p.last_kernel == G.KERNEL_SKINNY and torch.all(C == 256.0)
+        assert p.status() == 0 and p.last_kernel == G.KERNEL_WARP_MMA and torch.all(C == 256.0)
         p.set_option(G.OPT_WARP_MMA_MAX_M, 4)
         A = torch.ones(5, 256, dtype=torch.bfloat16, device="cuda")
         C = torch.empty(5, 512, device="cuda")
@@ -208,3 +208,57 @@ def test_dispatch_warp_mma():
         C = torch.empty(4, 512, device="cuda")
         pk.run(A, torch.ones(256, 512, dtype=torch.bfloat16, device="cuda"), C)
         assert pk.status() == 0 and pk.last_kernel == G.KERNEL_SKINNY
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(2, 1000, 4096), (5, 300, 2000), (8, 129, 33), (16, 520, 1000), (3, 64, 4111),
+                                   (8, 14336, 4096)])
+def test_warp_mma_fp8_integer_exact(plan, fmt, out, M, N, K):
+    """fp8 codes through m16n8k32: 16 k-values per 16-byte piece, ragged K
+    (tails inside a piece), bf16 bias, exact on small integers."""
+    f8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}[fmt]
+    A = int_bf16((M, K), M + K).to(f8)
+    W = int_bf16((N, K), N + K).to(f8)
+    bias = int_bf16((N,), N, lo=-8, hi=8)
+    C = torch.full((M, N), float("nan"), dtype=out, device="cuda")
+    plan.set_kernel(G.KERNEL_WARP_MMA)
+    plan.run(A.cuda(), W.cuda(), C, bias.cuda(), True)
+    assert plan.status() == 0 and plan.last_kernel == G.KERNEL_WARP_MMA
+    ref = oracle.gemm(A, W, bias=bias, relu=True, b_nk=True)
+    want = oracle.bf16_round(ref) if out == torch.bfloat16 else ref
+    assert np.array_equal(C.double().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("M", [2, 16])
+def test_warp_mma_fp8_float_with_scales(plan, M):
+    N, K = 700, 1024
+    g = torch.Generator().manual_seed(M)
+    a_scale, b_scale = 0.5, 0.125
+    A = (torch.randn(M, K, generator=g) / a_scale).to(torch.float8_e4m3fn)
+    W = (torch.randn(N, K, generator=g) / b_scale).to(torch.float8_e4m3fn)
+    C = torch.empty(M, N, device="cuda")
+    plan.set_kernel(G.KERNEL_WARP_MMA)
+    plan.run(A.cuda(), W.cuda(), C, alpha=a_scale * b_scale)
+    assert plan.status() == 0 and plan.last_kernel == G.KERNEL_WARP_MMA
+    C_ref, S = oracle.gemm_ex(A, W, alpha=a_scale * b_scale, b_nk=True)
+    ok, worst, _ = oracle.check_close(C.double().cpu().numpy(), C_ref, S)
+    assert ok, f"worst err/bound {worst:.3f}"
+
+
+@pytest.mark.parametrize("K", [1, 15, 16, 17, 263, 2047])
+def test_warp_mma_fp8_reads_nothing_past_k(plan, K):
+    """fp8 rows with 16-byte aligned pitches longer than K, padded with NaN codes."""
+    M, N = 5, 300
+    ld = (K + 15) // 16 * 16 + 16
+    A = int_bf16((M, K), K, lo=-3, hi=3).to(torch.float8_e4m3fn)
+    W = int_bf16((N, K), K + 1, lo=-3, hi=3).to(torch.float8_e4m3fn)
+    Ab = torch.full((M, ld), float("nan")).to(torch.float8_e4m3fn)
+    Wb = torch.full((N, ld), float("nan")).to(torch.float8_e4m3fn)
+    Ab[:, :K] = A
+    Wb[:, :K] = W
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    plan.set_kernel(G.KERNEL_WARP_MMA)
+    plan.run(Ab.cuda()[:, :K], Wb.cuda()[:, :K], C)
+    assert plan.status() == 0 and plan.last_kernel == G.KERNEL_WARP_MMA
+    assert np.array_equal(C.double().cpu().numpy(), oracle.gemm(A, W, b_nk=True))
