@@ -440,7 +440,7 @@ class Workload:
 
 # Decode-like Linear layers timed after the headline in the same process and
 # reported under "secondary" (the memory-bound half of the target).
-SECONDARY = ("linear_m1_4096x14336", "linear_m16_4096x14336")
+SECONDARY = ("linear_m1_4096x14336", "linear_m4_4096x14336", "linear_m16_4096x14336")
 
 
 def secondary_lines(dev, local_rank, args, world):
