@@ -1,8 +1,13 @@
-// GEMV / very-small-M Linear layer on the CUDA cores:
+// Very-small-M Linear layers that stream the weight without staging it:
 //
-//   Y[m][n] = epilogue( sum_k X[m][k] * W[n][k] ),   m < M <= 4, W stored N x K
+//   Y[m][n] = epilogue( sum_k X[m][k] * W[n][k] ),   W stored N x K
 //
-// (a Linear weight, out x in).  With M <= 4 every weight byte feeds at most a
+// (a Linear weight, out x in).  Two kernels: the CUDA-core GEMV below (M <= 4,
+// chosen for M = 1) and, further down, the warp-MMA kernel (2 <= M <= 16,
+// chosen up to M = 8), which keeps the GEMV's loads and replaces its FMAs by
+// warp-level tensor-core MMAs.
+//
+// GEMV.  With M <= 4 every weight byte feeds at most a
 // few multiply-adds (arithmetic intensity about M FLOP per byte: youngju.dev
 // "GEMM to FlashAttention", arithmetic-intensity listing, batch-1 case; CMU
 // 15-418 notes, question 1 on GEMV), so the kernel is bound by streaming W
@@ -117,17 +122,6 @@ template <int E5M2> struct OpFp8 {
         if constexpr (E5M2) asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(c));
         else asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
         return r;
-    }
-    // codes 2j, 2j + 1 of the piece -> f16x2 (exact) -> two fp32 values
-    static __device__ __forceinline__ uint64_t pair(const uint4& v, int j) {
-        const uint32_t u = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
-        const uint16_t c = (uint16_t)((j & 1) ? (u >> 16) : (u & 0xFFFFu));
-        uint32_t h2;
-        if constexpr (E5M2) asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
-        else asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-        __half2 h = *reinterpret_cast<const __half2*>(&h2);
-        const float2 f = __half22float2(h);
-        return f2_pack(f.x, f.y);
     }
 };
 template <> struct Op<2> : OpFp8<0> {};
