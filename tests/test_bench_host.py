@@ -1,6 +1,7 @@
 """Host-side pieces of the benchmark: whole-job throughput over replicas, the
-max-over-ranks timing on a real 2-rank process group (gloo, CPU), and the
-reference arm's rank handling.  No GPU needed."""
+max-over-ranks timing on a real 2-rank process group (gloo, CPU), the
+reference arm's rank handling, and the map from every benchmarked workload to
+the GPU parity tests that run it at its own size.  No GPU needed."""
 import os
 import socket
 import sys
@@ -97,3 +98,64 @@ def test_gemm_oracle_unit_and_operand_types():
     assert abs(bench.PEAK_RATIO["tf32"] - 1.1 / 2.25) < 1e-12
     for name, (M, N, K, lay, *_rest) in bench.WORKLOADS.items():
         assert M > 0 and N > 0 and K > 0 and lay in ("kn", "nk"), name
+
+
+# Every benchmarked workload and the GPU parity tests that run it at its own
+# size (test file, test function): the benchmark publishes no number for a
+# configuration that no parity test covers.
+WORKLOAD_TESTS = {
+    "square8192_bf16": [("test_fullsize_gpu.py", "test_square_8192_bf16"),
+                        ("test_fullsize_gpu.py", "test_square_8192_integer_exact_whole_matrix")],
+    "square4096_bf16": [("test_fullsize_gpu.py", "test_square_sweep_integer_exact"),
+                        ("test_fullsize_gpu.py", "test_square_sweep_float_sampled")],
+    "square2048_bf16": [("test_fullsize_gpu.py", "test_square_sweep_integer_exact")],
+    "square1024_bf16": [("test_fullsize_gpu.py", "test_square_sweep_integer_exact")],
+    "square512_f32": [("test_gemm_gpu.py", "test_config_512_f32_out")],
+    "square8192_nk_bf16": [("test_fullsize_gpu.py", "test_square_nk_weight_layout")],
+    "square4096_nk_bf16": [("test_fullsize_gpu.py", "test_square_nk_weight_layout")],
+    "qkv_8192x4096x12288": [("test_fullsize_gpu.py", "test_transformer_layers")],
+    "ffn_up_8192x4096x14336": [("test_fullsize_gpu.py", "test_transformer_layers")],
+    "ffn_down_8192x14336x4096": [("test_fullsize_gpu.py", "test_transformer_layers")],
+    "conv_im2col_100352x2304x256": [("test_conv_gpu.py", "test_full_conv_config_sampled")],
+    "conv_implicit_32x56x56x256_3x3": [("test_conv_gpu.py", "test_full_conv_config_implicit_sampled")],
+    "conv_pool_32x56x56x256_3x3": [("test_fullsize_gpu.py", "test_pooled_conv_full_size_every_output")],
+    "odd_3000x5000x2048": [("test_fullsize_gpu.py", "test_odd_shapes")],
+    "attention_b4h32s4096d128": [("test_fullsize_gpu.py", "test_attention_full_size_sampled_heads")],
+    "attention_causal_b4h32s4096d128": [("test_fullsize_gpu.py", "test_attention_full_size_sampled_heads")],
+    "attention_b4h32s4096d64": [("test_fullsize_gpu.py", "test_attention_d64_full_size_sampled_heads")],
+    "square8192_e4m3": [("test_fullsize_gpu.py", "test_square_8192_fp8")],
+    "square8192_e5m2": [("test_fullsize_gpu.py", "test_square_8192_fp8")],
+    "square8192_tf32": [("test_fullsize_gpu.py", "test_square_8192_tf32")],
+    "square8192_transa_bf16": [("test_fullsize_gpu.py", "test_square_8192_transposed_a")],
+    "odd_4095": [("test_fullsize_gpu.py", "test_odd_shapes")],
+    "odd_1000": [("test_fullsize_gpu.py", "test_odd_shapes")],
+    "linear_m1_4096x14336": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m16_4096x14336": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m128_4096x14336": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m1_4096x4096": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m2_4096x14336": [("test_warp_mma_gpu.py", "test_warp_mma_decode_layers_every_output")],
+    "linear_m4_4096x14336": [("test_fullsize_gpu.py", "test_decode_linear_layers_m4_every_output"),
+                             ("test_warp_mma_gpu.py", "test_warp_mma_decode_layers_every_output")],
+    "linear_m8_4096x14336": [("test_warp_mma_gpu.py", "test_warp_mma_decode_layers_every_output")],
+    "linear_m4_4096x4096": [("test_fullsize_gpu.py", "test_decode_linear_layers_m4_every_output")],
+    "linear_m16_4096x4096": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m128_4096x4096": [("test_fullsize_gpu.py", "test_decode_linear_layers_every_output")],
+    "linear_m1_4096x14336_e4m3": [("test_fullsize_gpu.py", "test_decode_fp8_layers_every_output")],
+    "linear_m4_4096x14336_e4m3": [("test_fullsize_gpu.py", "test_decode_fp8_layers_every_output")],
+    "linear_m16_4096x14336_e4m3": [("test_fullsize_gpu.py", "test_decode_fp8_layers_every_output")],
+    "linear_m128_4096x14336_e4m3": [("test_fullsize_gpu.py", "test_decode_fp8_layers_every_output")],
+}
+
+
+def test_every_benchmarked_workload_has_a_parity_test_at_its_size():
+    import ast
+    from pathlib import Path
+    here = Path(__file__).resolve().parent
+    assert set(WORKLOAD_TESTS) == set(bench.WORKLOADS), "workload list and parity map disagree"
+    defined = {}
+    for f in {f for tests in WORKLOAD_TESTS.values() for f, _ in tests}:
+        tree = ast.parse((here / f).read_text())
+        defined[f] = {n.name for n in tree.body if isinstance(n, ast.FunctionDef)}
+    for name, tests in WORKLOAD_TESTS.items():
+        for f, fn in tests:
+            assert fn in defined[f], f"{name}: {f}::{fn} does not exist"

@@ -73,6 +73,17 @@ def test_square_8192_bf16(plans):
     freivalds(case, A, B, bias, C)
 
 
+@pytest.mark.parametrize("n", [4096, 8192])
+def test_square_nk_weight_layout(plans, n):
+    """n^3 with B stored N x K (the Linear weight layout), as benchmarked:
+    sampled tile-boundary rows and columns against the oracle, Freivalds on
+    the whole matrix."""
+    case = GemmCase(f"square{n}_nk", n, n, n, b_nk=True, out="bf16", seed=n + 7)
+    A, B, bias, C = run_full(plans, case)
+    check_sampled(case, A, B, bias, C, n_random=8)
+    freivalds(case, A, B, bias, C, trials=1)
+
+
 def test_square_8192_integer_exact_whole_matrix(plans):
     case = GemmCase("square8192_int", 8192, 8192, 8192, out="f32", integer=True, seed=1)
     A, B, bias, C = run_full(plans, case)
