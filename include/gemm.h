@@ -14,20 +14,24 @@
  * (B[k][j] at B + k*ldb + j, ldb >= N) by default; with the plan flag
  * GEMM_B_NK, B is a Linear weight W stored N x K, out x in (B(k, j) = W[j][k]
  * at B + j*ldb + k, ldb >= K) -- the "transb" of the BLAS interface.  C is
- * M x N (ldc >= N).  bias has N elements of the input type.
+ * M x N (ldc >= N).  bias has N elements of the input type (bf16 for fp8 and
+ * tf32 inputs).  With the plan flag GEMM_A_KM, A is stored K x M instead.
  *
- * Numerics.  A, B, bias: bf16 or fp16; products and sums in fp32 (the mixed-
- * precision rule of the same notes, section 2.7: low-precision storage, fp32
- * accumulation); the bias is added in fp32 before the ReLU and the single
- * final cast (round to nearest even) to the output type.  alpha = 1 and
- * beta = 0: C is overwritten, never read.
+ * Numerics.  A, B: bf16, fp16, fp8 (e4m3 / e5m2) or fp32 read as tf32 (see
+ * gemm_dtype_t); products and sums in fp32 (the mixed-precision rule of the
+ * same notes, section 2.7: low-precision storage, fp32 accumulation); the bias
+ * is added in fp32 before the ReLU and the single final cast (round to
+ * nearest even) to the output type.  gemm_run: alpha = 1 and beta = 0, C is
+ * overwritten, never read; gemm_run_ex takes alpha, beta, a per-column scale.
  *
  * Memory.  A, B, bias and C are DEVICE pointers on the plan's device, owned by
  * the caller and never freed by the library.  The plan owns a small device
- * status word and, only when an operand breaks the 16-byte rule of the TMA
- * copies (base address or leading dimension x element size not a multiple of
- * 16 bytes), a workspace into which that operand is packed; the workspace is
- * allocated on first need, grows, and is freed by gemm_plan_destroy.
+ * status block and, only when needed, a workspace: packed copies of operands
+ * that break the 16-byte rule of the TMA copies (base address or leading
+ * dimension x element size not a multiple of 16 bytes), K-major copies of tf32
+ * operands stored MN-major, and the partial tiles of the optional stream-K
+ * split.  The workspace is allocated on first need, grows, and is freed by
+ * gemm_plan_destroy.
  *
  * Asynchrony.  gemm_run enqueues its kernels on `stream` (a cudaStream_t,
  * NULL = legacy default stream) and returns without waiting.  Only
@@ -301,8 +305,8 @@ int64_t gemm_plan_workspace_bytes(gemm_plan_t plan);
  * of tiles, the tiles of the last, partial wave are split by k over the
  * workers so every worker carries the same work; the value is the fewest
  * k-atoms a worker takes (0: off, the last wave runs as N-halves; default
- * 0, off; 8 is a good value).  Split tiles keep fp32 partials in the plan's
- * workspace. */
+ * 0: on GB300 it measured equal or slower than the N-halves).  Split tiles
+ * keep fp32 partials in the plan's workspace. */
 #define GEMM_OPT_STREAM_K 11
 
 /* Set / read a GEMM_OPT_* option.  GEMM_ERR_INVALID_ARG for a NULL plan, an
