@@ -476,34 +476,41 @@ gemv_mma_kernel(const GemvParams p) {
     }
 }
 
-template <int NH, int KS>
+template <int NH, int KS, int U>
 GemvFn mma_kernel_for(int dtype) {
     switch (dtype) {
-        case DT_BF16_F32: return gemv_mma_kernel<NH, 4, KS, 0, __nv_bfloat16, float>;
-        case DT_BF16_BF16: return gemv_mma_kernel<NH, 4, KS, 0, __nv_bfloat16, __nv_bfloat16>;
-        case DT_F16_F32: return gemv_mma_kernel<NH, 4, KS, 1, __half, float>;
-        case DT_F16_F16: return gemv_mma_kernel<NH, 4, KS, 1, __half, __half>;
+        case DT_BF16_F32: return gemv_mma_kernel<NH, U, KS, 0, __nv_bfloat16, float>;
+        case DT_BF16_BF16: return gemv_mma_kernel<NH, U, KS, 0, __nv_bfloat16, __nv_bfloat16>;
+        case DT_F16_F32: return gemv_mma_kernel<NH, U, KS, 1, __half, float>;
+        case DT_F16_F16: return gemv_mma_kernel<NH, U, KS, 1, __half, __half>;
         // fp8 codes; bf16 bias / scale
-        case DT_E4M3_F32: return gemv_mma_kernel<NH, 4, KS, 2, __nv_bfloat16, float>;
-        case DT_E4M3_BF16: return gemv_mma_kernel<NH, 4, KS, 2, __nv_bfloat16, __nv_bfloat16>;
-        case DT_E5M2_F32: return gemv_mma_kernel<NH, 4, KS, 3, __nv_bfloat16, float>;
-        case DT_E5M2_BF16: return gemv_mma_kernel<NH, 4, KS, 3, __nv_bfloat16, __nv_bfloat16>;
+        case DT_E4M3_F32: return gemv_mma_kernel<NH, U, KS, 2, __nv_bfloat16, float>;
+        case DT_E4M3_BF16: return gemv_mma_kernel<NH, U, KS, 2, __nv_bfloat16, __nv_bfloat16>;
+        case DT_E5M2_F32: return gemv_mma_kernel<NH, U, KS, 3, __nv_bfloat16, float>;
+        case DT_E5M2_BF16: return gemv_mma_kernel<NH, U, KS, 3, __nv_bfloat16, __nv_bfloat16>;
     }
     return nullptr;
 }
 
-GemvFn mma_kernel_for(int nh, int ks, int dtype) {
+// u: chunks per lane in flight, 4, or 8 for one group of tokens and k split 8 ways
+GemvFn mma_kernel_for(int nh, int ks, int dtype, int u = 4) {
 #define GB300_KS(NHV) \
     switch (ks) { \
-        case 1: return mma_kernel_for<NHV, 1>(dtype); \
-        case 2: return mma_kernel_for<NHV, 2>(dtype); \
-        case 4: return mma_kernel_for<NHV, 4>(dtype); \
-        case 8: return mma_kernel_for<NHV, 8>(dtype); \
+        case 1: return mma_kernel_for<NHV, 1, 4>(dtype); \
+        case 2: return mma_kernel_for<NHV, 2, 4>(dtype); \
+        case 4: return mma_kernel_for<NHV, 4, 4>(dtype); \
+        case 8: return mma_kernel_for<NHV, 8, 4>(dtype); \
     }
+    if (nh == 1 && ks == 8 && u == 8) return mma_kernel_for<1, 8, 8>(dtype);
+    if (u != 4) return nullptr;
     if (nh == 1) { GB300_KS(1) } else if (nh == 2) { GB300_KS(2) }
 #undef GB300_KS
     return nullptr;
 }
+
+// Co-resident CTAs per SM of the 8-chunk variant, per device and operand type
+// (looked up once; 0 = not yet).
+int g_wide_blocks[16][8];
 
 }  // namespace
 
@@ -540,8 +547,31 @@ cudaError_t gemv_mma_prepare(int nh, int ks, int dtype, int* blocks_per_sm) {
 }
 
 cudaError_t launch_gemv_mma(int dtype, int ks, const GemvParams& p, int grid, cudaStream_t stream) {
-    GemvFn fn = mma_kernel_for(gemv_mma_groups(p.M), ks, dtype);
+    const int nh = gemv_mma_groups(p.M);
+    GemvFn fn = mma_kernel_for(nh, ks, dtype);
     if (fn == nullptr || grid < 1) return cudaErrorInvalidValue;
+    // A layer with no more 16-row groups than the grid has CTAs (every CTA one
+    // group, k split over its 8 warps) runs in a single wave; if the variant
+    // with 8 chunks in flight per lane (more registers, fewer CTAs per SM)
+    // still fits that wave, it hides more load latency: 4096 -> 4096 at M = 4
+    // 6.7 against 8.1 us.  Larger layers need several waves, where the 4-chunk
+    // variant's extra CTAs per SM keep the waves balanced (4096 -> 14336: 19.3
+    // against 24 us for the 8-chunk variant).
+    if (nh == 1 && ks == kWarps && (int64_t)grid * 16 >= p.N && dtype >= 0 && dtype < 8) {
+        int dev = 0, sms = 0;
+        bool ok = cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 16 &&
+                  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+        if (ok) {
+            GemvFn wide = mma_kernel_for(1, kWarps, dtype, 8);
+            int& bps = g_wide_blocks[dev][dtype];
+            if (bps == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, wide, kGemvThreads, 0) != cudaSuccess) {
+                bps = -1;
+                ok = false;
+            }
+            if (bps > 0 && grid <= sms * bps) fn = wide;
+        }
+        if (!ok) cudaGetLastError();   // a failed query only means the 4-chunk variant runs
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
